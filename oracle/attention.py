@@ -1,0 +1,165 @@
+"""Plain double-precision CPU oracle for attention forward and backward.
+
+TEST INFRASTRUCTURE ONLY. This module is the yardstick the CUDA library is
+checked against. It is imported by ``tests/``, by the package's ``smoke()``
+self-check and by the CPU-baseline leg of ``bench.py`` — never by the product
+path, which fails loudly when its CUDA library is missing instead of falling
+back to anything here. It shares no code with the CUDA side: no kernels,
+headers, tables or helpers; the only thing both sides consume is the seeded
+input generator, which holds none of the method's arithmetic.
+
+What is computed (one head at a time, every value widened to float64; the
+N x N probability matrix is materialised, which is exactly what the CUDA
+kernels avoid):
+
+* Forward, "FlashAttention backward" §What the forward left behind and
+  "Lecture 7 — Backward Pass and Validation" §The math:
+  S = scale * Q K^T, masked entries set to -inf; L_i = m_i + log sum_j
+  exp(S_ij - m_i) (natural log, computed before dropout); P = exp(S - L);
+  O = (P o Z / (1 - p)) V with Z the dropout keep-mask.
+* Backward, "FlashAttention backward" §The gradients, and the one scalar that
+  makes them local; "Lecture 7" §The math; "Implementing Flash Attention's
+  Backward Pass in Raw CUDA" §Deriving the gradients, with dropout folded in
+  by the chain rule:
+  dV = (P o Z/(1-p))^T dO; dP = (dO V^T) o Z/(1-p); D_i = sum_k dO_ik O_ik;
+  dS = P o (dP - D); dQ = scale * dS K; dK = scale * dS^T Q.
+* Masks, "Lecture 7" §Mask behaviour: causal keeps j <= i (top-left aligned,
+  square), a window W > 0 keeps j > i - W; both may be on at once.
+  A row with no allowed key has L = -inf, P = 0, O = 0 and zero gradients.
+
+Parity pins (tests that fix this oracle to something other than itself) live
+in ``tests/test_oracle_pins.py``: central finite differences, the D identity,
+zero row sums of dS, closed forms, exact zero flow across mask boundaries, and
+cross-checks against torch's float64 autograd and SDPA. The dropout generator
+is pinned against cuRAND's device Philox on a GPU.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .philox import keep_mask
+
+# Largest probability panel (rows x N, float64) held at once: 256 MiB.
+_PANEL_BYTES = 1 << 28
+
+
+def allowed(rows, N: int, causal: bool, window: int):
+    """Boolean matrix of (query row i, key j) pairs the mask lets through."""
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(N, dtype=np.int64)[None, :]
+    ok = np.ones((i.shape[0], N), dtype=bool)
+    if causal:
+        ok &= j <= i
+    if window > 0:
+        ok &= j > i - window
+    return ok
+
+
+def _panels(N: int):
+    rows = max(1, min(N, _PANEL_BYTES // (8 * max(N, 1))))
+    for r0 in range(0, N, rows):
+        yield r0, min(N, r0 + rows)
+
+
+def _f64(x):
+    return np.asarray(x).astype(np.float64)
+
+
+def _dropout_scale(b, h, H, N, rows, seed, offset, p):
+    """Z / (1 - p) as float64 (1 everywhere when p == 0)."""
+    if p == 0.0:
+        return None
+    z = keep_mask(b, h, H, N, rows, seed, offset, p)
+    return z.astype(np.float64) / (1.0 - p)
+
+
+def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+    """Attention forward; returns (O [B,N,H,d] float64, L [B,H,N] float64).
+
+    q, k, v are [B, N, H, d] arrays of any float dtype (widened exactly).
+    ``scale`` is taken as the float32 value the CUDA side receives, widened.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, d = q.shape
+    scale = float(np.float32(scale))
+    O = np.zeros((B, N, H, d))
+    L = np.full((B, H, N), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            Q, K, V = q[b, :, h, :], k[b, :, h, :], v[b, :, h, :]
+            for r0, r1 in _panels(N):
+                rows = np.arange(r0, r1)
+                ok = allowed(rows, N, causal, window)
+                S = np.where(ok, scale * (Q[r0:r1] @ K.T), -np.inf)
+                m = S.max(axis=1)
+                live = np.isfinite(m)
+                ms = np.where(live, m, 0.0)
+                E = np.where(ok, np.exp(S - ms[:, None]), 0.0)
+                lse = np.where(live, ms + np.log(np.where(live, E.sum(axis=1), 1.0)), -np.inf)
+                P = np.where(ok, np.exp(S - np.where(live, lse, 0.0)[:, None]), 0.0)
+                zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
+                Pt = P if zs is None else P * zs
+                O[b, r0:r1, h, :] = Pt @ V
+                L[b, h, r0:r1] = lse
+    return O, L
+
+
+def preprocess_D(o, do):
+    """D_i = rowsum(dO o O) per (b, h, i) in float64, returned as [B, H, N].
+
+    "FlashAttention backward" §The gradients, and the one scalar that makes
+    them local; "Implementing Flash Attention's Backward Pass" §Deriving the
+    gradients (D[i] = dot(dO[i], O[i])).
+    """
+    return np.einsum("bnhd,bnhd->bhn", _f64(do), _f64(o))
+
+
+def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
+             seed=0, offset=0):
+    """Attention backward from the saved state (O, L); returns (dQ, dK, dV, D).
+
+    Gradients are [B, N, H, d] float64, D is [B, H, N] float64. ``o`` and
+    ``lse`` are used exactly as given (function mode): pass the O and L a
+    forward produced to check a backward fed by that forward, or the float64
+    ones from :func:`forward` for the exact gradient.
+    """
+    q, k, v, o, do = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do)
+    lse = _f64(lse)
+    B, N, H, d = q.shape
+    scale = float(np.float32(scale))
+    D = preprocess_D(o, do)
+    dQ = np.zeros_like(q)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, dO = q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], do[b, :, h, :]
+            for r0, r1 in _panels(N):
+                rows = np.arange(r0, r1)
+                ok = allowed(rows, N, causal, window)
+                Lr = lse[b, h, r0:r1]
+                live = np.isfinite(Lr)
+                S = scale * (Q[r0:r1] @ K.T)
+                # P_ij = exp(S_ij - L_i) on allowed pairs of rows that have any.
+                P = np.where(ok & live[:, None],
+                             np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
+                zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
+                Pt = P if zs is None else P * zs
+                dV[b, :, h, :] += Pt.T @ dO[r0:r1]
+                dP = dO[r0:r1] @ V.T
+                if zs is not None:
+                    dP = dP * zs
+                dS = P * (dP - D[b, h, r0:r1][:, None])
+                dQ[b, r0:r1, h, :] = scale * (dS @ K)
+                dK[b, :, h, :] += scale * (dS.T @ Q[r0:r1])
+    return dQ, dK, dV, D
+
+
+def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+    """Exact mode: forward in float64, then backward from that O and L."""
+    O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset)
+    dQ, dK, dV, D = backward(q, k, v, O, do, L, scale, causal, window, dropout_p, seed, offset)
+    return O, L, dQ, dK, dV, D
+
+
+__all__ = ["allowed", "forward", "backward", "preprocess_D", "reference_grads"]
