@@ -1,0 +1,330 @@
+"""Backward-pass throughput of the GB300 FlashAttention library.
+
+One step = one full backward (fa_bwd: D preprocess, key/value-major dK/dV
+kernel, dQ step) over the causal bf16 workload B=1, H=32, N=8192, d=128, with
+inputs resident in HBM. Throughput is counted as 10*N^2*d FLOPs per head,
+halved under the causal mask, per step. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--dq deterministic|atomic]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+replicas: heads shard with no exchange, so there is no data-path collective);
+value = units of all ranks / max-over-ranks time. ``--impl reference`` times
+the float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from flashattention_backward_fa_gb300.inputs import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attn bwd TFLOP/s and % of dense bf16 peak (causal, d=128, N=8192), 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def counted_flops(w) -> float:
+    """10*N^2*d per head, halved under causal; windowed: 10*d per allowed pair."""
+    if w.window > 0:
+        W = min(w.window, w.N)
+        pairs = (W * (W + 1) // 2 + (w.N - W) * W) if w.causal else sum(
+            min(w.N, i + w.window) for i in range(w.N))
+        return 10.0 * w.d * pairs * w.B * w.H
+    per_head = 10.0 * w.N * w.N * w.d
+    return w.B * w.H * (per_head / 2 if w.causal else per_head)
+
+
+def causal_pairs(w) -> float:
+    return counted_flops(w) / (10.0 * w.d)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf: torch.Tensor):
+    buf.add_(1)
+
+
+def time_ours(w, steps, warmup, deterministic, world):
+    import flashattention_backward_fa_gb300 as fa
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
+              offset=w.philox_offset)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.alloc_workspace(q, deterministic)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=deterministic, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    # Inputs (5 x 64 MiB at the headline size) exceed the 129 MB L2, so consecutive
+    # steps do not hit in L2 on their inputs.
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / steps
+    # Per-stage durations (same stream), for the roofline of the dominant kernel.
+    stage_ms = [0.0, 0.0, 0.0]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(steps):
+        evs[0].record(stream)
+        for s in range(3):
+            fa.fa_bwd_stage(s, q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=deterministic,
+                            stream=stream)
+            evs[s + 1].record(stream)
+        torch.cuda.synchronize()
+        for s in range(3):
+            stage_ms[s] += evs[s].elapsed_time(evs[s + 1]) / steps
+    sampler.stop()
+    status = fa.fa_get_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status} after the timed region")
+    # e2e: pinned host buffers, H2D of the step's inputs, backward, D2H of the gradients.
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    e2e_steps = max(1, min(steps, 5))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        fa.fa_bwd(*dev_in[:6], dq, dk, dv, ws, **kw, deterministic=deterministic, stream=stream)
+        for h_, d_ in zip(host_out, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+
+def time_oracle(w, max_seconds=20.0):
+    """Float64 oracle backward on a bounded head sample; returns (TFLOP/s, sample text, cores)."""
+    import numpy as np
+
+    import oracle
+    q, k, v, do = make_inputs(w.with_(B=1, H=1))
+    q, k, v, do = (t.float().numpy() for t in (q, k, v, do))
+    args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
+    O, L = oracle.forward(q, k, v, *args)
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        oracle.backward(q, k, v, O, do, L, *args)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el > max_seconds / 2 or heads >= 4:
+            break
+    flops = counted_flops(w.with_(B=1, H=1)) * heads
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"{heads} head(s) of B=1,H=1,N={w.N},d={w.d} (float64 oracle backward, numpy/OpenBLAS)"
+    del np
+    return flops / el / 1e12, sample, cores, el / heads
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--dq", default="deterministic", choices=["deterministic", "atomic"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default=None, help="B,H,N override (smaller cases for profiler captures)")
+    ap.add_argument("--profile", action="store_true",
+                    help="forward, then --warmup + 1 backward steps, no timing (for ncu captures)")
+    a = ap.parse_args()
+    w = WORKLOADS[a.workload]
+    if a.shape:
+        B, H, N = (int(x) for x in a.shape.split(","))
+        w = w.with_(B=B, H=H, N=N, name=f"{w.name}@B{B}H{H}N{N}")
+    if a.profile:
+        import flashattention_backward_fa_gb300 as fa
+        q, k, v, do = (t.cuda() for t in make_inputs(w))
+        kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
+                  offset=w.philox_offset)
+        o, lse = fa.attention_forward(q, k, v, **kw)
+        for _ in range(a.warmup + 1):
+            fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=a.dq == "deterministic")
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": w.name, "status": fa.fa_get_device_status(clear=True)}))
+        return
+    world, rank, _ = dist_setup()
+    peaks, peak_src = load_peaks()
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+              "window": w.window, "dropout_p": w.dropout_p, "dq_mode": a.dq,
+              "l2": "inputs larger than L2 (5 x 64 MiB at the headline size), no flush"}
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        tf, sample, cores, sec_per_head = time_oracle(w)
+        line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": a.gpus,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec_per_head * w.B * w.H * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": tf,
+                                 "unit": "TFLOP/s"},
+                "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    r = time_ours(w, a.steps, a.warmup, a.dq == "deterministic", world)
+    ms = max_over_ranks(r["ms"], world)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    flops = counted_flops(w)
+    value = world * flops / (ms * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    det = a.dq == "deterministic"
+    # Dominant kernel: the key/value-major backward. Its algorithmic work is the
+    # S, dP, dV and dK contractions (8*d FLOPs per allowed pair), plus dQ (2*d)
+    # in atomic mode.
+    kv_ms = r["stage_ms"][1]
+    kv_flops = causal_pairs(w) * w.d * (8.0 if det else 10.0)
+    kv_tflops = kv_flops / (kv_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": config,
+        "pct_of_dense_bf16_peak": 100.0 * value / peak,
+        "stages_ms": {"preprocess": r["stage_ms"][0], "dkdv": r["stage_ms"][1],
+                      ("dq_qmajor" if det else "dq_convert"): r["stage_ms"][2]},
+        "roofline": {"kernel": "bwd_dkdv (key/value-major, tcgen05)", "bound": "tensor", "achieved": kv_tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": kv_tflops / peak, "traffic": None,
+                     "peak_source": f"{peak_src} burst bf16"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 3 * a.steps,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and not a.no_cpu_baseline:
+        tf, sample, cores, _ = time_oracle(w)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

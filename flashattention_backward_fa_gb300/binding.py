@@ -1,0 +1,226 @@
+"""Thin ctypes binding over libfa.so (the C ABI declared in include/fa.h).
+
+Argument marshalling only: shapes, strides and pointers of torch tensors are
+passed to the C entry points, which validate them and launch the CUDA kernels
+on the caller's current stream. torch supplies device memory and streams;
+every step of the computation runs in the library's kernels. There is no
+fallback: if the library is missing or the tensors are not on a CUDA device,
+these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libfa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_F32, FA_F16, FA_BF16 = 0, 1, 2
+FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ = 0, 1, 2
+ERROR_CODES = {
+    0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED", -3: "FA_ERR_ALIGNMENT",
+    -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_CUDA", -6: "FA_ERR_TIMEOUT",
+}
+_TORCH_TO_FA = {torch.float32: FA_F32, torch.float16: FA_F16, torch.bfloat16: FA_BF16}
+
+
+class FaStrides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("n", ctypes.c_int64), ("h", ctypes.c_int64)]
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_CODES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfa.so and declare the C signatures; raises if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfa.so not found at {path}: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i, f, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+    lib.fa_version.argtypes, lib.fa_version.restype = [], i
+    lib.fa_strerror.argtypes, lib.fa_strerror.restype = [i], ctypes.c_char_p
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp]
+    lib.fa_fwd.restype = i
+    bwd_args = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, i, vp, sz, vp]
+    lib.fa_bwd.argtypes, lib.fa_bwd.restype = bwd_args, i
+    lib.fa_bwd_stage.argtypes, lib.fa_bwd_stage.restype = [i] + bwd_args, i
+    lib.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+    lib.fa_get_device_status.restype = i
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER_PATH):
+    """Names of the functions include/fa.h declares (used to check the exports)."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def fa_strerror(code: int) -> str:
+    return load_library().fa_strerror(int(code)).decode()
+
+
+def _check(code: int):
+    if code != 0:
+        raise FaError(code, fa_strerror(code))
+
+
+def _layout(t: torch.Tensor):
+    if t.dim() != 4:
+        raise ValueError("attention tensors are [B, N, H, d]")
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if t.stride(3) != 1:
+        raise ValueError("the head dimension must be contiguous")
+    B, N, H, d = t.shape
+    return (B, N, H, d), FaStrides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _same_layout(ref: torch.Tensor, *others: torch.Tensor):
+    shp, st = _layout(ref)
+    for o in others:
+        s2, st2 = _layout(o)
+        if s2 != shp or (st2.b, st2.n, st2.h) != (st.b, st.n, st.h) or o.dtype != ref.dtype:
+            raise ValueError("all [B, N, H, d] tensors must share shape, strides and dtype")
+    return shp, st
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def default_scale(d: int) -> float:
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype, deterministic: bool = True) -> int:
+    code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d, code, int(bool(deterministic))))
+
+
+def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, stream=None):
+    """Forward through the C ABI: fills o ([B,N,H,d]) and lse ([B,H,N] fp32)."""
+    (B, N, H, d), st = _same_layout(q, k, v, o)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    lib = load_library()
+    _check(lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, st,
+                      _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal),
+                      int(window), float(dropout_p), int(seed), int(offset), _stream(stream)))
+
+
+def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p, seed, offset, deterministic,
+              workspace, stream):
+    (B, N, H, d), st = _same_layout(q, k, v, o, do, dq, dk, dv)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    return (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
+            default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p),
+            int(seed), int(offset), int(bool(deterministic)), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, window=0, dropout_p=0.0,
+           seed=0, offset=0, deterministic=True, stream=None):
+    """Backward through the C ABI: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor."""
+    _check(load_library().fa_bwd(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
+                                            seed, offset, deterministic, workspace, stream)))
+
+
+def fa_bwd_stage(stage, q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, window=0,
+                 dropout_p=0.0, seed=0, offset=0, deterministic=True, stream=None):
+    """One of the three backward steps (FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ)."""
+    _check(load_library().fa_bwd_stage(int(stage), *_bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal,
+                                                              window, dropout_p, seed, offset, deterministic,
+                                                              workspace, stream)))
+
+
+def fa_get_device_status(clear: bool = True) -> int:
+    """Raw device status bits of the current device (synchronises it)."""
+    s = ctypes.c_uint(0)
+    code = load_library().fa_get_device_status(ctypes.byref(s), int(clear))
+    if code not in (0, -6):
+        _check(code)
+    return int(s.value)
+
+
+def alloc_workspace(q: torch.Tensor, deterministic: bool = True) -> torch.Tensor:
+    B, N, H, d = q.shape
+    nbytes = fa_bwd_workspace_size(B, H, N, d, q.dtype, deterministic)
+    return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+
+
+def attention_forward(q, k, v, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+    """Allocate O and L and run the forward; returns (o, lse)."""
+    B, N, H, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, window, dropout_p, seed, offset)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, do, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
+                       deterministic=True, workspace=None):
+    """Allocate dQ, dK, dV (and the workspace unless given) and run the backward."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = alloc_workspace(q, deterministic)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, window, dropout_p, seed, offset,
+           deterministic)
+    return dq, dk, dv
+
+
+class _FlashAttnFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal, window, dropout_p, seed, offset, deterministic):
+        o, lse = attention_forward(q, k, v, scale, causal, window, dropout_p, seed, offset)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cfg = (scale, causal, window, dropout_p, seed, offset, deterministic)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        scale, causal, window, dropout_p, seed, offset, deterministic = ctx.cfg
+        if do.stride() != q.stride():
+            do = _match_layout(do, q)
+        dq, dk, dv = attention_backward(q, k, v, o, do, lse, scale, causal, window, dropout_p, seed, offset,
+                                        deterministic)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def _match_layout(t: torch.Tensor, ref: torch.Tensor) -> torch.Tensor:
+    out = torch.empty_strided(ref.shape, ref.stride(), dtype=ref.dtype, device=ref.device)
+    out.copy_(t)
+    return out
+
+
+def flash_attn_func(q, k, v, causal=False, window=0, dropout_p=0.0, softmax_scale=None, seed=0, offset=0,
+                    deterministic=True):
+    """Attention on [B, S, H, D] tensors with autograd (forward fa_fwd, backward fa_bwd)."""
+    k = k if k.stride() == q.stride() else _match_layout(k, q)
+    v = v if v.stride() == q.stride() else _match_layout(v, q)
+    return _FlashAttnFunc.apply(q, k, v, softmax_scale, causal, window, dropout_p, seed, offset, deterministic)

@@ -1,0 +1,270 @@
+// C ABI of libfa.so: argument validation, workspace layout, TMA descriptor
+// creation and kernel dispatch. Declarations and the contract: include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st);
+cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st);
+cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
+                               cudaStream_t st);
+cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
+                             cudaStream_t st);
+}  // namespace fa
+
+namespace {
+
+using fa::AttnParams;
+
+// Device status word, one per device context; kernels get its address.
+__device__ unsigned int g_status_word = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+int status_ptr(unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned int*>(ptr);
+  }
+  *out = g_status_ptr[dev];
+  return FA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a [B, N, H, d] tensor (dims innermost first: d, N, H, B), 128-byte
+// swizzle, boxes of 64 head-dim elements x `rows` sequence rows.
+bool make_map(CUtensorMap* m, const void* base, const AttnParams& p, bool bf16, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)p.sn * 2, (cuuint64_t)p.sh * 2, (cuuint64_t)p.sb * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+inline int pad_rows(int N) { return (N + fa::kPadRows - 1) / fa::kPadRows * fa::kPadRows; }
+
+bool needs_dq_accum(int dtype, int deterministic) { return dtype != FA_F32 && !deterministic; }
+
+struct WsLayout {
+  size_t off_L2, off_D, off_dq, total;
+};
+
+WsLayout ws_layout(int B, int H, int N, int d, int dtype, int deterministic) {
+  const size_t rows = (size_t)B * H * pad_rows(N);
+  WsLayout w;
+  w.off_L2 = 0;
+  w.off_D = round256(rows * 4);
+  w.off_dq = w.off_D + round256(rows * 4);
+  w.total = w.off_dq + (needs_dq_accum(dtype, deterministic) ? round256(rows * (size_t)d * 4) : 0);
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validation shared by the forward and the backward. Returns FA_OK or an error.
+int check_common(int B, int H, int N, int d, fa_strides s, int dtype, float scale, int window, float dropout_p) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_F32 ? d > 128 : (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+  if (s.b < 1 || s.n < 1 || s.h < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (window < 0) return FA_ERR_INVALID_ARG;
+  if (!(dropout_p >= 0.f && dropout_p < 1.f)) return FA_ERR_INVALID_ARG;
+  // Index arithmetic stays in 32-bit grids and 64-bit offsets.
+  if ((long long)B * H > (1ll << 24) || N > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_F32 && ((s.b | s.n | s.h) & 7)) return FA_ERR_ALIGNMENT;
+  return FA_OK;
+}
+
+void fill_params(AttnParams& p, int B, int H, int N, int d, fa_strides s, float scale, int causal, int window,
+                 float dropout_p, uint64_t seed, uint64_t offset) {
+  std::memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.sb = s.b;
+  p.sn = s.n;
+  p.sh = s.h;
+  p.n_pad = pad_rows(N);
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.window = window;
+  const double t = std::floor((double)dropout_p * 4294967296.0);
+  p.drop.threshold = dropout_p > 0.f ? (uint32_t)t : 0u;
+  p.drop.rp = 1.f / (1.f - dropout_p);
+  p.drop.seed_lo = (uint32_t)seed;
+  p.drop.seed_hi = (uint32_t)(seed >> 32);
+  p.drop.off_lo = (uint32_t)offset;
+  p.drop.off_hi = (uint32_t)(offset >> 32);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension, dtype or size";
+    case FA_ERR_ALIGNMENT: return "pointer or stride violates the alignment rules";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case FA_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    default: return "unknown error code";
+  }
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || d > 128) return 0;
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return 0;
+  return ws_layout(B, H, N, d, dtype, deterministic).total;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+           uint64_t seed, uint64_t offset, void* stream) {
+  int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  AttnParams p;
+  fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = o;
+  p.lse_out = lse;
+  if ((rc = status_ptr(&p.status))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_F32) return cuda_rc(fa::launch_fwd_f32(p, st));
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
+      !make_map(&maps[2], v, p, bf16, fa::kStepKV))
+    return FA_ERR_CUDA;
+  maps[3] = maps[0];
+  return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, st));
+}
+
+int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
+                 const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                 uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
+  if (rc) return rc;
+  if (stage != FA_BWD_PREPROCESS && stage != FA_BWD_DKDV && stage != FA_BWD_DQ) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return FA_ERR_ALIGNMENT;
+  const WsLayout w = ws_layout(B, H, N, d, dtype, deterministic);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  AttnParams p;
+  fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.out = dq;
+  p.dk = dk;
+  p.dv = dv;
+  char* ws = static_cast<char*>(workspace);
+  p.ws_L2 = reinterpret_cast<float*>(ws + w.off_L2);
+  p.ws_D = reinterpret_cast<float*>(ws + w.off_D);
+  p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
+  if ((rc = status_ptr(&p.status))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stage == FA_BWD_PREPROCESS) return cuda_rc(fa::launch_preprocess(p, dtype, st));
+  if (dtype == FA_F32)
+    return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
+  const bool bf16 = dtype == FA_BF16;
+  if (stage == FA_BWD_DKDV) {
+    CUtensorMap maps[4];
+    if (!make_map(&maps[0], q, p, bf16, fa::kStepQ) || !make_map(&maps[1], k, p, bf16, fa::kRowsKV) ||
+        !make_map(&maps[2], v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], dout, p, bf16, fa::kStepQ))
+      return FA_ERR_CUDA;
+    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
+  }
+  if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
+      !make_map(&maps[2], v, p, bf16, fa::kStepKV) || !make_map(&maps[3], dout, p, bf16, fa::kRowsQ))
+    return FA_ERR_CUDA;
+  return cuda_rc(fa::launch_qmajor_tc(p, bf16, true, maps, st));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+           float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+           int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  const fa_bwd_stage_id stages[3] = {FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ};
+  for (fa_bwd_stage_id s : stages) {
+    const int rc = fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal,
+                                window, dropout_p, seed, offset, deterministic, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+  }
+  return FA_OK;
+}
+
+int fa_get_device_status(unsigned int* status, int clear) {
+  if (!status) return FA_ERR_INVALID_ARG;
+  unsigned int* ptr = nullptr;
+  int rc = status_ptr(&ptr);
+  if (rc) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpy(status, ptr, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (clear && cudaMemset(ptr, 0, sizeof(unsigned int)) != cudaSuccess) return FA_ERR_CUDA;
+  return (*status & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,330 @@
+// Bandwidth-bound helpers of the backward pass and the CUDA-core fp32 path.
+//
+// * preprocess: D_i = rowsum(dO o O) in fp32 ("FlashAttention backward",
+//   §The gradients, and the one scalar that makes them local: one cheap pass
+//   over dO and O before the main loop), plus L*log2(e) into a padded
+//   workspace vector and, in atomic-dQ mode, the zero fill of the fp32 dQ
+//   accumulator.
+// * dq_convert: dQ = scale * dQ_accum, rounded to the tensor dtype (atomic mode).
+// * fp32 kernels: forward (two passes: row statistics, then O) and the
+//   key-major dK/dV plus query-major dQ kernels of the backward, on CUDA cores.
+//   fp32 needs ~1e-7 relative accuracy, which the tf32 tensor-core kind cannot
+//   give, so this path multiplies in FFMA.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One warp per (b, i, h) row; rows enumerated in [B, n_pad, H] order so that a
+// contiguous [B, N, H, d] tensor is read front to back.
+template <typename T>
+__global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__ AttnParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)p.B * p.n_pad * p.H;
+  if (warp >= rows) return;
+  const int h = warp % p.H;
+  const int i = (warp / p.H) % p.n_pad;
+  const int b = warp / (p.H * p.n_pad);
+  const int bh = b * p.H + h;
+  const long long ws = (long long)bh * p.n_pad + i;
+  float acc = 0.f;
+  if (i < p.N) {
+    const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+    const T* o = static_cast<const T*>(p.o) + off;
+    const T* g = static_cast<const T*>(p.dout) + off;
+    if (sizeof(T) == 2 && (p.d & 63) == 0) {
+      // 16-bit types, d in {64, 128}: lanes read 2 or 4 contiguous elements.
+      const int per = p.d >> 5;
+      for (int e = 0; e < per; e += 2) {
+        const int k = lane * per + e;
+        const uint32_t ow = *reinterpret_cast<const uint32_t*>(o + k);
+        const uint32_t gw = *reinterpret_cast<const uint32_t*>(g + k);
+        const T* o2 = reinterpret_cast<const T*>(&ow);
+        const T* g2 = reinterpret_cast<const T*>(&gw);
+        acc = fmaf(to_f32(o2[0]), to_f32(g2[0]), acc);
+        acc = fmaf(to_f32(o2[1]), to_f32(g2[1]), acc);
+      }
+    } else {
+      for (int k = lane; k < p.d; k += 32) acc = fmaf(to_f32(o[k]), to_f32(g[k]), acc);
+    }
+    acc = warp_sum(acc);
+  }
+  if (lane == 0) {
+    p.ws_D[ws] = acc;
+    p.ws_L2[ws] = (i < p.N) ? p.lse[(long long)bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
+  }
+  if (p.ws_dq != nullptr) {
+    float* dq = p.ws_dq + ws * p.d;
+    for (int k = lane; k < p.d; k += 32) dq[k] = 0.f;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const __grid_constant__ AttnParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)p.B * p.N * p.H;
+  if (warp >= rows) return;
+  const int h = warp % p.H;
+  const int i = (warp / p.H) % p.N;
+  const int b = warp / (p.H * p.N);
+  const float* src = p.ws_dq + ((long long)(b * p.H + h) * p.n_pad + i) * p.d;
+  T* dst = static_cast<T*>(p.out) + (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+  for (int k = lane; k < p.d; k += 32) dst[k] = from_f32<T>(src[k] * p.scale);
+}
+
+// ------------------------------- fp32 path ---------------------------------
+constexpr int kF32Warps = 4;  // rows per block (one warp each)
+
+__device__ __forceinline__ const float* row_ptr(const AttnParams& p, const void* base, int b, int i, int h) {
+  return static_cast<const float*>(base) + (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+}
+
+__device__ __forceinline__ float dot_row(const float* __restrict__ a_smem, const float* __restrict__ g, int d) {
+  float acc = 0.f;
+  for (int k = 0; k < d; ++k) acc = fmaf(a_smem[k], g[k], acc);
+  return acc;
+}
+
+// Forward, one warp per query row: pass 1 row max and sum of exp2 (lanes take
+// keys lane, lane+32, ...), pass 2 O = sum_j P~_ij V_j with lanes owning head
+// dimensions and P broadcast by shuffles.
+__global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float qrow[kF32Warps][128];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kF32Warps + w;
+  if (row >= (long long)p.B * p.H * p.N) return;
+  const int i = row % p.N, bh = row / p.N, b = bh / p.H, h = bh % p.H;
+  const float* q = row_ptr(p, p.q, b, i, h);
+  for (int k = lane; k < p.d; k += 32) qrow[w][k] = q[k];
+  __syncwarp();
+  const int jlo = p.window > 0 ? max(0, i - p.window + 1) : 0;
+  const int jhi = p.causal ? i : p.N - 1;
+  float m = -INFINITY, l = 0.f;
+  for (int j = jlo + lane; j <= jhi; j += 32) {
+    const float x = dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2;
+    const float mn = fmaxf(m, x);
+    l = l * ex2_approx(m - mn) + ex2_approx(x - mn);
+    m = mn;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m, o), lo = __shfl_xor_sync(0xffffffffu, l, o);
+    const float mn = fmaxf(m, mo);
+    if (mn == -INFINITY) continue;
+    l = l * ex2_approx(m - mn) + lo * ex2_approx(mo - mn);
+    m = mn;
+  }
+  const bool live = l > 0.f;
+  float lg;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(live ? l : 1.f));
+  const float L2 = live ? m + lg : __int_as_float(0x7f800000);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int jb = jlo; jb <= jhi; jb += 32) {
+    const int j = jb + lane;
+    float pj = 0.f;
+    if (j <= jhi) {
+      pj = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 - L2);
+      if (p.drop.threshold) pj = dropout_keep(p.drop, bh, p.N, i, j) ? pj * p.drop.rp : 0.f;
+    }
+    const int cnt = min(32, jhi - jb + 1);
+    for (int t = 0; t < cnt; ++t) {
+      const float pb = __shfl_sync(0xffffffffu, pj, t);
+      const float* vr = row_ptr(p, p.v, b, jb + t, h);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = lane + 32 * u;
+        if (k < p.d) acc[u] = fmaf(pb, vr[k], acc[u]);
+      }
+    }
+  }
+  float* o = static_cast<float*>(p.out) + (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane + 32 * u;
+    if (k < p.d) o[k] = acc[u];
+  }
+  if (lane == 0) p.lse_out[(long long)bh * p.N + i] = live ? L2 * kLn2 : -INFINITY;
+}
+
+// dK, dV, one warp per key row j: lanes take queries, the per-pair P~ and dS
+// are broadcast by shuffles and accumulated into lane-owned head dimensions.
+__global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float krow[kF32Warps][128];
+  __shared__ float vrow[kF32Warps][128];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kF32Warps + w;
+  if (row >= (long long)p.B * p.H * p.N) return;
+  const int j = row % p.N, bh = row / p.N, b = bh / p.H, h = bh % p.H;
+  const float* kk = row_ptr(p, p.k, b, j, h);
+  const float* vv = row_ptr(p, p.v, b, j, h);
+  for (int k = lane; k < p.d; k += 32) {
+    krow[w][k] = kk[k];
+    vrow[w][k] = vv[k];
+  }
+  __syncwarp();
+  const int ilo = p.causal ? j : 0;
+  const int ihi = p.window > 0 ? min(p.N - 1, j + p.window - 1) : p.N - 1;
+  const float* L2 = p.ws_L2 + (long long)bh * p.n_pad;
+  const float* Dv = p.ws_D + (long long)bh * p.n_pad;
+  float dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int ib = ilo; ib <= ihi; ib += 32) {
+    const int i = ib + lane;
+    float pt = 0.f, ds = 0.f;
+    if (i <= ihi) {
+      const float pv = ex2_approx(dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2 - L2[i]);
+      float dp = dot_row(vrow[w], row_ptr(p, p.dout, b, i, h), p.d);
+      pt = pv;
+      if (p.drop.threshold) {
+        const bool keep = dropout_keep(p.drop, bh, p.N, i, j);
+        pt = keep ? pv * p.drop.rp : 0.f;
+        dp = keep ? dp * p.drop.rp : 0.f;
+      }
+      ds = pv * (dp - Dv[i]);
+    }
+    const int cnt = min(32, ihi - ib + 1);
+    for (int t = 0; t < cnt; ++t) {
+      const float pb = __shfl_sync(0xffffffffu, pt, t), sb = __shfl_sync(0xffffffffu, ds, t);
+      const float* qr = row_ptr(p, p.q, b, ib + t, h);
+      const float* gr = row_ptr(p, p.dout, b, ib + t, h);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = lane + 32 * u;
+        if (k < p.d) {
+          dv[u] = fmaf(pb, gr[k], dv[u]);
+          dk[u] = fmaf(sb, qr[k], dk[u]);
+        }
+      }
+    }
+  }
+  const long long off = (long long)b * p.sb + (long long)j * p.sn + (long long)h * p.sh;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane + 32 * u;
+    if (k < p.d) {
+      static_cast<float*>(p.dk)[off + k] = dk[u] * p.scale;
+      static_cast<float*>(p.dv)[off + k] = dv[u];
+    }
+  }
+}
+
+// dQ, one warp per query row i (query-major: deterministic, no atomics).
+__global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid_constant__ AttnParams p) {
+  __shared__ float qrow[kF32Warps][128];
+  __shared__ float grow[kF32Warps][128];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kF32Warps + w;
+  if (row >= (long long)p.B * p.H * p.N) return;
+  const int i = row % p.N, bh = row / p.N, b = bh / p.H, h = bh % p.H;
+  const float* q = row_ptr(p, p.q, b, i, h);
+  const float* g = row_ptr(p, p.dout, b, i, h);
+  for (int k = lane; k < p.d; k += 32) {
+    qrow[w][k] = q[k];
+    grow[w][k] = g[k];
+  }
+  __syncwarp();
+  const int jlo = p.window > 0 ? max(0, i - p.window + 1) : 0;
+  const int jhi = p.causal ? i : p.N - 1;
+  const float L2 = p.ws_L2[(long long)bh * p.n_pad + i];
+  const float Dv = p.ws_D[(long long)bh * p.n_pad + i];
+  float dq[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int jb = jlo; jb <= jhi; jb += 32) {
+    const int j = jb + lane;
+    float ds = 0.f;
+    if (j <= jhi) {
+      const float pv = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 - L2);
+      float dp = dot_row(grow[w], row_ptr(p, p.v, b, j, h), p.d);
+      if (p.drop.threshold) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
+      ds = pv * (dp - Dv);
+    }
+    const int cnt = min(32, jhi - jb + 1);
+    for (int t = 0; t < cnt; ++t) {
+      const float sb = __shfl_sync(0xffffffffu, ds, t);
+      const float* kr = row_ptr(p, p.k, b, jb + t, h);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = lane + 32 * u;
+        if (k < p.d) dq[u] = fmaf(sb, kr[k], dq[u]);
+      }
+    }
+  }
+  float* o = static_cast<float*>(p.out) + (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane + 32 * u;
+    if (k < p.d) o[k] = dq[u] * p.scale;
+  }
+}
+
+// ------------------------------- launchers ---------------------------------
+static inline unsigned grid_for_rows(long long rows, int rows_per_block) {
+  return (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+}
+
+cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.n_pad * p.H;
+  const unsigned grid = grid_for_rows(rows, 8);
+  if (dtype == 0) preprocess_kernel<float><<<grid, 256, 0, st>>>(p);
+  else if (dtype == 1) preprocess_kernel<__half><<<grid, 256, 0, st>>>(p);
+  else preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.N * p.H;
+  const unsigned grid = grid_for_rows(rows, 8);
+  if (dtype == 0) dq_convert_kernel<float><<<grid, 256, 0, st>>>(p);
+  else if (dtype == 1) dq_convert_kernel<__half><<<grid, 256, 0, st>>>(p);
+  else dq_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st) {
+  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  fwd_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st) {
+  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  bwd_dkdv_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st) {
+  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  bwd_dq_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,140 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) FlashAttention forward/backward library (libfa.so).
+ *
+ * What is computed. For every batch b and head h of [B, N, H, d] tensors:
+ *   S = scale * Q K^T; pairs outside the mask get S = -inf
+ *   L_i = log sum_j exp(S_ij)                         (natural log, before dropout)
+ *   P = exp(S - L);  P~ = P o Z / (1 - p)             (Z: dropout keep-mask)
+ *   O = P~ V
+ * and the backward, from the saved state (O, L) and the upstream gradient dO:
+ *   D_i = sum_k dO_ik O_ik
+ *   dV = P~^T dO;  dP = (dO V^T) o Z / (1 - p);  dS = P o (dP - D)
+ *   dQ = scale * dS K;  dK = scale * dS^T Q
+ * Sources: "FlashAttention backward" (GPU-kernels lesson 29), §What the forward
+ * left behind (O and L are the saved state; P = exp(S - L)) and §The gradients,
+ * and the one scalar that makes them local (the formulas and D); "Lecture 7 —
+ * Backward Pass and Validation", §The math, §Mask behaviour, §Dropout,
+ * §Determinism; "Implementing Flash Attention's Backward Pass in Raw CUDA",
+ * §Deriving the gradients. The N x N matrix P is never materialised.
+ *
+ * Masks. causal != 0 keeps pairs j <= i (top-left aligned, square attention).
+ * window > 0 keeps pairs j > i - window; with causal this is the two-sided
+ * sliding window i - window < j <= i. window == 0 means no window.
+ *
+ * Dropout. 0 <= dropout_p < 1. The keep decision of element (b, h, i, j) is
+ * word (j mod 4) of Philox4x32-10 (Salmon et al., SC'11) with
+ *   key     = (lo32(seed), hi32(seed))
+ *   counter = (lo32(g), hi32(g), lo32(offset), hi32(offset)),
+ *   g       = ((b*H + h)*N + i) * ceil(N/4) + floor(j/4)
+ * and the element is kept iff that word >= floor(dropout_p * 2^32). Kept
+ * elements are scaled by 1/(1 - dropout_p). fa_fwd and fa_bwd draw the same
+ * mask for the same (seed, offset).
+ *
+ * Layout. Q, K, V, O, dO, dQ, dK, dV share one element-stride triple
+ * fa_strides {b, n, h}: element (b, i, h, k) lives at b*s.b + i*s.n + h*s.h + k
+ * (the head dimension is contiguous). [B, N, H, d] contiguous is
+ * {N*H*d, H*d, d}; [B, H, N, d] contiguous is {H*N*d, d, N*d}.
+ * L (lse) is a contiguous fp32 [B, H, N] array.
+ *
+ * Supported. fp16 / bf16: d in {64, 128}, tensor-core (tcgen05) kernels.
+ * fp32: 1 <= d <= 128, CUDA-core kernels. Any N >= 1, B >= 1, H >= 1.
+ * Alignment: every tensor base 16-byte aligned; for fp16/bf16 every stride a
+ * multiple of 8 elements (the TMA rule of 16-byte strides); for fp32 strides
+ * only need to be positive.
+ *
+ * Ownership and execution. The caller owns every buffer; the library never
+ * allocates device memory and keeps no per-call state. All pointers are
+ * device pointers. Calls are asynchronous on `stream` (a cudaStream_t, NULL =
+ * the legacy default stream). Outputs are overwritten, never accumulated into.
+ * Return value: FA_OK, or a negative FA_ERR_* code when an argument is
+ * rejected (nothing is launched) or a launch fails. Faults during execution
+ * surface at the caller's next synchronisation, as for any CUDA call. A kernel
+ * whose internal bounded wait gives up sets a device status bit that
+ * fa_get_device_status() reports as FA_ERR_TIMEOUT. No C++ exception crosses
+ * this boundary. Thread-safe.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad mask/dropout value */
+  FA_ERR_UNSUPPORTED = -2, /* head dimension or dtype this library does not handle */
+  FA_ERR_ALIGNMENT = -3,   /* base pointer or stride violates the alignment rules */
+  FA_ERR_WORKSPACE = -4,   /* workspace missing, misaligned (256 B) or too small */
+  FA_ERR_CUDA = -5,        /* a CUDA runtime/driver call or kernel launch failed */
+  FA_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (see fa_get_device_status) */
+};
+
+/* Element strides of the [B, N, H, d] tensors; the d stride is 1. */
+typedef struct {
+  int64_t b, n, h;
+} fa_strides;
+
+/* Bytes of device workspace fa_bwd needs: two fp32 vectors of B*H*roundup(N,128)
+ * (L*log2(e) and D), plus, for fp16/bf16 with deterministic == 0, the fp32 dQ
+ * accumulator of B*H*roundup(N,128)*d floats. Returns 0 for invalid sizes. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic);
+
+/* Forward: writes O ([B, N, H, d], dtype) and lse ([B, H, N] fp32, natural
+ * log). Produces the saved state the backward consumes. */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+           uint64_t seed, uint64_t offset, void* stream);
+
+/* Backward: from Q, K, V, the forward's O and lse, and dO, writes dQ, dK, dV
+ * (same dtype and strides). deterministic != 0 (the default the library
+ * recommends) computes dQ in a separate query-major kernel, bit-reproducible
+ * run to run; deterministic == 0 adds dQ with fp32 atomics from the
+ * key/value-major kernel and converts it afterwards (faster, dQ may differ in
+ * the last bits between runs; dK and dV are deterministic in both modes).
+ * fp32 inputs always use the deterministic path. `workspace` must be
+ * 256-byte aligned and hold fa_bwd_workspace_size(...) bytes; its contents on
+ * entry do not matter. Runs fa_bwd_stage(FA_BWD_PREPROCESS), (FA_BWD_DKDV),
+ * (FA_BWD_DQ) in order on `stream`. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+           float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+           int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three steps of fa_bwd, for callers that schedule or time them apart.
+ * Arguments as fa_bwd; the stages must run in order with the same arguments.
+ *  FA_BWD_PREPROCESS: D_i = rowsum(dO o O) and lse*log2(e) into the workspace;
+ *                     zero-fills the dQ accumulator in atomic mode.
+ *  FA_BWD_DKDV:       key/value-major kernel: dK, dV (and atomic dQ adds).
+ *  FA_BWD_DQ:         deterministic: query-major dQ kernel; atomic: dQ =
+ *                     scale * accumulator, rounded to the dtype. */
+typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ = 2 } fa_bwd_stage_id;
+
+int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
+                 const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                 uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Reads (and with clear != 0 resets) the status word of the current device.
+ * Call after synchronising the streams the kernels ran on. *status receives
+ * the raw bits (1 = a bounded wait timed out). Returns FA_OK, FA_ERR_TIMEOUT
+ * when the timeout bit is set, or FA_ERR_CUDA. This call synchronises the device. */
+int fa_get_device_status(unsigned int* status, int clear);
+
+/* Static string for an FA_* code. */
+const char* fa_strerror(int code);
+
+/* Library ABI version (major*100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,128 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function include/fa.h declares, and rejects bad arguments with the documented
+codes before touching any GPU (none of these calls reaches the CUDA runtime).
+"""
+import ctypes
+import os
+import shutil
+
+import pytest
+
+import flashattention_backward_fa_gb300 as fa
+from flashattention_backward_fa_gb300 import binding
+
+F32, F16, BF16 = fa.FA_F32, fa.FA_F16, fa.FA_BF16
+OK, EINVAL, EUNSUP, EALIGN, EWS = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("no nvcc to build the library")
+        from flashattention_backward_fa_gb300.build import build_library
+        build_library()
+    return fa.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = binding.header_functions()
+    assert {"fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_bwd_stage"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(lib):
+    assert lib.fa_version() >= 100
+    for code in (OK, EINVAL, EUNSUP, EALIGN, EWS, -5, -6):
+        s = fa.fa_strerror(code)
+        assert s and s != "unknown error code"
+    assert fa.fa_strerror(-99) == "unknown error code"
+
+
+def _rows(N):
+    return (N + 127) // 128 * 128
+
+
+@pytest.mark.parametrize("B,H,N,d", [(1, 32, 8192, 128), (4, 16, 2048, 128), (2, 16, 4096, 64), (1, 1, 1, 64),
+                                     (3, 5, 777, 128)])
+def test_workspace_size(lib, B, H, N, d):
+    r = B * H * _rows(N)
+    vec = (r * 4 + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, True) == 2 * vec
+    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, False) == 2 * vec + (r * d * 4 + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, N, d, F32, False) == 2 * vec  # fp32 never accumulates dQ atomically
+    assert fa.fa_bwd_workspace_size(0, H, N, d, BF16, True) == 0
+    assert fa.fa_bwd_workspace_size(B, H, N, 129, BF16, True) == 0
+
+
+def _strides(N, H, d):
+    return fa.FaStrides(N * H * d, H * d, d)
+
+
+P = 0x10000  # a fake, 16-byte-aligned "device" address: validation rejects before any use
+
+
+def _fwd(lib, *, q=P, k=P, v=P, o=P, lse=P, B=1, H=2, N=64, d=128, st=None, dt=BF16, scale=0.1, causal=0,
+         window=0, p=0.0):
+    st = st or _strides(N, H, d)
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, st, dt, scale, causal, window, p, 0, 0, None)
+
+
+def _bwd(lib, *, ptrs=None, B=1, H=2, N=64, d=128, st=None, dt=BF16, scale=0.1, window=0, p=0.0, det=1,
+         ws=0x100000, ws_bytes=1 << 30, stage=None):
+    ptrs = ptrs or [P] * 9
+    st = st or _strides(N, H, d)
+    args = [*ptrs, B, H, N, d, st, dt, scale, 1, window, p, 0, 0, det, ws, ws_bytes, None]
+    return lib.fa_bwd(*args) if stage is None else lib.fa_bwd_stage(stage, *args)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, B=0) == EINVAL
+    assert _fwd(lib, N=0) == EINVAL
+    assert _fwd(lib, d=96) == EUNSUP
+    assert _fwd(lib, d=256) == EUNSUP
+    assert _fwd(lib, dt=7) == EUNSUP
+    assert _fwd(lib, dt=F32, d=129) == EUNSUP
+    assert _fwd(lib, q=0) == EINVAL
+    assert _fwd(lib, lse=0) == EINVAL
+    assert _fwd(lib, q=P + 8) == EALIGN
+    assert _fwd(lib, st=fa.FaStrides(64 * 2 * 128, 2 * 128 + 4, 128)) == EALIGN
+    assert _fwd(lib, window=-1) == EINVAL
+    assert _fwd(lib, p=1.0) == EINVAL
+    assert _fwd(lib, p=-0.1) == EINVAL
+    assert _fwd(lib, scale=float("nan")) == EINVAL
+    assert _fwd(lib, st=fa.FaStrides(0, 128, 128)) == EINVAL
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert _bwd(lib, B=0) == EINVAL
+    assert _bwd(lib, d=32) == EUNSUP
+    assert _bwd(lib, ptrs=[P] * 8 + [0]) == EINVAL
+    assert _bwd(lib, ptrs=[P] * 5 + [P + 4] + [P] * 3) == EALIGN
+    assert _bwd(lib, ws=0) == EWS
+    assert _bwd(lib, ws=0x100000 + 128) == EWS
+    need = fa.fa_bwd_workspace_size(1, 2, 64, 128, BF16, True)
+    assert _bwd(lib, ws_bytes=need - 1) == EWS
+    need_atomic = fa.fa_bwd_workspace_size(1, 2, 64, 128, BF16, False)
+    assert _bwd(lib, det=0, ws_bytes=need) == EWS and need_atomic > need
+    assert _bwd(lib, p=1.5) == EINVAL
+    assert _bwd(lib, stage=7) == EINVAL
+    assert _bwd(lib, stage=1, d=80) == EUNSUP
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q, lse)
+
+
+def test_oracle_not_imported_by_product_path():
+    """The package never imports the oracle (its only users are tests, smoke and the bench)."""
+    import pathlib
+    pkg = pathlib.Path(binding.__file__).parent
+    for f in pkg.rglob("*.py"):
+        text = f.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, f
