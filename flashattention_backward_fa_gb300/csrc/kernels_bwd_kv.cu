@@ -2,83 +2,88 @@
 //
 // "FlashAttention backward", §The loop structure: the outer loop runs over
 // key/value blocks and the inner loop over query blocks, so that dK_j and dV_j
-// accumulate on chip and are written once. Per (query step, key block) pair:
+// accumulate on chip and are written once. Per (query step of 64 rows, key
+// block of 128 rows):
 //
 //   S^T  = K_j Q_i^T            (recomputed, "Lecture 7" §The recomputation trick)
 //   dP~T = V_j dO_i^T
 //   P^T  = exp2(S^T * scale*log2e - L_i*log2e)    masked pairs -> 0
 //   P~T  = P^T o Z/(1-p),  dP^T = dP~T o Z/(1-p)  (dropout, "Lecture 7" §Dropout)
 //   dS^T = P^T o (dP^T - D_i)                     ("FlashAttention backward" §The gradients)
-//   dV  += P~T dO_i,   dK += dS^T Q_i             (fp32 in TMEM, scaled by `scale` on store)
+//   dV  += P~T dO_i,   dK += dS^T Q_i             (fp32 in TMEM; dK scaled on store)
 //   atomic mode only: dQ_i^T = K_j^T dS^T, added into an fp32 HBM accumulator
 //   with red.add ("FlashAttention backward" §The loop structure, choice (a)).
 //
-// Keys sit on the 128 TMEM lanes, so one thread owns one key row of S^T and
-// dP^T, and its row of P~T / dS^T goes to shared memory in the 128-byte
-// swizzled layout the MMA reads as a K-major A operand. The same dS^T tile is
-// read as an MN-major B operand for dQ^T.
+// Keys sit on the 128 TMEM lanes: one thread owns one key row of S^T and dP^T.
+// The row math writes P~T and dS^T back into the TMEM columns it has just read
+// (rounded to 16 bits, two per column, plus the rounding residual when a
+// tile holds probabilities above kSplitThreshold), and dV / dK take them as
+// the A operand straight from TMEM. In atomic mode dS^T also goes to shared
+// memory, where it is the B operand of dQ^T and the A operand of dK.
 //
-// Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues MMAs,
-// warps 4-7 turn S/dP into P/dS and write the dK/dV epilogue, warps 8-11
-// (atomic mode) drain dQ^T from TMEM into the HBM accumulator.
+// Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues MMAs, two
+// row-math warpgroups (warps 4-7, 8-11) take alternate query steps so that
+// one computes while the other waits on the tensor cores; warpgroup w always
+// uses TMEM buffer w. They also drain dQ^T in atomic mode and write the
+// dV (warpgroup 0) / dK (warpgroup 1) epilogue.
 //
-// TMEM columns (512 allocated): [0,128) S^T double buffer (reused for dQ^T in
-// atomic mode once S^T has been consumed), [128,256) dP^T double buffer,
-// [256,256+d) dV, [256+d,256+2d) dK.
+// TMEM columns (512): S^T/P buffers [0,64) and [64,128), dP^T/dS (or dQ^T in
+// atomic mode) buffers [128,192) and [192,256), dV [256,256+d), dK [256+d,256+2d).
 #include "fa_internal.h"
 
 namespace fa {
 
-template <int D>
+template <int D, bool kAtomic>
 struct KVCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kNS = (D == 128) ? 2 : 4;               // Q/dO pipeline stages
   static constexpr uint32_t kKVPanel = kRowsKV * 128;          // 16 KB: 128 rows x 64 elements
   static constexpr uint32_t kKVTile = kPanels * kKVPanel;
   static constexpr uint32_t kQPanel = kStepQ * 128;            // 8 KB: 64 rows x 64 elements
   static constexpr uint32_t kQTile = kPanels * kQPanel;
   static constexpr uint32_t kPTile = kRowsKV * kStepQ * 2;     // 16 KB: 128 keys x 64 queries
+  static constexpr uint32_t kDSBytes = kAtomic ? 4 * kPTile : 0;  // dS^T rounded + residual, x2 buffers
+  static constexpr uint32_t kStageBytes = 2 * kQTile + 2 * kStepQ * 4;
+  static constexpr uint32_t kBudget = 225u * 1024u;
+  static constexpr int kNSraw = (int)((kBudget - 2 * kKVTile - kDSBytes - 2048) / kStageBytes);
+  static constexpr int kNS = kNSraw > 4 ? 4 : kNSraw;          // Q/dO pipeline stages
   static constexpr uint32_t oK = 0;
   static constexpr uint32_t oV = oK + kKVTile;
   static constexpr uint32_t oQ = oV + kKVTile;
   static constexpr uint32_t oDO = oQ + kNS * kQTile;
-  static constexpr uint32_t oP = oDO + kNS * kQTile;    // P~T, rounded to 16 bits
-  static constexpr uint32_t oDS = oP + kPTile;           // dS^T, rounded
-  static constexpr uint32_t oPlo = oDS + kPTile;         // rounding residuals (split tiles only)
-  static constexpr uint32_t oDSlo = oPlo + kPTile;
-  static constexpr uint32_t oL = oDSlo + kPTile;
+  static constexpr uint32_t oDS = oDO + kNS * kQTile;          // [buffer][rounded, residual] tiles
+  static constexpr uint32_t oL = oDS + kDSBytes;
   static constexpr uint32_t oD = oL + kNS * kStepQ * 4;
   static constexpr uint32_t oBar = oD + kNS * kStepQ * 4;
-  // barrier indices
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kNS;
   static constexpr int bSFull = bQEmpty + kNS;
   static constexpr int bSEmpty = bSFull + 2;
   static constexpr int bPFull = bSEmpty + 2;
-  static constexpr int bPEmpty = bPFull + 1;
-  static constexpr int bDQFull = bPEmpty + 1;
+  static constexpr int bDQFull = bPFull + 2;
   static constexpr int bAcc = bDQFull + 2;
   static constexpr int bDrain = bAcc + 1;
-  static constexpr int bVote = bDrain + 1;
-  static constexpr int kBars = bVote + 1;
+  static constexpr int kBars = bDrain + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
-  static constexpr uint32_t oFlags = oAbort + 8;         // per-warp "split this tile" votes
-  static constexpr uint32_t kSmem = oFlags + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
+  static constexpr uint32_t kSmem = oFlags + 32 + 1024;        // + slack for 1024-byte alignment
+  static_assert(kNS >= 2, "shared memory budget leaves fewer than two Q/dO stages");
+  static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
 
-template <int D, bool kBf16, bool kAtomic>
-__global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
+template <int D, bool kBf16, bool kAtomic, bool kDrop>
+__global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmDO) {
-  using C = KVCfg<D>;
+  using C = KVCfg<D, kAtomic>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oAbort);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
   auto bar = [&](int idx) -> uint32_t { return sb + C::oBar + 8u * idx; };
 
   // Work unit: (batch*head, key block), heaviest key blocks first under a causal mask.
@@ -100,14 +105,12 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::bSFull + x), 1);
-      mbar_init(bar(C::bSEmpty + x), kAtomic ? 256 : 128);
+      mbar_init(bar(C::bSEmpty + x), kAtomic ? 1 + 128 : 1);
+      mbar_init(bar(C::bPFull + x), 128);
       mbar_init(bar(C::bDQFull + x), 1);
     }
-    mbar_init(bar(C::bPFull), 128);
-    mbar_init(bar(C::bPEmpty), 1);
     mbar_init(bar(C::bAcc), 1);
     mbar_init(bar(C::bDrain), 1);
-    mbar_init(bar(C::bVote), 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::oTmemSlot);
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
         const int s = it % C::kNS;
         if (!mbar_wait(bar(C::bQEmpty + s), ((it / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
         const int i0 = i_first + it * kStepQ;
-        mbar_arrive_expect_tx(bar(C::bQFull + s), 2 * C::kQTile + 2 * kStepQ * 4);
+        mbar_arrive_expect_tx(bar(C::bQFull + s), C::kStageBytes);
         for (int pn = 0; pn < C::kPanels; ++pn) {
           tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn, i0,
                       h, b);
@@ -161,52 +165,65 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer --------------------------------
     if (lane == 0) {
-      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
-      constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);
-      constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);
-      const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);   // S^T, dP^T
+      constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);         // dV, dK
+      constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);     // dQ^T
       bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
       tc_fence_after();
       auto grads = [&](int t) -> bool {
-        const int bp = t & 1, sp = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull), t & 1, abort_flag, p.status)) return false;
+        const int bt = t & 1, st = t % C::kNS;
+        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const volatile int* flags = reinterpret_cast<const volatile int*>(smem + C::oFlags);
-        const bool split = (flags[0] | flags[1] | flags[2] | flags[3]) != 0;
-        const uint32_t doB = sb + C::oDO + sp * C::kQTile, qB = sb + C::oQ + sp * C::kQTile;
-        // dV += P~T dO and dK += dS^T Q, from the rounded tiles and, on split
-        // tiles, again from the rounding residuals.
-        for (int part = 0; part < (split ? 2 : 1); ++part) {
-          const uint32_t pA = sb + (part ? C::oPlo : C::oP), dsA = sb + (part ? C::oDSlo : C::oDS);
+        const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+        const uint32_t doB = sb + C::oDO + st * C::kQTile, qB = sb + C::oQ + st * C::kQTile;
+        const int parts = split ? 2 : 1;
+        // dV += P~T dO: A = P~T from TMEM; K step k reads the 8 rounded columns at
+        // 16k and, on split tiles, the 8 residual columns at 16k + 8.
+        for (int part = 0; part < parts; ++part) {
 #pragma unroll
           for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ss(tdV, make_sdesc(pA + 32 * k, 16, 1024), make_sdesc(doB + 2048 * k, C::kQPanel, 1024), idG,
-                      (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ss(tdK, make_sdesc(dsA + 32 * k, 16, 1024), make_sdesc(qB + 2048 * k, C::kQPanel, 1024), idG,
+            tc_mma_ts(tdV, tS + 64 * bt + 16 * k + 8 * part, make_sdesc(doB + 2048 * k, C::kQPanel, 1024), idG,
                       (t > 0 || k > 0 || part > 0) ? 1u : 0u);
         }
-        if constexpr (kAtomic) {
-          // dQ^T (d x 64) = K_j^T (d x 128 keys) . dS^T (128 keys x 64); for d = 64 the
-          // upper 64 rows of the 128-row MMA are ignored.
-          for (int part = 0; part < (split ? 2 : 1); ++part) {
-            const uint32_t dsA = sb + (part ? C::oDSlo : C::oDS);
+        if constexpr (!kAtomic) {
+          // dK += dS^T Q: A = dS^T from TMEM, same column image.
+          for (int part = 0; part < parts; ++part) {
+#pragma unroll
+            for (int k = 0; k < kStepQ / 16; ++k)
+              tc_mma_ts(tdK, tdP + 64 * bt + 16 * k + 8 * part, make_sdesc(qB + 2048 * k, C::kQPanel, 1024),
+                        idG, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
+          }
+        } else {
+          // dK += dS^T Q and dQ^T = K^T dS^T with dS^T from shared memory; dQ^T
+          // lands in this buffer's dP^T columns, which the row math has consumed.
+          for (int part = 0; part < parts; ++part) {
+            const uint32_t dsA = sb + C::oDS + (2 * bt + part) * C::kPTile;
+#pragma unroll
+            for (int k = 0; k < kStepQ / 16; ++k)
+              tc_mma_ss(tdK, make_sdesc(dsA + 32 * k, 16, 1024), make_sdesc(qB + 2048 * k, C::kQPanel, 1024), idG,
+                        (t > 0 || k > 0 || part > 0) ? 1u : 0u);
+          }
+          // For d = 64 the upper 64 rows of the 128-row dQ^T MMA are ignored.
+          for (int part = 0; part < parts; ++part) {
+            const uint32_t dsA = sb + C::oDS + (2 * bt + part) * C::kPTile;
 #pragma unroll
             for (int k = 0; k < kRowsKV / 16; ++k)
-              tc_mma_ss(tS + 64 * bp, make_sdesc(sb + C::oK + 2048 * k, C::kKVPanel, 1024),
+              tc_mma_ss(tdP + 64 * bt, make_sdesc(sb + C::oK + 2048 * k, C::kKVPanel, 1024),
                         make_sdesc(dsA + 2048 * k, C::kPTile, 1024), idQ, (k > 0 || part > 0) ? 1u : 0u);
           }
-          tc_commit(bar(C::bDQFull + bp));
+          tc_commit(bar(C::bDQFull + bt));
         }
-        tc_commit(bar(C::bPEmpty));
-        tc_commit(bar(C::bQEmpty + sp));
+        tc_commit(bar(C::bSEmpty + bt));
+        tc_commit(bar(C::bQEmpty + st));
         return true;
       };
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t qB = sb + C::oQ + s * C::kQTile, doB = sb + C::oDO + s * C::kQTile;
 #pragma unroll
@@ -222,158 +239,170 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
                     k > 0 ? 1u : 0u);
         }
         tc_commit(bar(C::bSFull + bb));
-        if (it > 0 && !grads(it - 1)) { ok = false; break; }
+        if (it > 0 && !grads(it - 1)) {
+          ok = false;
+          break;
+        }
       }
       if (ok && nsteps > 0) ok = grads(nsteps - 1);
       tc_commit(bar(C::bAcc));
       if (!ok) {
-        // Drain MMAs already issued before TMEM is released.
         tc_commit(bar(C::bDrain));
         mbar_wait_drain(bar(C::bDrain), 0, p.status);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // --------------------- softmax-gradient warpgroup + epilogue -------------
+  } else if (warp >= 4) {
+    // --------------- row-math warpgroups (alternate query steps) -------------
+    const int wg = (warp - 4) >> 2;   // 0 or 1: steps it with it % 2 == wg, TMEM buffer wg
     const int wq = warp & 3;
     const int jl = wq * 32 + lane;
     const int j = j0 + jl;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const bool drop = p.drop.threshold != 0;
+    const uint32_t tSb = tS + lane_off + 64 * wg, tdPb = tdP + lane_off + 64 * wg;
     bool ok = true;
-    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
-    const uint32_t pRow = sb + C::oP + jl * 128, dsRow = sb + C::oDS + jl * 128;
-    const uint32_t pRowLo = sb + C::oPlo + jl * 128, dsRowLo = sb + C::oDSlo + jl * 128;
-    for (int it = 0; it < nsteps; ++it) {
-      const int bb = it & 1, s = it % C::kNS;
+    for (int it = wg; it < nsteps; it += 2) {
+      const int s = it % C::kNS;
       const int i0 = i_first + it * kStepQ;
       if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
-          !mbar_wait(bar(C::bPEmpty), (it & 1) ^ 1, abort_flag, p.status)) {
+          !mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* Ls = reinterpret_cast<const float*>(smem + C::oL + s * kStepQ * 4);
-      const float* Ds = reinterpret_cast<const float*>(smem + C::oD + s * kStepQ * 4);
-      const bool need_mask = (p.causal && i0 < j0 + kRowsKV - 1) ||
-                             (p.window > 0 && i0 + kStepQ - 1 - p.window >= j0) || (j0 + kRowsKV > p.N);
-      // Pass 0 writes P~T and dS^T rounded to 16 bits; pass 1 (only when some
-      // P of the tile exceeds kSplitThreshold) recomputes them from TMEM and
-      // writes the rounding residuals.
-      float pmax = 0.f;
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) {
-          const bool mine = __any_sync(0xffffffffu, pmax > kSplitThreshold);
-          if (lane == 0) flags[wq] = mine ? 1 : 0;
-          mbar_arrive(bar(C::bVote));
-          if (!mbar_wait(bar(C::bVote), it & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const bool split = (flags[0] | flags[1] | flags[2] | flags[3]) != 0;
-          if (!split) break;
+      const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * kStepQ * 4);
+      const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + s * kStepQ * 4);
+      bool lo_any = false;
+#pragma unroll
+      for (int c = 0; c < kStepQ / 32; ++c) {
+        const int base = i0 + 32 * c;
+        // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep bits
+        uint32_t allow = 0u;
+        if (j < p.N) {
+          const int lo = p.causal ? j - base : 0;
+          int hi = p.N - base;
+          if (p.window > 0) hi = min(hi, j + p.window - base);
+          allow = bit_range(lo, hi);
         }
+        uint32_t keep = 0xFFFFFFFFu;
+        if constexpr (kDrop) keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tSb + 32 * c, sr);
+        tmem_ld32(tdPb + 32 * c, dr);
+        tmem_ld_wait2(sr, dr);
+        float cmax = 0.f;
+        float pt[32], ds[32];
 #pragma unroll
-        for (int c = 0; c < kStepQ / 32; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + 64 * bb + 32 * c, sr);
-          tmem_ld32(tmem + lane_off + 128 + 64 * bb + 32 * c, dr);
-          tmem_ld_wait2(sr, dr);
-          const uint32_t keep = drop ? keep_bits_for_key(p.drop, bh, p.N, i0 + 32 * c, j) : 0xFFFFFFFFu;
-          const float rp = drop ? p.drop.rp : 1.f;
-          uint32_t pp[16], dd[16];
+        for (int x = 0; x < 32; x += 4) {
+          const float4 l4 = L4[(32 * c + x) >> 2], d4 = D4[(32 * c + x) >> 2];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            float pt[2], ds[2];
-#pragma unroll
-            for (int y = 0; y < 2; ++y) {
-              const int col = 32 * c + x + y;
-              const int i = i0 + col;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -Ls[col]));
-              if (need_mask && !pair_allowed(p, i, j)) pv = 0.f;
-              pmax = fmaxf(pmax, pv);
+          for (int y = 0; y < 4; ++y) {
+            const bool on = (allow >> (x + y)) & 1u;
+            const float pv = on ? ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y])) : 0.f;
+            cmax = fmaxf(cmax, pv);
+            float dpv = __uint_as_float(dr[x + y]);
+            float ptv = pv;
+            if constexpr (kDrop) {
               const bool kept = (keep >> (x + y)) & 1u;
-              const float dpv = kept ? __uint_as_float(dr[x + y]) * rp : 0.f;
-              const float ptv = kept ? pv * rp : 0.f;
-              pt[y] = ptv;
-              ds[y] = pv * (dpv - Ds[col]);
+              dpv = kept ? dpv * p.drop.rp : 0.f;
+              ptv = kept ? pv * p.drop.rp : 0.f;
             }
-            const uint32_t ph = pack2<kBf16>(pt[0], pt[1]), dh = pack2<kBf16>(ds[0], ds[1]);
-            pp[x >> 1] = pass ? pack2_residual<kBf16>(pt[0], pt[1], ph) : ph;
-            dd[x >> 1] = pass ? pack2_residual<kBf16>(ds[0], ds[1], dh) : dh;
+            ds[x + y] = pv * (dpv - dv[y]);
+            pt[x + y] = ptv;
           }
-          const uint32_t pr = pass ? pRowLo : pRow, dr2 = pass ? dsRowLo : dsRow;
+        }
+        uint32_t hp[16], hd[16], ep[16], ed[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          hp[x] = pack2<kBf16>(pt[2 * x], pt[2 * x + 1]);
+          hd[x] = pack2<kBf16>(ds[2 * x], ds[2 * x + 1]);
+        }
+        // Residuals only where this warp's rows hold a probability above the
+        // split threshold; zeros elsewhere keep the residual tile well defined.
+        const bool split_c = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        lo_any |= split_c;
+        if (split_c) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            ep[x] = pack2_residual<kBf16>(pt[2 * x], pt[2 * x + 1], hp[x]);
+            ed[x] = pack2_residual<kBf16>(ds[2 * x], ds[2 * x + 1], hd[x]);
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) ep[x] = ed[x] = 0u;
+        }
+        // Rounded + residual image over the 32 S^T (dP^T) columns just read.
+        uint32_t img[32];
+        interleave_split(hp, ep, img);
+        tmem_st32(tSb + 32 * c, img);
+        if constexpr (!kAtomic) {
+          interleave_split(hd, ed, img);
+          tmem_st32(tdPb + 32 * c, img);
+        } else {
+          // dS^T row jl into the shared tiles (128-byte rows, 128-byte swizzle)
+          const uint32_t row = sb + C::oDS + (2 * wg) * C::kPTile + jl * 128;
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const uint32_t chunk = (uint32_t)((4 * c + t) ^ (jl & 7)) << 4;
-            st_shared_v4(pr + chunk, pp[4 * t], pp[4 * t + 1], pp[4 * t + 2], pp[4 * t + 3]);
-            st_shared_v4(dr2 + chunk, dd[4 * t], dd[4 * t + 1], dd[4 * t + 2], dd[4 * t + 3]);
+            st_shared_v4(row + chunk, hd[4 * t], hd[4 * t + 1], hd[4 * t + 2], hd[4 * t + 3]);
+            st_shared_v4(row + C::kPTile + chunk, ed[4 * t], ed[4 * t + 1], ed[4 * t + 2], ed[4 * t + 3]);
           }
         }
       }
-      if (!ok) break;
+      tmem_st_wait();
+      if (lane == 0) flags[4 * wg + wq] = lo_any ? 1 : 0;
       tc_fence_before();
-      mbar_arrive(bar(C::bSEmpty + bb));
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::bPFull));
+      if constexpr (kAtomic) fence_proxy_async_smem();
+      mbar_arrive(bar(C::bPFull + wg));
+      if constexpr (kAtomic) {
+        // dQ^T (d on lanes, 64 queries on columns) -> fp32 accumulator in HBM.
+        if (!mbar_wait(bar(C::bDQFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tdPb, r0);
+        tmem_ld32(tdPb + 32, r1);
+        tmem_ld_wait2(r0, r1);
+        tc_fence_before();
+        mbar_arrive(bar(C::bSEmpty + wg));
+        if (jl < D) {
+          float* dst = p.ws_dq + ((long long)bh * p.n_pad + i0) * D + jl;
+#pragma unroll
+          for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
+#pragma unroll
+          for (int x = 0; x < 32; ++x) atomicAdd(dst + (32 + x) * D, __uint_as_float(r1[x]));
+        }
+      }
     }
-    // Epilogue: dV and scale * dK, rounded to the tensor dtype, one key row per thread.
+    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK.
     if (ok && nsteps > 0) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const long long off = (long long)b * p.sb + (long long)j * p.sn + (long long)h * p.sh;
-      uint16_t* dv = static_cast<uint16_t*>(p.dv) + off;
-      uint16_t* dk = static_cast<uint16_t*>(p.dk) + off;
+      uint16_t* dst = static_cast<uint16_t*>(wg ? p.dk : p.dv) + off;
+      const uint32_t col0 = wg ? (tdK + lane_off) : (tdV + lane_off);
+      const float mul = wg ? p.scale : 1.f;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col0 = 256 + which * D;
-        const float mul = which ? p.scale : 1.f;
-        uint16_t* dst = which ? dk : dv;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (nsteps > 0) {
+          tmem_ld32(col0 + 32 * c, r);
+          tmem_ld_wait(r);
+        } else {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          if (nsteps > 0) {
-            tmem_ld32(tmem + lane_off + col0 + 32 * c, r);
-            tmem_ld_wait(r);
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = 0u;
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
-          if (j < p.N) {
-            uint4* g = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-          }
+          for (int x = 0; x < 32; ++x) r[x] = 0u;
         }
-      }
-    }
-  } else if (kAtomic && warp >= 8) {
-    // ------------------ dQ drain: TMEM dQ^T -> fp32 HBM accumulator ----------
-    const int wq = warp & 3;
-    const int dd = wq * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    for (int it = 0; it < nsteps; ++it) {
-      const int bb = it & 1;
-      if (!mbar_wait(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) break;
-      tc_fence_after();
-      const int i0 = i_first + it * kStepQ;
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + lane_off + 64 * bb, r0);
-      tmem_ld32(tmem + lane_off + 64 * bb + 32, r1);
-      tmem_ld_wait2(r0, r1);
-      tc_fence_before();
-      mbar_arrive(bar(C::bSEmpty + bb));
-      if (dd < D) {
-        float* dst = p.ws_dq + ((long long)bh * p.n_pad + i0) * D + dd;
+        uint32_t w[16];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
+        if (j < p.N) {
+          uint4* g = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) atomicAdd(dst + (32 + x) * D, __uint_as_float(r1[x]));
+          for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
       }
     }
   }
@@ -387,30 +416,33 @@ __global__ void __launch_bounds__(kAtomic ? 384 : 256, 1)
   }
 }
 
-template <int D, bool kBf16, bool kAtomic>
+template <int D, bool kBf16, bool kAtomic, bool kDrop>
 static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  using C = KVCfg<D>;
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic>;
+  using C = KVCfg<D, kAtomic>;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (p.N + kRowsKV - 1) / kRowsKV;
   const unsigned grid = (unsigned)(tiles * p.B * p.H);
-  kern<<<grid, kAtomic ? 384 : 256, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, 384, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
+}
+
+template <int D, bool kBf16>
+static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, const CUtensorMap* maps, cudaStream_t st) {
+  const bool drop = p.drop.threshold != 0;
+  if (atomic)
+    return drop ? launch_dkdv_t<D, kBf16, true, true>(p, maps, st) : launch_dkdv_t<D, kBf16, true, false>(p, maps, st);
+  return drop ? launch_dkdv_t<D, kBf16, false, true>(p, maps, st) : launch_dkdv_t<D, kBf16, false, false>(p, maps, st);
 }
 
 // maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows).
 cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
                                cudaStream_t st) {
-  if (p.d == 128) {
-    if (bf16) return atomic ? launch_dkdv_t<128, true, true>(p, maps, st) : launch_dkdv_t<128, true, false>(p, maps, st);
-    return atomic ? launch_dkdv_t<128, false, true>(p, maps, st) : launch_dkdv_t<128, false, false>(p, maps, st);
-  }
-  if (bf16) return atomic ? launch_dkdv_t<64, true, true>(p, maps, st) : launch_dkdv_t<64, true, false>(p, maps, st);
-  return atomic ? launch_dkdv_t<64, false, true>(p, maps, st) : launch_dkdv_t<64, false, false>(p, maps, st);
+  if (p.d == 128)
+    return bf16 ? launch_dkdv_d<128, true>(p, atomic, maps, st) : launch_dkdv_d<128, false>(p, atomic, maps, st);
+  return bf16 ? launch_dkdv_d<64, true>(p, atomic, maps, st) : launch_dkdv_d<64, false>(p, atomic, maps, st);
 }
-
-size_t smem_bwd_dkdv_tc(int d) { return d == 128 ? KVCfg<128>::kSmem : KVCfg<64>::kSmem; }
 
 }  // namespace fa

@@ -15,8 +15,12 @@
 // so O never needs rescaling — and accumulates O += (P o Z/(1-p)) V.
 //
 // Queries sit on the 128 TMEM lanes: one thread owns one query row, so L_i and
-// D_i are per-thread scalars. Warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues MMAs, warps 4-7 run the row math and the epilogue.
+// D_i are per-thread scalars. The row math writes dS (or P~) back over the S
+// columns it has read, rounded to 16 bits with the rounding residual beside
+// it (see interleave_split), and the accumulating MMA reads it from TMEM.
+// Warp 0 issues TMA loads, warp 1 owns TMEM and issues MMAs, two row-math
+// warpgroups (warps 4-7, 8-11) take alternate key steps (warpgroup w uses TMEM
+// buffer w) and split the epilogue columns.
 //
 // TMEM columns: [0,128) S double buffer, [128,256) dP double buffer (dQ mode),
 // [256,256+d) the O or dQ accumulator.
@@ -30,34 +34,37 @@ constexpr int kModeDq = 1;
 template <int D, int kMode>
 struct QCfg {
   static constexpr int kPanels = D / 64;
-  static constexpr int kNS = (D == 128) ? 3 : 4;               // K/V pipeline stages
   static constexpr uint32_t kRowPanel = kRowsQ * 128;          // 16 KB
   static constexpr uint32_t kRowTile = kPanels * kRowPanel;
   static constexpr uint32_t kKVPanel = kStepKV * 128;          // 8 KB
   static constexpr uint32_t kKVTile = kPanels * kKVPanel;
-  static constexpr uint32_t kPTile = kRowsQ * kStepKV * 2;     // 16 KB
+  static constexpr uint32_t kResident = (kMode == kModeDq ? 2 : 1) * kRowTile;
+  static constexpr uint32_t kStats = kMode == kModeFwd ? 2 * 2 * kRowsQ * 4 : 0;
+  static constexpr uint32_t kBudget = 225u * 1024u;
+  static constexpr int kNSraw = (int)((kBudget - kResident - kStats - 2048) / (2 * kKVTile));
+  static constexpr int kNS = kNSraw > 6 ? 6 : kNSraw;          // K/V pipeline stages
   static constexpr uint32_t oQ = 0;
   static constexpr uint32_t oDO = oQ + kRowTile;
-  static constexpr uint32_t oK = oDO + (kMode == kModeDq ? kRowTile : 0);
+  static constexpr uint32_t oK = kResident;
   static constexpr uint32_t oV = oK + kNS * kKVTile;
-  static constexpr uint32_t oP = oV + kNS * kKVTile;   // P~ or dS rounded to 16 bits
-  static constexpr uint32_t oPlo = oP + kPTile;         // rounding residuals (split tiles only)
-  static constexpr uint32_t oBar = oPlo + kPTile;
+  static constexpr uint32_t oStats = oV + kNS * kKVTile;       // forward: [wg][m | l][row]
+  static constexpr uint32_t oBar = oStats + kStats;
   static constexpr int bRes = 0;
   static constexpr int bKVFull = 1;
   static constexpr int bKVEmpty = bKVFull + kNS;
   static constexpr int bSFull = bKVEmpty + kNS;
   static constexpr int bSEmpty = bSFull + 2;
   static constexpr int bPFull = bSEmpty + 2;
-  static constexpr int bPEmpty = bPFull + 1;
-  static constexpr int bAcc = bPEmpty + 1;
+  static constexpr int bAcc = bPFull + 2;
   static constexpr int bDrain = bAcc + 1;
-  static constexpr int bVote = bDrain + 1;
-  static constexpr int kBars = bVote + 1;
+  static constexpr int bStats = bDrain + 1;
+  static constexpr int kBars = bStats + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
-  static constexpr uint32_t oFlags = oAbort + 8;        // per-warp "split this tile" votes
-  static constexpr uint32_t kSmem = oFlags + 16 + 1024;
+  static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
+  static constexpr uint32_t kSmem = oFlags + 32 + 1024;
+  static_assert(kNS >= 2, "shared memory budget leaves fewer than two K/V stages");
+  static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
 
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -66,8 +73,8 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
-template <int D, bool kBf16, int kMode>
-__global__ void __launch_bounds__(256, 1)
+template <int D, bool kBf16, int kMode, bool kDrop>
+__global__ void __launch_bounds__(384, 1)
     qmajor_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmDO) {
@@ -78,6 +85,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oAbort);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
   auto bar = [&](int idx) -> uint32_t { return sb + C::oBar + 8u * idx; };
 
   // Work unit: (batch*head, query block), heaviest query blocks first under a causal mask.
@@ -102,13 +110,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::bSFull + x), 1);
-      mbar_init(bar(C::bSEmpty + x), 128);
+      mbar_init(bar(C::bSEmpty + x), 1);
+      mbar_init(bar(C::bPFull + x), 128);
     }
-    mbar_init(bar(C::bPFull), 128);
-    mbar_init(bar(C::bPEmpty), 1);
     mbar_init(bar(C::bAcc), 1);
     mbar_init(bar(C::bDrain), 1);
-    mbar_init(bar(C::bVote), 128);
+    mbar_init(bar(C::bStats), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -126,11 +133,12 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::oTmemSlot);
+  const uint32_t tS = tmem, tdP = tmem + 128, tAcc = tmem + 256;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::bRes), (kDq ? 2 : 1) * C::kRowTile);
+      mbar_arrive_expect_tx(bar(C::bRes), C::kResident);
       for (int pn = 0; pn < C::kPanels; ++pn) {
         tma_load_4d(sb + C::oQ + pn * C::kRowPanel, &tmQ, bar(C::bRes), 64 * pn, i0, h, b);
         if (kDq) tma_load_4d(sb + C::oDO + pn * C::kRowPanel, &tmDO, bar(C::bRes), 64 * pn, i0, h, b);
@@ -163,28 +171,27 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
       constexpr uint32_t idO = make_idesc(128, D, kBf16, false, true);
-      const uint32_t tS = tmem, tdP = tmem + 128, tAcc = tmem + 256;
       bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
       tc_fence_after();
-      // Second MMA of an output step: acc += (P~ or dS) . (V_j or K_j).
+      // After the row math of step t: acc += (P~ or dS) . (V_j or K_j) on output steps,
+      // then release the S/dP buffer and the K/V stage.
       auto second = [&](int t) -> bool {
-        const int u = t - first_out;
-        const int sp = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull), u & 1, abort_flag, p.status)) return false;
+        const int bt = t & 1, st = t % C::kNS;
+        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const volatile int* flags = reinterpret_cast<const volatile int*>(smem + C::oFlags);
-        const bool split = (flags[0] | flags[1] | flags[2] | flags[3]) != 0;
-        const uint32_t bOp = sb + (kDq ? C::oK : C::oV) + sp * C::kKVTile;
-        // From the rounded tile and, on split tiles, again from the residuals.
-        for (int part = 0; part < (split ? 2 : 1); ++part) {
-          const uint32_t aP = sb + (part ? C::oPlo : C::oP);
+        if (t >= first_out) {
+          const int u = t - first_out;
+          const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+          const uint32_t bOp = sb + (kDq ? C::oK : C::oV) + st * C::kKVTile;
+          for (int part = 0; part < (split ? 2 : 1); ++part) {
 #pragma unroll
-          for (int k = 0; k < kStepKV / 16; ++k)
-            tc_mma_ss(tAcc, make_sdesc(aP + 32 * k, 16, 1024), make_sdesc(bOp + 2048 * k, C::kKVPanel, 1024),
-                      idO, (u > 0 || k > 0 || part > 0) ? 1u : 0u);
+            for (int k = 0; k < kStepKV / 16; ++k)
+              tc_mma_ts(tAcc, tS + 64 * bt + 16 * k + 8 * part, make_sdesc(bOp + 2048 * k, C::kKVPanel, 1024), idO,
+                        (u > 0 || k > 0 || part > 0) ? 1u : 0u);
+          }
         }
-        tc_commit(bar(C::bPEmpty));
-        tc_commit(bar(C::bKVEmpty + sp));
+        tc_commit(bar(C::bSEmpty + bt));
+        tc_commit(bar(C::bKVEmpty + st));
         return true;
       };
       for (int it = 0; ok && it < nsteps; ++it) {
@@ -211,13 +218,12 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
         tc_commit(bar(C::bSFull + bb));
-        if (it < first_out) tc_commit(bar(C::bKVEmpty + s));  // statistics step: K no longer needed
-        if (it > first_out && !second(it - 1)) {
+        if (it > 0 && !second(it - 1)) {
           ok = false;
           break;
         }
       }
-      if (ok && nsteps > first_out) ok = second(nsteps - 1);
+      if (ok && nsteps > 0) ok = second(nsteps - 1);
       tc_commit(bar(C::bAcc));
       if (!ok) {
         tc_commit(bar(C::bDrain));
@@ -225,46 +231,62 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= 4) {
-    // ----------------------- row math + epilogue warpgroup -------------------
+    // ------------- row-math warpgroups (alternate key steps) + epilogue -------
+    const int wg = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int il = wq * 32 + lane;
     const int i = i0 + il;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const bool drop = p.drop.threshold != 0;
+    const uint32_t tSb = tS + lane_off + 64 * wg, tdPb = tdP + lane_off + 64 * wg;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
-    float L2 = 0.f, Dv = 0.f;
+    float L2 = INFINITY, Dv = 0.f;
     if (kDq) {
       L2 = p.ws_L2[ws];
       Dv = p.ws_D[ws];
     }
-    float m = -INFINITY, l = 0.f;  // forward statistics, log2 domain
-    if (!kDq) L2 = INFINITY;
-    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
+    float m = -INFINITY, l = 0.f;  // forward statistics of this warpgroup's steps, log2 domain
+    bool merged = kDq;
     bool ok = true;
-    for (int it = 0; it < nsteps; ++it) {
-      const int bb = it & 1;
+    for (int it = wg; it < nsteps; it += 2) {
       const int jt = it >= nkv ? it - nkv : it;
       const int jj0 = j_first + jt * kStepKV;
-      if (!mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+      if (!kDq && it >= first_out && !merged) {
+        // Combine the two warpgroups' partial row statistics into L.
+        float* st = reinterpret_cast<float*>(smem + C::oStats);
+        st[(2 * wg) * kRowsQ + il] = m;
+        st[(2 * wg + 1) * kRowsQ + il] = l;
+        mbar_arrive(bar(C::bStats));
+        if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const float mo = st[(2 * (1 - wg)) * kRowsQ + il], lo = st[(2 * (1 - wg) + 1) * kRowsQ + il];
+        const float mm = fmaxf(m, mo);
+        const float ll = (mm == -INFINITY) ? 0.f
+                                           : l * ex2_approx(m - mm) + lo * ex2_approx(mo - mm);
+        L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
+        merged = true;
+      }
+      if (!mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
-      const bool need_mask = (p.causal && jj0 + kStepKV - 1 > i0) ||
-                             (p.window > 0 && jj0 <= i0 + kRowsQ - 1 - p.window) || (jj0 + kStepKV > p.N);
+      tc_fence_after();
       if (!kDq && it < first_out) {
         // statistics step
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kStepKV / 32; ++c) {
+          const int base = jj0 + 32 * c;
+          const uint32_t allow =
+              bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
           uint32_t sr[32];
-          tmem_ld32(tmem + lane_off + 64 * bb + 32 * c, sr);
+          tmem_ld32(tSb + 32 * c, sr);
           tmem_ld_wait(sr);
           float x[32];
           float mx = m;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            x[e] = __uint_as_float(sr[e]) * p.scale_log2;
-            if (need_mask && !pair_allowed(p, i, jj0 + 32 * c + e)) x[e] = -INFINITY;
+            x[e] = ((allow >> e) & 1u) ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
             mx = fmaxf(mx, x[e]);
           }
           if (mx != -INFINITY) {
@@ -276,81 +298,75 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bar(C::bSEmpty + bb));
-        if (it == first_out - 1) L2 = (l > 0.f) ? m + lg2_approx(l) : INFINITY;
+        mbar_arrive(bar(C::bPFull + wg));
         continue;
       }
-      const int u = it - first_out;
-      if (!mbar_wait(bar(C::bPEmpty), (u & 1) ^ 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // Pass 0 writes the tile (P~ or dS) rounded to 16 bits; pass 1 (only when
-      // some P of the tile exceeds kSplitThreshold) recomputes it from TMEM and
-      // writes the rounding residuals.
-      float pmax = 0.f;
-#pragma unroll 1
-      for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) {
-          const bool mine = __any_sync(0xffffffffu, pmax > kSplitThreshold);
-          if (lane == 0) flags[wq] = mine ? 1 : 0;
-          mbar_arrive(bar(C::bVote));
-          if (!mbar_wait(bar(C::bVote), u & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if ((flags[0] | flags[1] | flags[2] | flags[3]) == 0) break;
-        }
-        const uint32_t pRow = sb + (pass ? C::oPlo : C::oP) + il * 128;
+      bool lo_any = false;
 #pragma unroll
-        for (int c = 0; c < kStepKV / 32; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + 64 * bb + 32 * c, sr);
-          if (kDq) {
-            tmem_ld32(tmem + lane_off + 128 + 64 * bb + 32 * c, dr);
-            tmem_ld_wait2(sr, dr);
+      for (int c = 0; c < kStepKV / 32; ++c) {
+        const int base = jj0 + 32 * c;
+        const uint32_t allow =
+            bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
+        uint32_t keep = 0xFFFFFFFFu;
+        if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tSb + 32 * c, sr);
+        if constexpr (kDq) {
+          tmem_ld32(tdPb + 32 * c, dr);
+          tmem_ld_wait2(sr, dr);
+        } else {
+          tmem_ld_wait(sr);
+        }
+        float outv[32];
+        float cmax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool on = (allow >> e) & 1u;
+          const float pv = on ? ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, -L2)) : 0.f;
+          cmax = fmaxf(cmax, pv);
+          const bool kept = !kDrop || ((keep >> e) & 1u);
+          const float rp = kDrop ? p.drop.rp : 1.f;
+          if constexpr (kDq) {
+            const float dpv = kept ? __uint_as_float(dr[e]) * rp : 0.f;
+            outv[e] = pv * (dpv - Dv);
           } else {
-            tmem_ld_wait(sr);
-          }
-          uint32_t pk[16];
-          const uint32_t keep = drop ? keep_bits_for_query(p.drop, bh, p.N, i, jj0 + 32 * c) : 0xFFFFFFFFu;
-          const float rp = drop ? p.drop.rp : 1.f;
-#pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            const int jb = jj0 + 32 * c + x;
-            float outv[4];
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -L2));
-              if (need_mask && !pair_allowed(p, i, jb + y)) pv = 0.f;
-              pmax = fmaxf(pmax, pv);
-              const bool kept = (keep >> (x + y)) & 1u;
-              if constexpr (kDq) {
-                const float dpv = kept ? __uint_as_float(dr[x + y]) * rp : 0.f;
-                outv[y] = pv * (dpv - Dv);
-              } else {
-                outv[y] = kept ? pv * rp : 0.f;
-              }
-            }
-            const uint32_t h0 = pack2<kBf16>(outv[0], outv[1]), h1 = pack2<kBf16>(outv[2], outv[3]);
-            pk[x >> 1] = pass ? pack2_residual<kBf16>(outv[0], outv[1], h0) : h0;
-            pk[(x >> 1) + 1] = pass ? pack2_residual<kBf16>(outv[2], outv[3], h1) : h1;
-          }
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t chunk = (uint32_t)((4 * c + t) ^ (il & 7)) << 4;
-            st_shared_v4(pRow + chunk, pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+            outv[e] = kept ? pv * rp : 0.f;
           }
         }
+        uint32_t hv[16], ev[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
+        const bool split_c = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        lo_any |= split_c;
+        if (split_c) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) ev[x] = pack2_residual<kBf16>(outv[2 * x], outv[2 * x + 1], hv[x]);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) ev[x] = 0u;
+        }
+        uint32_t img[32];
+        interleave_split(hv, ev, img);
+        tmem_st32(tSb + 32 * c, img);
       }
-      if (!ok) break;
+      tmem_st_wait();
+      if (lane == 0) flags[4 * wg + wq] = lo_any ? 1 : 0;
       tc_fence_before();
-      mbar_arrive(bar(C::bSEmpty + bb));
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::bPFull));
+      mbar_arrive(bar(C::bPFull + wg));
     }
-    // Epilogue: O (forward) or scale * dQ, one query row per thread.
+    if (!kDq && ok && !merged) {
+      // This warpgroup saw no output step (tiny key ranges): still publish its statistics.
+      float* st = reinterpret_cast<float*>(smem + C::oStats);
+      st[(2 * wg) * kRowsQ + il] = m;
+      st[(2 * wg + 1) * kRowsQ + il] = l;
+      mbar_arrive(bar(C::bStats));
+      if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) ok = false;
+      const float mo = st[(2 * (1 - wg)) * kRowsQ + il], lo = st[(2 * (1 - wg) + 1) * kRowsQ + il];
+      const float mm = fmaxf(m, mo);
+      const float ll = (mm == -INFINITY) ? 0.f : l * ex2_approx(m - mm) + lo * ex2_approx(mo - mm);
+      L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
+    }
+    // Epilogue: O (forward) or scale * dQ; warpgroup w writes columns [w*d/2, (w+1)*d/2).
     const bool have_acc = nsteps > first_out;
     if (ok && have_acc) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
@@ -359,10 +375,11 @@ __global__ void __launch_bounds__(256, 1)
       uint16_t* dst = static_cast<uint16_t*>(p.out) + off;
       const float mul = kDq ? p.scale : 1.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = wg * (D / 2) + 32 * c;
         uint32_t r[32];
         if (have_acc) {
-          tmem_ld32(tmem + lane_off + 256 + 32 * c, r);
+          tmem_ld32(tAcc + lane_off + col, r);
           tmem_ld_wait(r);
         } else {
 #pragma unroll
@@ -373,12 +390,12 @@ __global__ void __launch_bounds__(256, 1)
         for (int x = 0; x < 16; ++x)
           w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
         if (i < p.N) {
-          uint4* g = reinterpret_cast<uint4*>(dst + 32 * c);
+          uint4* g = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
         }
       }
-      if (!kDq && i < p.N)
+      if (!kDq && wg == 0 && i < p.N)
         p.lse_out[(long long)bh * p.N + i] = (L2 == INFINITY) ? -INFINITY : L2 * 0.6931471805599453f;
     }
   }
@@ -392,33 +409,33 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode>
+template <int D, bool kBf16, int kMode, bool kDrop>
 static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   using C = QCfg<D, kMode>;
-  auto kern = qmajor_kernel<D, kBf16, kMode>;
+  auto kern = qmajor_kernel<D, kBf16, kMode, kDrop>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (p.N + kRowsQ - 1) / kRowsQ;
   const unsigned grid = (unsigned)(tiles * p.B * p.H);
-  kern<<<grid, 256, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, 384, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
+}
+
+template <int D, bool kBf16>
+static cudaError_t launch_q_d(const AttnParams& p, bool dq_mode, const CUtensorMap* maps, cudaStream_t st) {
+  const bool drop = p.drop.threshold != 0;
+  if (dq_mode)
+    return drop ? launch_q_t<D, kBf16, kModeDq, true>(p, maps, st) : launch_q_t<D, kBf16, kModeDq, false>(p, maps, st);
+  return drop ? launch_q_t<D, kBf16, kModeFwd, true>(p, maps, st) : launch_q_t<D, kBf16, kModeFwd, false>(p, maps, st);
 }
 
 // maps: Q, K, V, dO (Q/dO boxes of kRowsQ rows, K/V boxes of kStepKV rows).
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st) {
-  if (p.d == 128) {
-    if (bf16) return dq_mode ? launch_q_t<128, true, kModeDq>(p, maps, st) : launch_q_t<128, true, kModeFwd>(p, maps, st);
-    return dq_mode ? launch_q_t<128, false, kModeDq>(p, maps, st) : launch_q_t<128, false, kModeFwd>(p, maps, st);
-  }
-  if (bf16) return dq_mode ? launch_q_t<64, true, kModeDq>(p, maps, st) : launch_q_t<64, true, kModeFwd>(p, maps, st);
-  return dq_mode ? launch_q_t<64, false, kModeDq>(p, maps, st) : launch_q_t<64, false, kModeFwd>(p, maps, st);
-}
-
-size_t smem_qmajor_tc(int d, bool dq_mode) {
-  if (d == 128) return dq_mode ? QCfg<128, kModeDq>::kSmem : QCfg<128, kModeFwd>::kSmem;
-  return dq_mode ? QCfg<64, kModeDq>::kSmem : QCfg<64, kModeFwd>::kSmem;
+  if (p.d == 128)
+    return bf16 ? launch_q_d<128, true>(p, dq_mode, maps, st) : launch_q_d<128, false>(p, dq_mode, maps, st);
+  return bf16 ? launch_q_d<64, true>(p, dq_mode, maps, st) : launch_q_d<64, false>(p, dq_mode, maps, st);
 }
 
 }  // namespace fa
