@@ -238,6 +238,11 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory descriptor advanced by a byte offset (the start address field
+// is the low 14 bits of the descriptor, in 16-byte units; shared addresses stay
+// below 2^18 bytes, so the addition never carries out of that field).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // 32 lanes x 32 consecutive 32-bit columns; thread t of the warp gets lane (base lane + t).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

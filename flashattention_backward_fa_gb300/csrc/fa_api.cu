@@ -7,7 +7,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 #include "fa_internal.h"
 
 namespace fa {

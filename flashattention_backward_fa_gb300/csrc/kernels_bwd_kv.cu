@@ -15,20 +15,22 @@
 //   with red.add ("FlashAttention backward" §The loop structure, choice (a)).
 //
 // Keys sit on the 128 TMEM lanes: one thread owns one key row of S^T and dP^T.
-// The row math writes P~T and dS^T back into the TMEM columns it has just read
-// (rounded to 16 bits, two per column, plus the rounding residual when a
-// tile holds probabilities above kSplitThreshold), and dV / dK take them as
-// the A operand straight from TMEM. In atomic mode dS^T also goes to shared
-// memory, where it is the B operand of dQ^T and the A operand of dK.
+// The row math turns them into P~T and dS^T, each rounded to 16 bits plus the
+// rounding residual where a tile holds probabilities above kSplitThreshold
+// (see interleave_split), and writes them back over the TMEM columns it has
+// just read: dV and dK take them as the A operand straight from TMEM. In
+// atomic mode dS^T goes to shared memory instead, where it is the A operand
+// of dK and the B operand of dQ^T.
 //
-// Warp roles: warp 0 issues TMA loads, warp 1 owns TMEM and issues MMAs, two
-// row-math warpgroups (warps 4-7, 8-11) take alternate query steps so that
-// one computes while the other waits on the tensor cores; warpgroup w always
-// uses TMEM buffer w. They also drain dQ^T in atomic mode and write the
-// dV (warpgroup 0) / dK (warpgroup 1) epilogue.
+// Warp roles: warp 0 issues TMA loads; warp 1 owns TMEM and issues the S^T and
+// dP^T MMAs; warp 2 issues the dV / dK (and dQ^T) MMAs, so that the two MMA
+// streams are issued in parallel; two row-math warpgroups (warps 4-7, 8-11)
+// take alternate query steps, warpgroup w using buffer w. They also drain dQ^T
+// in atomic mode and write the dV (warpgroup 0) / dK (warpgroup 1) epilogue.
 //
-// TMEM columns (512): S^T/P buffers [0,64) and [64,128), dP^T/dS (or dQ^T in
-// atomic mode) buffers [128,192) and [192,256), dV [256,256+d), dK [256+d,256+2d).
+// TMEM columns (512): S^T buffers [0,64) and [64,128), dP^T buffers [128,192)
+// and [192,256) (dS^T image, or dQ^T in atomic mode, later in the step),
+// dV [256,256+d), dK [256+d,256+2d).
 #include "fa_internal.h"
 
 namespace fa {
@@ -41,17 +43,17 @@ struct KVCfg {
   static constexpr uint32_t kQPanel = kStepQ * 128;            // 8 KB: 64 rows x 64 elements
   static constexpr uint32_t kQTile = kPanels * kQPanel;
   static constexpr uint32_t kPTile = kRowsKV * kStepQ * 2;     // 16 KB: 128 keys x 64 queries
-  static constexpr uint32_t kDSBytes = kAtomic ? 4 * kPTile : 0;  // dS^T rounded + residual, x2 buffers
+  static constexpr uint32_t kImgBytes = kAtomic ? 4 * kPTile : 0;  // dS^T [buffer][rounded, residual]
   static constexpr uint32_t kStageBytes = 2 * kQTile + 2 * kStepQ * 4;
-  static constexpr uint32_t kBudget = 225u * 1024u;
-  static constexpr int kNSraw = (int)((kBudget - 2 * kKVTile - kDSBytes - 2048) / kStageBytes);
+  static constexpr uint32_t kFixed = 2 * kKVTile + kImgBytes + 512 + 1024;
+  static constexpr int kNSraw = (int)((227u * 1024u - kFixed) / kStageBytes);
   static constexpr int kNS = kNSraw > 4 ? 4 : kNSraw;          // Q/dO pipeline stages
   static constexpr uint32_t oK = 0;
   static constexpr uint32_t oV = oK + kKVTile;
   static constexpr uint32_t oQ = oV + kKVTile;
   static constexpr uint32_t oDO = oQ + kNS * kQTile;
-  static constexpr uint32_t oDS = oDO + kNS * kQTile;          // [buffer][rounded, residual] tiles
-  static constexpr uint32_t oL = oDS + kDSBytes;
+  static constexpr uint32_t oImg = oDO + kNS * kQTile;
+  static constexpr uint32_t oL = oImg + kImgBytes;
   static constexpr uint32_t oD = oL + kNS * kStepQ * 4;
   static constexpr uint32_t oBar = oD + kNS * kStepQ * 4;
   static constexpr int bKV = 0;
@@ -59,11 +61,13 @@ struct KVCfg {
   static constexpr int bQEmpty = bQFull + kNS;
   static constexpr int bSFull = bQEmpty + kNS;
   static constexpr int bSEmpty = bSFull + 2;
-  static constexpr int bPFull = bSEmpty + 2;
-  static constexpr int bDQFull = bPFull + 2;
+  static constexpr int bDPEmpty = bSEmpty + 2;
+  static constexpr int bPFull = bDPEmpty + 2;
+  static constexpr int bPEmpty = bPFull + 2;
+  static constexpr int bDQFull = bPEmpty + 2;
   static constexpr int bAcc = bDQFull + 2;
-  static constexpr int bDrain = bAcc + 1;
-  static constexpr int kBars = bDrain + 1;
+  static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
+  static constexpr int kBars = bDrain + 2;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
@@ -71,6 +75,16 @@ struct KVCfg {
   static_assert(kNS >= 2, "shared memory budget leaves fewer than two Q/dO stages");
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
+
+// One row of a 128-row x 64-element, 128-byte-swizzled shared tile: chunk t of
+// the 32 elements [32c, 32c+32) goes to 16-byte slot (4c + t) ^ (row & 7).
+__device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row, int c, const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t slot = (uint32_t)((4 * c + t) ^ (row & 7)) << 4;
+    st_shared_v4(row_addr + slot, v[4 * t], v[4 * t + 1], v[4 * t + 2], v[4 * t + 3]);
+  }
+}
 
 template <int D, bool kBf16, bool kAtomic, bool kDrop>
 __global__ void __launch_bounds__(384, 1)
@@ -105,12 +119,14 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::bSFull + x), 1);
-      mbar_init(bar(C::bSEmpty + x), kAtomic ? 1 + 128 : 1);
+      mbar_init(bar(C::bSEmpty + x), 1);                       // dV done with the P~T image
+      mbar_init(bar(C::bDPEmpty + x), kAtomic ? 128 : 1);     // dK done / dQ^T drained
       mbar_init(bar(C::bPFull + x), 128);
+      mbar_init(bar(C::bPEmpty + x), 1);                       // atomic: shared dS^T free
       mbar_init(bar(C::bDQFull + x), 1);
+      mbar_init(bar(C::bDrain + x), 1);
     }
     mbar_init(bar(C::bAcc), 1);
-    mbar_init(bar(C::bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -163,108 +179,127 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer --------------------------------
+    // ------------------------ S^T / dP^T MMA issuer ---------------------------
     if (lane == 0) {
-      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);   // S^T, dP^T
-      constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);         // dV, dK
-      constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);     // dQ^T
+      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
+      const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
+      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
       bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
-      tc_fence_after();
-      auto grads = [&](int t) -> bool {
-        const int bt = t & 1, st = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
-        const uint32_t doB = sb + C::oDO + st * C::kQTile, qB = sb + C::oQ + st * C::kQTile;
-        const int parts = split ? 2 : 1;
-        // dV += P~T dO: A = P~T from TMEM; K step k reads the 8 rounded columns at
-        // 16k and, on split tiles, the 8 residual columns at 16k + 8.
-        for (int part = 0; part < parts; ++part) {
-#pragma unroll
-          for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ts(tdV, tS + 64 * bt + 16 * k + 8 * part, make_sdesc(doB + 2048 * k, C::kQPanel, 1024), idG,
-                      (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-        }
-        if constexpr (!kAtomic) {
-          // dK += dS^T Q: A = dS^T from TMEM, same column image.
-          for (int part = 0; part < parts; ++part) {
-#pragma unroll
-            for (int k = 0; k < kStepQ / 16; ++k)
-              tc_mma_ts(tdK, tdP + 64 * bt + 16 * k + 8 * part, make_sdesc(qB + 2048 * k, C::kQPanel, 1024),
-                        idG, (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-          }
-        } else {
-          // dK += dS^T Q and dQ^T = K^T dS^T with dS^T from shared memory; dQ^T
-          // lands in this buffer's dP^T columns, which the row math has consumed.
-          for (int part = 0; part < parts; ++part) {
-            const uint32_t dsA = sb + C::oDS + (2 * bt + part) * C::kPTile;
-#pragma unroll
-            for (int k = 0; k < kStepQ / 16; ++k)
-              tc_mma_ss(tdK, make_sdesc(dsA + 32 * k, 16, 1024), make_sdesc(qB + 2048 * k, C::kQPanel, 1024), idG,
-                        (t > 0 || k > 0 || part > 0) ? 1u : 0u);
-          }
-          // For d = 64 the upper 64 rows of the 128-row dQ^T MMA are ignored.
-          for (int part = 0; part < parts; ++part) {
-            const uint32_t dsA = sb + C::oDS + (2 * bt + part) * C::kPTile;
-#pragma unroll
-            for (int k = 0; k < kRowsKV / 16; ++k)
-              tc_mma_ss(tdP + 64 * bt, make_sdesc(sb + C::oK + 2048 * k, C::kKVPanel, 1024),
-                        make_sdesc(dsA + 2048 * k, C::kPTile, 1024), idQ, (k > 0 || part > 0) ? 1u : 0u);
-          }
-          tc_commit(bar(C::bDQFull + bt));
-        }
-        tc_commit(bar(C::bSEmpty + bt));
-        tc_commit(bar(C::bQEmpty + st));
-        return true;
-      };
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
+        const uint32_t par = ((it >> 1) & 1) ^ 1;
         if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+            !mbar_wait(bar(C::bSEmpty + bb), par, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t qB = sb + C::oQ + s * C::kQTile, doB = sb + C::oDO + s * C::kQTile;
+        const uint64_t q = desc_add(dQ0, s * C::kQTile), g = desc_add(dO0, s * C::kQTile);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKVPanel + (k & 3) * 32, qo = (k >> 2) * C::kQPanel + (k & 3) * 32;
-          tc_mma_ss(tS + 64 * bb, make_sdesc(sb + C::oK + ko, 16, 1024), make_sdesc(qB + qo, 16, 1024), idS,
-                    k > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKVPanel + (k & 3) * 32, qo = (k >> 2) * C::kQPanel + (k & 3) * 32;
-          tc_mma_ss(tdP + 64 * bb, make_sdesc(sb + C::oV + ko, 16, 1024), make_sdesc(doB + qo, 16, 1024), idS,
-                    k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(C::bSFull + bb));
-        if (it > 0 && !grads(it - 1)) {
+        for (int k = 0; k < D / 16; ++k)
+          tc_mma_ss(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                    desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        if (!mbar_wait(bar(C::bDPEmpty + bb), par, abort_flag, p.status)) {
           ok = false;
           break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          tc_mma_ss(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                    desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit(bar(C::bSFull + bb));
       }
-      if (ok && nsteps > 0) ok = grads(nsteps - 1);
-      tc_commit(bar(C::bAcc));
       if (!ok) {
         tc_commit(bar(C::bDrain));
         mbar_wait_drain(bar(C::bDrain), 0, p.status);
       }
     }
+  } else if (warp == 2) {
+    // ----------------------- dV / dK (/ dQ^T) MMA issuer ----------------------
+    if (lane == 0) {
+      constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);         // dV, dK
+      constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);     // dQ^T
+      const uint64_t mQ0 = make_sdesc(sb + C::oQ, C::kQPanel, 1024), mO0 = make_sdesc(sb + C::oDO, C::kQPanel, 1024);
+      const uint64_t mK0 = make_sdesc(sb + C::oK, C::kKVPanel, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < nsteps; ++t) {
+        const int bt = t & 1, st = t % C::kNS;
+        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+        const uint32_t first = t > 0 ? 1u : 0u;
+        const uint64_t q = desc_add(mQ0, st * C::kQTile), g = desc_add(mO0, st * C::kQTile);
+        // dV += P~T dO: K step k reads the 8 rounded columns at 16k of the P~T image
+        // and, on split tiles, the 8 residual columns at 16k + 8.
+#pragma unroll
+        for (int k = 0; k < kStepQ / 16; ++k)
+          tc_mma_ts(tdV, tS + 64 * bt + 16 * k, desc_add(g, 2048 * k), idG, k > 0 ? 1u : first);
+        if (split) {
+#pragma unroll
+          for (int k = 0; k < kStepQ / 16; ++k)
+            tc_mma_ts(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
+        }
+        tc_commit(bar(C::bSEmpty + bt));
+        if constexpr (!kAtomic) {
+          // dK += dS^T Q from the dS^T image over the dP^T columns.
+#pragma unroll
+          for (int k = 0; k < kStepQ / 16; ++k)
+            tc_mma_ts(tdK, tdP + 64 * bt + 16 * k, desc_add(q, 2048 * k), idG, k > 0 ? 1u : first);
+          if (split) {
+#pragma unroll
+            for (int k = 0; k < kStepQ / 16; ++k)
+              tc_mma_ts(tdK, tdP + 64 * bt + 16 * k + 8, desc_add(q, 2048 * k), idG, 1u);
+          }
+          tc_commit(bar(C::bDPEmpty + bt));
+        } else {
+          // dK += dS^T Q and dQ^T = K^T dS^T from the shared dS^T tiles; dQ^T lands in
+          // this buffer's dP^T columns, which the row math has consumed. For d = 64
+          // the upper 64 rows of the 128-row dQ^T MMA are ignored.
+          const uint32_t img = sb + C::oImg + 2 * bt * C::kPTile;
+          const uint64_t aK = make_sdesc(img, 16, 1024), bQT = make_sdesc(img, C::kPTile, 1024);
+          for (int part = 0; part < (split ? 2 : 1); ++part) {
+#pragma unroll
+            for (int k = 0; k < kStepQ / 16; ++k)
+              tc_mma_ss(tdK, desc_add(aK, part * C::kPTile + 32 * k), desc_add(q, 2048 * k), idG,
+                        (k > 0 || part > 0) ? 1u : first);
+          }
+          for (int part = 0; part < (split ? 2 : 1); ++part) {
+#pragma unroll
+            for (int k = 0; k < kRowsKV / 16; ++k)
+              tc_mma_ss(tdP + 64 * bt, desc_add(mK0, 2048 * k), desc_add(bQT, part * C::kPTile + 2048 * k), idQ,
+                        (k > 0 || part > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::bDQFull + bt));
+          tc_commit(bar(C::bPEmpty + bt));
+        }
+        tc_commit(bar(C::bQEmpty + st));
+      }
+      tc_commit(bar(C::bAcc));
+      if (!ok) {
+        tc_commit(bar(C::bDrain + 1));
+        mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+      }
+    }
   } else if (warp >= 4) {
     // --------------- row-math warpgroups (alternate query steps) -------------
-    const int wg = (warp - 4) >> 2;   // 0 or 1: steps it with it % 2 == wg, TMEM buffer wg
+    const int wg = (warp - 4) >> 2;   // 0 or 1: steps it with it % 2 == wg, buffer wg
     const int wq = warp & 3;
     const int jl = wq * 32 + lane;
     const int j = j0 + jl;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tSb = tS + lane_off + 64 * wg, tdPb = tdP + lane_off + 64 * wg;
+    const uint32_t imgRow = sb + C::oImg + 2 * wg * C::kPTile + jl * 128;
     bool ok = true;
     for (int it = wg; it < nsteps; it += 2) {
       const int s = it % C::kNS;
       const int i0 = i_first + it * kStepQ;
       if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
+          !mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status) ||
+          (kAtomic && !mbar_wait(bar(C::bPEmpty + wg), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -318,7 +353,7 @@ __global__ void __launch_bounds__(384, 1)
           hd[x] = pack2<kBf16>(ds[2 * x], ds[2 * x + 1]);
         }
         // Residuals only where this warp's rows hold a probability above the
-        // split threshold; zeros elsewhere keep the residual tile well defined.
+        // split threshold; zeros elsewhere keep the residual image well defined.
         const bool split_c = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
         lo_any |= split_c;
         if (split_c) {
@@ -331,22 +366,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int x = 0; x < 16; ++x) ep[x] = ed[x] = 0u;
         }
-        // Rounded + residual image over the 32 S^T (dP^T) columns just read.
-        uint32_t img[32];
-        interleave_split(hp, ep, img);
-        tmem_st32(tSb + 32 * c, img);
+        // P~T image over the S^T columns just read.
+        uint32_t timg[32];
+        interleave_split(hp, ep, timg);
+        tmem_st32(tSb + 32 * c, timg);
         if constexpr (!kAtomic) {
-          interleave_split(hd, ed, img);
-          tmem_st32(tdPb + 32 * c, img);
+          // dS^T image over the dP^T columns just read.
+          interleave_split(hd, ed, timg);
+          tmem_st32(tdPb + 32 * c, timg);
         } else {
-          // dS^T row jl into the shared tiles (128-byte rows, 128-byte swizzle)
-          const uint32_t row = sb + C::oDS + (2 * wg) * C::kPTile + jl * 128;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t chunk = (uint32_t)((4 * c + t) ^ (jl & 7)) << 4;
-            st_shared_v4(row + chunk, hd[4 * t], hd[4 * t + 1], hd[4 * t + 2], hd[4 * t + 3]);
-            st_shared_v4(row + C::kPTile + chunk, ed[4 * t], ed[4 * t + 1], ed[4 * t + 2], ed[4 * t + 3]);
-          }
+          store_tile_row_chunk(imgRow, jl, c, hd);
+          store_tile_row_chunk(imgRow + C::kPTile, jl, c, ed);
         }
       }
       tmem_st_wait();
@@ -366,7 +396,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tdPb + 32, r1);
         tmem_ld_wait2(r0, r1);
         tc_fence_before();
-        mbar_arrive(bar(C::bSEmpty + wg));
+        mbar_arrive(bar(C::bDPEmpty + wg));
         if (jl < D) {
           float* dst = p.ws_dq + ((long long)bh * p.n_pad + i0) * D + jl;
 #pragma unroll

@@ -17,13 +17,16 @@
 // Queries sit on the 128 TMEM lanes: one thread owns one query row, so L_i and
 // D_i are per-thread scalars. The row math writes dS (or P~) back over the S
 // columns it has read, rounded to 16 bits with the rounding residual beside
-// it (see interleave_split), and the accumulating MMA reads it from TMEM.
-// Warp 0 issues TMA loads, warp 1 owns TMEM and issues MMAs, two row-math
-// warpgroups (warps 4-7, 8-11) take alternate key steps (warpgroup w uses TMEM
-// buffer w) and split the epilogue columns.
+// it (see interleave_split), and the accumulating MMA reads it from TMEM. S
+// rotates over three TMEM buffers, so the S MMA of step it + 3 waits only for
+// the accumulating MMA of step it; dP rotates over two buffers that the row
+// math releases as soon as it has read them.
+// Warp 0 issues TMA loads, warp 1 owns TMEM and issues the S (and dP) MMAs,
+// warp 2 issues the accumulating MMAs, two row-math warpgroups (warps 4-7,
+// 8-11) take alternate key steps and split the epilogue columns.
 //
-// TMEM columns: [0,128) S double buffer, [128,256) dP double buffer (dQ mode),
-// [256,256+d) the O or dQ accumulator.
+// TMEM columns: [0,192) three S buffers, [192,320) two dP buffers (dQ mode),
+// [320,320+d) the O or dQ accumulator.
 #include "fa_internal.h"
 
 namespace fa {
@@ -53,11 +56,12 @@ struct QCfg {
   static constexpr int bKVFull = 1;
   static constexpr int bKVEmpty = bKVFull + kNS;
   static constexpr int bSFull = bKVEmpty + kNS;
-  static constexpr int bSEmpty = bSFull + 2;
-  static constexpr int bPFull = bSEmpty + 2;
+  static constexpr int bSEmpty = bSFull + 3;
+  static constexpr int bDPEmpty = bSEmpty + 3;
+  static constexpr int bPFull = bDPEmpty + 2;
   static constexpr int bAcc = bPFull + 2;
-  static constexpr int bDrain = bAcc + 1;
-  static constexpr int bStats = bDrain + 1;
+  static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
+  static constexpr int bStats = bDrain + 2;
   static constexpr int kBars = bStats + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
@@ -108,13 +112,17 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::bKVFull + s), 1);
       mbar_init(bar(C::bKVEmpty + s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < 3; ++x) {
       mbar_init(bar(C::bSFull + x), 1);
       mbar_init(bar(C::bSEmpty + x), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::bDPEmpty + x), 128);
       mbar_init(bar(C::bPFull + x), 128);
     }
     mbar_init(bar(C::bAcc), 1);
     mbar_init(bar(C::bDrain), 1);
+    mbar_init(bar(C::bDrain + 1), 1);
     mbar_init(bar(C::bStats), 256);
     *abort_flag = 0;
     fence_mbar_init();
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::oTmemSlot);
-  const uint32_t tS = tmem, tdP = tmem + 128, tAcc = tmem + 256;
+  const uint32_t tS = tmem, tdP = tmem + 192, tAcc = tmem + 320;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
@@ -167,67 +175,78 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer --------------------------------
+    // ---------------------------- S / dP MMA issuer ---------------------------
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
-      constexpr uint32_t idO = make_idesc(128, D, kBf16, false, true);
+      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
+      const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
       bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
-      tc_fence_after();
-      // After the row math of step t: acc += (P~ or dS) . (V_j or K_j) on output steps,
-      // then release the S/dP buffer and the K/V stage.
-      auto second = [&](int t) -> bool {
-        const int bt = t & 1, st = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        if (t >= first_out) {
-          const int u = t - first_out;
-          const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
-          const uint32_t bOp = sb + (kDq ? C::oK : C::oV) + st * C::kKVTile;
-          for (int part = 0; part < (split ? 2 : 1); ++part) {
-#pragma unroll
-            for (int k = 0; k < kStepKV / 16; ++k)
-              tc_mma_ts(tAcc, tS + 64 * bt + 16 * k + 8 * part, make_sdesc(bOp + 2048 * k, C::kKVPanel, 1024), idO,
-                        (u > 0 || k > 0 || part > 0) ? 1u : 0u);
-          }
-        }
-        tc_commit(bar(C::bSEmpty + bt));
-        tc_commit(bar(C::bKVEmpty + st));
-        return true;
-      };
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int s = it % C::kNS, bb = it & 1;
+        const int s = it % C::kNS, bb = it & 1, bs = it % 3;
         if (!mbar_wait(bar(C::bKVFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+            !mbar_wait(bar(C::bSEmpty + bs), ((it / 3) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kB = sb + C::oK + s * C::kKVTile, vB = sb + C::oV + s * C::kKVTile;
+        const uint64_t kd = desc_add(dK0, s * C::kKVTile), vd = desc_add(dV0, s * C::kKVTile);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t qo = (k >> 2) * C::kRowPanel + (k & 3) * 32, ko = (k >> 2) * C::kKVPanel + (k & 3) * 32;
-          tc_mma_ss(tS + 64 * bb, make_sdesc(sb + C::oQ + qo, 16, 1024), make_sdesc(kB + ko, 16, 1024), idS,
-                    k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          tc_mma_ss(tS + 64 * bs, desc_add(dQ0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
+                    desc_add(kd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
         if constexpr (kDq) {
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t qo = (k >> 2) * C::kRowPanel + (k & 3) * 32, ko = (k >> 2) * C::kKVPanel + (k & 3) * 32;
-            tc_mma_ss(tdP + 64 * bb, make_sdesc(sb + C::oDO + qo, 16, 1024), make_sdesc(vB + ko, 16, 1024), idS,
-                      k > 0 ? 1u : 0u);
+          if (!mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            tc_mma_ss(tdP + 64 * bb, desc_add(dO0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
+                      desc_add(vd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::bSFull + bb));
-        if (it > 0 && !second(it - 1)) {
-          ok = false;
-          break;
-        }
+        tc_commit(bar(C::bSFull + bs));
       }
-      if (ok && nsteps > 0) ok = second(nsteps - 1);
-      tc_commit(bar(C::bAcc));
       if (!ok) {
         tc_commit(bar(C::bDrain));
         mbar_wait_drain(bar(C::bDrain), 0, p.status);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------ accumulating MMA issuer (O or dQ) ---------------------
+    // After the row math of step t: acc += (P~ or dS) . (V_j or K_j) on output
+    // steps, then release the S buffer and the K/V stage.
+    if (lane == 0) {
+      constexpr uint32_t idO = make_idesc(128, D, kBf16, false, true);
+      const uint64_t b0 = make_sdesc(sb + (kDq ? C::oK : C::oV), C::kKVPanel, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < nsteps; ++t) {
+        const int bt = t & 1, bs = t % 3, st = t % C::kNS;
+        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (t >= first_out) {
+          const uint32_t first = t > first_out ? 1u : 0u;
+          const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+          const uint64_t bop = desc_add(b0, st * C::kKVTile);
+#pragma unroll
+          for (int k = 0; k < kStepKV / 16; ++k)
+            tc_mma_ts(tAcc, tS + 64 * bs + 16 * k, desc_add(bop, 2048 * k), idO, k > 0 ? 1u : first);
+          if (split) {
+#pragma unroll
+            for (int k = 0; k < kStepKV / 16; ++k)
+              tc_mma_ts(tAcc, tS + 64 * bs + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
+          }
+        }
+        tc_commit(bar(C::bSEmpty + bs));
+        tc_commit(bar(C::bKVEmpty + st));
+      }
+      tc_commit(bar(C::bAcc));
+      if (!ok) {
+        tc_commit(bar(C::bDrain + 1));
+        mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
       }
     }
   } else if (warp >= 4) {
@@ -237,7 +256,7 @@ __global__ void __launch_bounds__(384, 1)
     const int il = wq * 32 + lane;
     const int i = i0 + il;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tSb = tS + lane_off + 64 * wg, tdPb = tdP + lane_off + 64 * wg;
+    const uint32_t tdPb = tdP + lane_off + 64 * wg;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
     float L2 = INFINITY, Dv = 0.f;
     if (kDq) {
@@ -267,7 +286,8 @@ __global__ void __launch_bounds__(384, 1)
         L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
         merged = true;
       }
-      if (!mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
+      const uint32_t tSb = tS + lane_off + 64 * (it % 3);
+      if (!mbar_wait(bar(C::bSFull + it % 3), (it / 3) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -314,6 +334,11 @@ __global__ void __launch_bounds__(384, 1)
         if constexpr (kDq) {
           tmem_ld32(tdPb + 32 * c, dr);
           tmem_ld_wait2(sr, dr);
+          if (c == kStepKV / 32 - 1) {
+            // every dP column of this buffer is in registers: the next dP may land
+            tc_fence_before();
+            mbar_arrive(bar(C::bDPEmpty + wg));
+          }
         } else {
           tmem_ld_wait(sr);
         }
