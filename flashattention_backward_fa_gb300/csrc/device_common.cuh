@@ -192,6 +192,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 8 consecutive 32-bit columns of this thread's lane from r[off .. off+8).
+template <int off, int n>
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[n]) {
+  static_assert(off + 8 <= n, "range");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[off]), "r"(r[off + 1]), "r"(r[off + 2]), "r"(r[off + 3]), "r"(r[off + 4]), "r"(r[off + 5]),
+               "r"(r[off + 6]), "r"(r[off + 7])
+               : "memory");
+}
+
+// Writes the split image of 32 elements (see interleave_split) to the 32
+// columns at taddr: rounded pairs r, residual pairs e.
+__device__ __forceinline__ void tmem_st_split(uint32_t taddr, const uint32_t (&r)[16], const uint32_t (&e)[16]) {
+  tmem_st8<0>(taddr, r);
+  tmem_st8<0>(taddr + 8, e);
+  tmem_st8<8>(taddr + 16, r);
+  tmem_st8<8>(taddr + 24, e);
+}
+
 // TMEM image of a 16-bit MMA operand split into a rounded part and a residual:
 // per 16-element K step, 8 columns of rounded values followed by 8 columns of
 // residuals. A chunk of 32 elements therefore occupies exactly the 32 columns
