@@ -63,6 +63,8 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd_stage.argtypes, lib.fa_bwd_stage.restype = [i] + bwd_args, i
     lib.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
     lib.fa_get_device_status.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp]
+    lib.fa_bwd_noalloc.restype = i
     _lib = lib
     return lib
 
@@ -156,6 +158,23 @@ def fa_bwd_stage(stage, q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, 
     _check(load_library().fa_bwd_stage(int(stage), *_bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal,
                                                               window, dropout_p, seed, offset, deterministic,
                                                               workspace, stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale=None, causal=False, window=0, dropout_p=0.0, seed=0,
+                   offset=0, stream=None):
+    """Deterministic backward with the library's fixed internal scratch instead of a workspace.
+
+    For callers that cannot allocate device memory when they run the backward.
+    Limit B*H*roundup(N,128) <= 1048576; calls sharing a device must not overlap.
+    """
+    (B, N, H, d), st = _same_layout(q, k, v, o, do, dq, dk, dv)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _check(load_library().fa_bwd_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+        dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
+        default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p), int(seed),
+        int(offset), _stream(stream)))
 
 
 def fa_get_device_status(clear: bool = True) -> int:

@@ -121,6 +121,24 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
                  uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
                  void* stream);
 
+/* fa_bwd_noalloc: the deterministic backward for callers that cannot allocate
+ * device memory when they run it (a pre-planned memory arena that forbids new
+ * allocations, a runtime recording work before any allocator exists, an
+ * embedding that hands over only the tensors). The pages describe no such
+ * entry point; it is this library's own. Arguments as fa_bwd, without the
+ * deterministic flag (always deterministic) and without a workspace: the
+ * scratch (D and lse*log2(e) vectors) lives in one fixed 8 MiB device array
+ * inside the library, so the call allocates nothing. Limit:
+ * B*H*roundup(N,128) <= 1048576; larger problems return FA_ERR_WORKSPACE and
+ * launch nothing. All calls on a device share the array (each call overwrites
+ * what it reads, nothing needs clearing); calls that overlap on the GPU race,
+ * so order them. The first call on a device looks up the array's address
+ * (once per device): make it before any stream capture. */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                   uint64_t seed, uint64_t offset, void* stream);
+
 /* Reads (and with clear != 0 resets) the status word of the current device.
  * Call after synchronising the streams the kernels ran on. *status receives
  * the raw bits (1 = a bounded wait timed out). Returns FA_OK, FA_ERR_TIMEOUT
