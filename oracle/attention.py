@@ -155,6 +155,77 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
     return dQ, dK, dV, D
 
 
+def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+    """O[b, rows, h, :] and L[b, h, rows] of one head: the same definitions as
+    :func:`forward`, evaluated for the listed query rows only (rows are independent)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, d = q.shape
+    scale = float(np.float32(scale))
+    rows = np.asarray(rows, dtype=np.int64)
+    ok = allowed(rows, N, causal, window)
+    S = np.where(ok, scale * (q[b, rows, h, :] @ k[b, :, h, :].T), -np.inf)
+    m = S.max(axis=1)
+    live = np.isfinite(m)
+    ms = np.where(live, m, 0.0)
+    E = np.where(ok, np.exp(S - ms[:, None]), 0.0)
+    lse = np.where(live, ms + np.log(np.where(live, E.sum(axis=1), 1.0)), -np.inf)
+    P = np.where(ok, np.exp(S - np.where(live, lse, 0.0)[:, None]), 0.0)
+    zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
+    Pt = P if zs is None else P * zs
+    return Pt @ v[b, :, h, :], lse
+
+
+def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0,
+                  offset=0):
+    """dQ[b, rows, h, :] of one head from the given O and L (function mode), by the
+    definitions of :func:`backward` restricted to the listed query rows."""
+    q, k, v, o, do = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do)
+    lse = _f64(lse)
+    B, N, H, d = q.shape
+    scale = float(np.float32(scale))
+    rows = np.asarray(rows, dtype=np.int64)
+    ok = allowed(rows, N, causal, window)
+    Lr = lse[b, h, rows]
+    live = np.isfinite(Lr)
+    S = scale * (q[b, rows, h, :] @ k[b, :, h, :].T)
+    P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
+    D = np.einsum("rd,rd->r", do[b, rows, h, :], o[b, rows, h, :])
+    dP = do[b, rows, h, :] @ v[b, :, h, :].T
+    zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
+    if zs is not None:
+        dP = dP * zs
+    dS = P * (dP - D[:, None])
+    return scale * (dS @ k[b, :, h, :])
+
+
+def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0, dropout_p=0.0, seed=0,
+                  offset=0):
+    """(dK, dV)[b, cols, h, :] of one head from the given O and L (function mode):
+    the definitions of :func:`backward` restricted to the listed key rows, which
+    need the column slice P[:, cols] over all query rows."""
+    q, k, v, o, do = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do)
+    lse = _f64(lse)
+    B, N, H, d = q.shape
+    scale = float(np.float32(scale))
+    cols = np.asarray(cols, dtype=np.int64)
+    rows = np.arange(N)
+    ok = allowed(rows, N, causal, window)[:, cols]
+    Lr = lse[b, h, :]
+    live = np.isfinite(Lr)
+    S = scale * (q[b, :, h, :] @ k[b, cols, h, :].T)
+    P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
+    D = np.einsum("nd,nd->n", do[b, :, h, :], o[b, :, h, :])
+    zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
+    if zs is not None:
+        zs = zs[:, cols]
+    Pt = P if zs is None else P * zs
+    dP = do[b, :, h, :] @ v[b, cols, h, :].T
+    if zs is not None:
+        dP = dP * zs
+    dS = P * (dP - D[:, None])
+    return scale * (dS.T @ q[b, :, h, :]), Pt.T @ do[b, :, h, :]
+
+
 def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
     """Exact mode: forward in float64, then backward from that O and L."""
     O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset)
@@ -162,4 +233,5 @@ def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, s
     return O, L, dQ, dK, dV, D
 
 
-__all__ = ["allowed", "forward", "backward", "preprocess_D", "reference_grads"]
+__all__ = ["allowed", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows", "backward_rows",
+           "backward_cols"]

@@ -1,0 +1,137 @@
+"""Parity of the five full-size workloads against the float64 oracle.
+
+The GPU runs every workload at its full size. The oracle checks what it can
+compute cheaply at that size: whole heads for the smaller workloads, and for
+the long ones the dQ rows and dK / dV rows of sampled queries and keys
+(first, last and random positions) of sampled heads, plus the forward's O and
+L on the same rows. Deterministic mode is also checked for bit-identical
+results over ten runs at the headline size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import flashattention_backward_fa_gb300 as fa
+import oracle
+from flashattention_backward_fa_gb300.inputs import WORKLOADS, make_inputs
+from gpu_check import LSE_ATOL, check_against_oracle, to_np, within
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(w, deterministic=True):
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
+              offset=w.philox_offset)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=deterministic)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(clear=True) == 0
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    return dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+
+
+def _positions(N, rng, n_random=32):
+    edge = list(range(min(8, N))) + list(range(max(0, N - 8), N))
+    return np.unique(np.concatenate([edge, rng.integers(0, N, n_random)])).astype(np.int64)
+
+
+def _head_arrays(res, b, h, full=False):
+    """float64 numpy arrays of one head, as [1, N, 1, d] (or the whole tensors when full)."""
+    out = {}
+    for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv"):
+        t = res[n] if full else res[n][b:b + 1, :, h:h + 1, :]
+        out[n] = to_np(t)
+    lse = res["lse"] if full else res["lse"][b:b + 1, h:h + 1]
+    out["lse"] = lse.double().cpu().numpy()
+    return out
+
+
+def _check_sampled(w, res, heads, seed=0):
+    rng = np.random.default_rng(seed)
+    args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
+    full = w.dropout_p > 0  # dropout counters depend on (b, h, H): keep the whole tensors
+    failures = []
+    for (b, h) in heads:
+        a = _head_arrays(res, b, h, full)
+        bb, hh = (b, h) if full else (0, 0)
+        rows = _positions(w.N, rng)
+        o_r, l_r = oracle.forward_rows(a["q"], a["k"], a["v"], bb, hh, rows, *args)
+        ok, rep = within(a["o"][bb, rows, hh], o_r, w.dtype)
+        lerr = float(np.abs(a["lse"][bb, hh, rows] - l_r).max())
+        if not ok or lerr > LSE_ATOL:
+            failures.append(("forward", b, h, rep, lerr))
+        dq_r = oracle.backward_rows(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], bb, hh, rows, *args)
+        ok, rep = within(a["dq"][bb, rows, hh], dq_r, w.dtype)
+        if not ok:
+            failures.append(("dq", b, h, rep))
+        cols = _positions(w.N, rng)
+        dk_c, dv_c = oracle.backward_cols(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], bb, hh, cols, *args)
+        for name, r in (("dk", dk_c), ("dv", dv_c)):
+            ok, rep = within(a[name][bb, cols, hh], r, w.dtype)
+            if not ok:
+                failures.append((name, b, h, rep))
+    return failures
+
+
+def test_fp32_n128_d64_full():
+    w = WORKLOADS["fp32_n128_d64"]
+    from gpu_check import run_gpu
+    res = run_gpu(w)
+    failures, report = check_against_oracle(w, res)
+    assert not failures, (failures, report)
+
+
+@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+def test_bf16_causal_b4h16_n2048_whole_heads(deterministic):
+    w = WORKLOADS["bf16_causal_b4h16_n2048_d128"]
+    res = _gpu(w, deterministic)
+    args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
+    for (b, h) in ((0, 0), (1, 7), (2, 11), (3, 15)):
+        a = _head_arrays(res, b, h)
+        rq, rk, rv, _ = oracle.backward(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], *args)
+        for name, r in (("dq", rq), ("dk", rk), ("dv", rv)):
+            ok, rep = within(a[name], r, w.dtype)
+            assert ok, (b, h, name, rep)
+
+
+@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+def test_bf16_causal_b1h32_n8192_sampled(deterministic):
+    w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
+    res = _gpu(w, deterministic)
+    failures = _check_sampled(w, res, [(0, 0), (0, 13), (0, 31)], seed=1)
+    assert not failures, failures
+
+
+def test_bf16_causal_b1h8_n32768_sampled():
+    w = WORKLOADS["bf16_causal_b1h8_n32768_d128"]
+    res = _gpu(w)
+    failures = _check_sampled(w, res, [(0, 0), (0, 5)], seed=2)
+    assert not failures, failures
+    # small-gradient regime: also hold the sampled rows to a relative bar
+    a = _head_arrays(res, 0, 0)
+    rows = np.arange(0, w.N, 997)
+    dq_r = oracle.backward_rows(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], 0, 0, rows, w.scale, True)
+    rel = np.linalg.norm(a["dq"][0, rows, 0] - dq_r) / np.linalg.norm(dq_r)
+    assert rel < 1e-2, rel
+
+
+def test_fp16_window_dropout_b2h16_n4096_sampled():
+    w = WORKLOADS["fp16_window1024_drop0.1_b2h16_n4096_d64"]
+    for det in (True, False):
+        res = _gpu(w, det)
+        failures = _check_sampled(w, res, [(0, 0), (1, 15)], seed=3)
+        assert not failures, (det, failures)
+
+
+def test_headline_deterministic_bit_identical_ten_runs():
+    w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    ws = fa.alloc_workspace(q, True)
+    ref = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws)
+    for _ in range(9):
+        again = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws)
+        for a_, b_ in zip(ref, again):
+            assert torch.equal(a_, b_)

@@ -231,3 +231,23 @@ def test_row_panels_match_whole_matrix(monkeypatch):
     parts = oa.reference_grads(q, k, v, do, 0.3, True, 9, 0.2, 3, 1)
     for a, b in zip(whole, parts):
         np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,window,p", [(True, 0, 0.0), (False, 0, 0.0), (True, 6, 0.3)])
+def test_sampled_rows_and_columns_match_whole_head(causal, window, p):
+    """The row / column restrictions used for full-size checks reproduce the whole-head results."""
+    B, N, H, d = 2, 29, 3, 8
+    q, k, v, do = (_rand((B, N, H, d), 1300 + t) for t in range(4))
+    O, L = oracle.forward(q, k, v, 0.3, causal, window, p, 9, 2)
+    dQ, dK, dV, _ = oracle.backward(q, k, v, O, do, L, 0.3, causal, window, p, 9, 2)
+    rows = [0, 3, 17, 28]
+    for b in range(B):
+        for h in range(H):
+            o_r, l_r = oracle.forward_rows(q, k, v, b, h, rows, 0.3, causal, window, p, 9, 2)
+            np.testing.assert_allclose(o_r, O[b, rows, h], rtol=1e-13, atol=1e-14)
+            np.testing.assert_allclose(l_r, L[b, h, rows], rtol=1e-13, atol=1e-14)
+            dq_r = oracle.backward_rows(q, k, v, O, do, L, b, h, rows, 0.3, causal, window, p, 9, 2)
+            np.testing.assert_allclose(dq_r, dQ[b, rows, h], rtol=1e-12, atol=1e-13)
+            dk_c, dv_c = oracle.backward_cols(q, k, v, O, do, L, b, h, rows, 0.3, causal, window, p, 9, 2)
+            np.testing.assert_allclose(dk_c, dK[b, rows, h], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(dv_c, dV[b, rows, h], rtol=1e-12, atol=1e-13)
