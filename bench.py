@@ -50,6 +50,23 @@ def causal_pairs(w) -> float:
     return counted_flops(w) / (10.0 * w.d)
 
 
+def dkdv_traffic(w, deterministic: bool):
+    """DRAM bytes per launch of the key/value-major kernel from the committed ncu capture,
+    scaled to this workload's head count; None unless the kernel source still matches
+    the capture (and for the atomic variant, which that capture does not cover)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dkdv_traffic.json")
+    if not deterministic or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    csrc = os.path.join(ROOT, "flashattention_backward_fa_gb300", "csrc")
+    src = b"".join(open(os.path.join(csrc, n), "rb").read() for n in ("kernels_bwd_kv.cu", "device_common.cuh"))
+    if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["dram_bytes_per_launch_capture"] * (w.B * w.H) / rec["heads_in_capture"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -309,7 +326,8 @@ def main():
         "stages_ms": {"preprocess": r["stage_ms"][0], "dkdv": r["stage_ms"][1],
                       ("dq_qmajor" if det else "dq_convert"): r["stage_ms"][2]},
         "roofline": {"kernel": "bwd_dkdv (key/value-major, tcgen05)", "bound": "tensor", "achieved": kv_tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": kv_tflops / peak, "traffic": None,
+                     "peak": peak, "unit": "TFLOP/s", "frac": kv_tflops / peak,
+                     "traffic": dkdv_traffic(w, det),
                      "peak_source": f"{peak_src} burst bf16"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
