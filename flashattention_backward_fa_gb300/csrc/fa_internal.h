@@ -3,6 +3,8 @@
 
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace fa {

@@ -22,9 +22,10 @@
 // atomic mode dS^T goes to shared memory instead, where it is the A operand
 // of dK and the B operand of dQ^T.
 //
-// Warp roles: warp 0 issues TMA loads; warp 1 owns TMEM and issues the S^T and
-// dP^T MMAs; warp 2 issues the dV / dK (and dQ^T) MMAs, so that the two MMA
-// streams are issued in parallel; two row-math warpgroups (warps 4-7, 8-11)
+// Warp roles: warp 0 issues TMA loads; warp 1 owns TMEM and issues the S^T
+// MMAs, warp 3 the dP^T MMAs and warp 2 the dV / dK (and dQ^T) MMAs, so that
+// the three MMA streams are issued in parallel (one thread issues at most about
+// one MMA per 50 cycles); two row-math warpgroups (warps 4-7, 8-11)
 // take alternate query steps, warpgroup w using buffer w. They also drain dQ^T
 // in atomic mode and write the dV (warpgroup 0) / dK (warpgroup 1) epilogue.
 //
@@ -67,7 +68,7 @@ struct KVCfg {
   static constexpr int bDQFull = bPEmpty + 2;
   static constexpr int bAcc = bDQFull + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
-  static constexpr int kBars = bDrain + 2;
+  static constexpr int kBars = bDrain + 3;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
@@ -118,14 +119,14 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::bQEmpty + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::bSFull + x), 1);
+      mbar_init(bar(C::bSFull + x), 2);                       // S^T and dP^T both landed
       mbar_init(bar(C::bSEmpty + x), 1);                       // dV done with the P~T image
       mbar_init(bar(C::bDPEmpty + x), kAtomic ? 128 : 1);     // dK done / dQ^T drained
       mbar_init(bar(C::bPFull + x), 128);
       mbar_init(bar(C::bPEmpty + x), 1);                       // atomic: shared dS^T free
       mbar_init(bar(C::bDQFull + x), 1);
-      mbar_init(bar(C::bDrain + x), 1);
     }
+    for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bAcc), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -179,31 +180,46 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------ S^T / dP^T MMA issuer ---------------------------
+    // ------------------------------ S^T MMA issuer -----------------------------
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
-      const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
-      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
+      const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
       bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        const uint32_t par = ((it >> 1) & 1) ^ 1;
         if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bSEmpty + bb), par, abort_flag, p.status)) {
+            !mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t q = desc_add(dQ0, s * C::kQTile), g = desc_add(dO0, s * C::kQTile);
+        const uint64_t q = desc_add(dQ0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ss(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
                     desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        if (!mbar_wait(bar(C::bDPEmpty + bb), par, abort_flag, p.status)) {
+        tc_commit(bar(C::bSFull + bb));
+      }
+      if (!ok) {
+        tc_commit(bar(C::bDrain));
+        mbar_wait_drain(bar(C::bDrain), 0, p.status);
+      }
+    }
+  } else if (warp == 3) {
+    // ----------------------------- dP^T MMA issuer -----------------------------
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
+      const uint64_t dV0 = make_sdesc(sb + C::oV, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
+      bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
+      for (int it = 0; ok && it < nsteps; ++it) {
+        const int s = it % C::kNS, bb = it & 1;
+        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint64_t g = desc_add(dO0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ss(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
@@ -211,8 +227,8 @@ __global__ void __launch_bounds__(384, 1)
         tc_commit(bar(C::bSFull + bb));
       }
       if (!ok) {
-        tc_commit(bar(C::bDrain));
-        mbar_wait_drain(bar(C::bDrain), 0, p.status);
+        tc_commit(bar(C::bDrain + 2));
+        mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
       }
     }
   } else if (warp == 2) {
@@ -326,26 +342,34 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld_wait2(sr, dr);
         float cmax = 0.f;
         float pt[32], ds[32];
+        // P, dropout and dS for the 32 pairs of this chunk; the unmasked
+        // variant skips the per-pair mask test on full tiles.
+        auto elementwise = [&](auto masked) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 4) {
-          const float4 l4 = L4[(32 * c + x) >> 2], d4 = D4[(32 * c + x) >> 2];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          for (int x = 0; x < 32; x += 4) {
+            const float4 l4 = L4[(32 * c + x) >> 2], d4 = D4[(32 * c + x) >> 2];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const bool on = (allow >> (x + y)) & 1u;
-            const float pv = on ? ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y])) : 0.f;
-            cmax = fmaxf(cmax, pv);
-            float dpv = __uint_as_float(dr[x + y]);
-            float ptv = pv;
-            if constexpr (kDrop) {
-              const bool kept = (keep >> (x + y)) & 1u;
-              dpv = kept ? dpv * p.drop.rp : 0.f;
-              ptv = kept ? pv * p.drop.rp : 0.f;
+            for (int y = 0; y < 4; ++y) {
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
+              if constexpr (decltype(masked)::value) pv = ((allow >> (x + y)) & 1u) ? pv : 0.f;
+              cmax = fmaxf(cmax, pv);
+              float dpv = __uint_as_float(dr[x + y]);
+              float ptv = pv;
+              if constexpr (kDrop) {
+                const bool kept = (keep >> (x + y)) & 1u;
+                dpv = kept ? dpv * p.drop.rp : 0.f;
+                ptv = kept ? pv * p.drop.rp : 0.f;
+              }
+              ds[x + y] = pv * (dpv - dv[y]);
+              pt[x + y] = ptv;
             }
-            ds[x + y] = pv * (dpv - dv[y]);
-            pt[x + y] = ptv;
           }
-        }
+        };
+        if (allow == 0xFFFFFFFFu)
+          elementwise(std::false_type{});
+        else
+          elementwise(std::true_type{});
         uint32_t hp[16], hd[16], ep[16], ed[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
