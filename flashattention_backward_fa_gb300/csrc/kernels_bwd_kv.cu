@@ -25,7 +25,7 @@
 // Warp roles: warp 0 issues TMA loads; warp 1 owns TMEM and issues the S^T
 // MMAs, warp 3 the dP^T MMAs and warp 2 the dV / dK (and dQ^T) MMAs, so that
 // the three MMA streams are issued in parallel (one thread issues at most about
-// one MMA per 50 cycles); two row-math warpgroups (warps 4-7, 8-11)
+// one MMA per 50 cycles); four row-math warpgroups (warps 4-19)
 // take alternate query steps, warpgroup w using buffer w. They also drain dQ^T
 // in atomic mode and write the dV (warpgroup 0) / dK (warpgroup 1) epilogue.
 //
@@ -35,6 +35,8 @@
 #include "fa_internal.h"
 
 namespace fa {
+
+constexpr int kKVThreads = 640;  // 4 role warps + 4 row-math warpgroups
 
 template <int D, bool kAtomic>
 struct KVCfg {
@@ -72,7 +74,7 @@ struct KVCfg {
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
-  static constexpr uint32_t kSmem = oFlags + 32 + 1024;        // + slack for 1024-byte alignment
+  static constexpr uint32_t kSmem = oFlags + 64 + 1024;        // + slack for 1024-byte alignment
   static_assert(kNS >= 2, "shared memory budget leaves fewer than two Q/dO stages");
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
@@ -88,7 +90,7 @@ __device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row,
 }
 
 template <int D, bool kBf16, bool kAtomic, bool kDrop>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kKVThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmDO) {
@@ -121,8 +123,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::bSFull + x), 2);                       // S^T and dP^T both landed
       mbar_init(bar(C::bSEmpty + x), 1);                       // dV done with the P~T image
-      mbar_init(bar(C::bDPEmpty + x), kAtomic ? 128 : 1);     // dK done / dQ^T drained
-      mbar_init(bar(C::bPFull + x), 128);
+      mbar_init(bar(C::bDPEmpty + x), kAtomic ? 256 : 1);     // dK done / dQ^T drained
+      mbar_init(bar(C::bPFull + x), 256);                      // two warpgroups per step
       mbar_init(bar(C::bPEmpty + x), 1);                       // atomic: shared dS^T free
       mbar_init(bar(C::bDQFull + x), 1);
     }
@@ -246,7 +248,9 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+        bool split = false;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) split |= flags[8 * bt + x] != 0;
         const uint32_t first = t > 0 ? 1u : 0u;
         const uint64_t q = desc_add(mQ0, st * C::kQTile), g = desc_add(mO0, st * C::kQTile);
         // dV += P~T dO: K step k reads the 8 rounded columns at 16k of the P~T image
@@ -301,63 +305,70 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp >= 4) {
-    // --------------- row-math warpgroups (alternate query steps) -------------
-    const int wg = (warp - 4) >> 2;   // 0 or 1: steps it with it % 2 == wg, buffer wg
+    // ------------------------- row-math warpgroups --------------------------
+    // Four warpgroups: rg = 0, 1 take the even query steps (TMEM buffer 0) and
+    // rg = 2, 3 the odd ones (buffer 1); within a pair, warpgroup rg & 1 takes
+    // query columns [32 (rg & 1), 32 (rg & 1) + 32) of the step. Each works in
+    // halves of 16 columns (one MMA K step).
+    const int rg = (warp - 4) >> 2;
     const int wq = warp & 3;
+    const int c = rg & 1;
+    const int bb = rg >> 1;
     const int jl = wq * 32 + lane;
     const int j = j0 + jl;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tSb = tS + lane_off + 64 * wg, tdPb = tdP + lane_off + 64 * wg;
-    const uint32_t imgRow = sb + C::oImg + 2 * wg * C::kPTile + jl * 128;
+    const uint32_t tSc = tS + lane_off + 64 * bb + 32 * c, tdPc = tdP + lane_off + 64 * bb + 32 * c;
+    const uint32_t imgRow = sb + C::oImg + 2 * bb * C::kPTile + jl * 128;
     bool ok = true;
-    for (int it = wg; it < nsteps; it += 2) {
+    for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
       const int i0 = i_first + it * kStepQ;
       if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !mbar_wait(bar(C::bSFull + wg), (it >> 1) & 1, abort_flag, p.status) ||
-          (kAtomic && !mbar_wait(bar(C::bPEmpty + wg), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
+          !mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
+          (kAtomic && !mbar_wait(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * kStepQ * 4);
-      const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + s * kStepQ * 4);
+      const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * kStepQ * 4 + 128 * c);
+      const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + s * kStepQ * 4 + 128 * c);
+      const int base = i0 + 32 * c;
+      // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep bits
+      uint32_t allow = 0u;
+      if (j < p.N) {
+        const int lo = p.causal ? j - base : 0;
+        int hi = p.N - base;
+        if (p.window > 0) hi = min(hi, j + p.window - base);
+        allow = bit_range(lo, hi);
+      }
+      uint32_t keep = 0xFFFFFFFFu;
+      if constexpr (kDrop) keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
       bool lo_any = false;
 #pragma unroll
-      for (int c = 0; c < kStepQ / 32; ++c) {
-        const int base = i0 + 32 * c;
-        // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep bits
-        uint32_t allow = 0u;
-        if (j < p.N) {
-          const int lo = p.causal ? j - base : 0;
-          int hi = p.N - base;
-          if (p.window > 0) hi = min(hi, j + p.window - base);
-          allow = bit_range(lo, hi);
-        }
-        uint32_t keep = 0xFFFFFFFFu;
-        if constexpr (kDrop) keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tSb + 32 * c, sr);
-        tmem_ld32(tdPb + 32 * c, dr);
-        tmem_ld_wait2(sr, dr);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[16], dr[16];
+        tmem_ld16(tSc + 16 * hh, sr);
+        tmem_ld16(tdPc + 16 * hh, dr);
+        tmem_ld_wait16x2(sr, dr);
         float cmax = 0.f;
-        float pt[32], ds[32];
-        // P, dropout and dS for the 32 pairs of this chunk; the unmasked
-        // variant skips the per-pair mask test on full tiles.
+        float pt[16], ds[16];
+        // P, dropout and dS for the 16 pairs; the unmasked variant skips the
+        // per-pair mask test on full tiles.
         auto elementwise = [&](auto masked) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            const float4 l4 = L4[(32 * c + x) >> 2], d4 = D4[(32 * c + x) >> 2];
+          for (int x = 0; x < 16; x += 4) {
+            const float4 l4 = L4[(16 * hh + x) >> 2], d4 = D4[(16 * hh + x) >> 2];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
             for (int y = 0; y < 4; ++y) {
+              const int bit = 16 * hh + x + y;
               float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
-              if constexpr (decltype(masked)::value) pv = ((allow >> (x + y)) & 1u) ? pv : 0.f;
+              if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
               cmax = fmaxf(cmax, pv);
               float dpv = __uint_as_float(dr[x + y]);
               float ptv = pv;
               if constexpr (kDrop) {
-                const bool kept = (keep >> (x + y)) & 1u;
+                const bool kept = (keep >> bit) & 1u;
                 dpv = kept ? dpv * p.drop.rp : 0.f;
                 ptv = kept ? pv * p.drop.rp : 0.f;
               }
@@ -370,79 +381,82 @@ __global__ void __launch_bounds__(384, 1)
           elementwise(std::false_type{});
         else
           elementwise(std::true_type{});
-        uint32_t hp[16], hd[16], ep[16], ed[16];
+        uint32_t hp[8], hd[8], ep[8], ed[8];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
+        for (int x = 0; x < 8; ++x) {
           hp[x] = pack2<kBf16>(pt[2 * x], pt[2 * x + 1]);
           hd[x] = pack2<kBf16>(ds[2 * x], ds[2 * x + 1]);
         }
         // Residuals only where this warp's rows hold a probability above the
         // split threshold; zeros elsewhere keep the residual image well defined.
-        const bool split_c = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
-        lo_any |= split_c;
-        if (split_c) {
+        const bool split_h = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        lo_any |= split_h;
+        if (split_h) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
+          for (int x = 0; x < 8; ++x) {
             ep[x] = pack2_residual<kBf16>(pt[2 * x], pt[2 * x + 1], hp[x]);
             ed[x] = pack2_residual<kBf16>(ds[2 * x], ds[2 * x + 1], hd[x]);
           }
         } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) ep[x] = ed[x] = 0u;
+          for (int x = 0; x < 8; ++x) ep[x] = ed[x] = 0u;
         }
-        // P~T image over the S^T columns just read.
-        uint32_t timg[32];
-        interleave_split(hp, ep, timg);
-        tmem_st32(tSb + 32 * c, timg);
+        // This K step's image: 8 rounded columns, then 8 residual columns, over the
+        // 16 S^T (and dP^T) columns just read.
+        tmem_st8<0>(tSc + 16 * hh, hp);
+        tmem_st8<0>(tSc + 16 * hh + 8, ep);
         if constexpr (!kAtomic) {
-          // dS^T image over the dP^T columns just read.
-          interleave_split(hd, ed, timg);
-          tmem_st32(tdPb + 32 * c, timg);
+          tmem_st8<0>(tdPc + 16 * hh, hd);
+          tmem_st8<0>(tdPc + 16 * hh + 8, ed);
         } else {
-          store_tile_row_chunk(imgRow, jl, c, hd);
-          store_tile_row_chunk(imgRow + C::kPTile, jl, c, ed);
+          // dS^T row jl: 16 queries = two 16-byte slots of the 128-byte swizzled rows.
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t slot = (uint32_t)((4 * c + 2 * hh + t) ^ (jl & 7)) << 4;
+            st_shared_v4(imgRow + slot, hd[4 * t], hd[4 * t + 1], hd[4 * t + 2], hd[4 * t + 3]);
+            st_shared_v4(imgRow + C::kPTile + slot, ed[4 * t], ed[4 * t + 1], ed[4 * t + 2], ed[4 * t + 3]);
+          }
         }
       }
       tmem_st_wait();
-      if (lane == 0) flags[4 * wg + wq] = lo_any ? 1 : 0;
+      if (lane == 0) flags[8 * bb + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
       if constexpr (kAtomic) fence_proxy_async_smem();
-      mbar_arrive(bar(C::bPFull + wg));
+      mbar_arrive(bar(C::bPFull + bb));
       if constexpr (kAtomic) {
-        // dQ^T (d on lanes, 64 queries on columns) -> fp32 accumulator in HBM.
-        if (!mbar_wait(bar(C::bDQFull + wg), (it >> 1) & 1, abort_flag, p.status)) {
+        // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
+        if (!mbar_wait(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tdPb, r0);
-        tmem_ld32(tdPb + 32, r1);
-        tmem_ld_wait2(r0, r1);
+        uint32_t r0[32];
+        tmem_ld32(tdPc, r0);
+        tmem_ld_wait(r0);
         tc_fence_before();
-        mbar_arrive(bar(C::bDPEmpty + wg));
+        mbar_arrive(bar(C::bDPEmpty + bb));
         if (jl < D) {
-          float* dst = p.ws_dq + ((long long)bh * p.n_pad + i0) * D + jl;
+          float* dst = p.ws_dq + ((long long)bh * p.n_pad + base) * D + jl;
 #pragma unroll
           for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
-#pragma unroll
-          for (int x = 0; x < 32; ++x) atomicAdd(dst + (32 + x) * D, __uint_as_float(r1[x]));
         }
       }
     }
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK.
+    // Epilogue: warpgroups 0, 1 write dV and 2, 3 write scale * dK, each half of the columns.
     if (ok && nsteps > 0) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
+      const bool isK = rg >= 2;
       const long long off = (long long)b * p.sb + (long long)j * p.sn + (long long)h * p.sh;
-      uint16_t* dst = static_cast<uint16_t*>(wg ? p.dk : p.dv) + off;
-      const uint32_t col0 = wg ? (tdK + lane_off) : (tdV + lane_off);
-      const float mul = wg ? p.scale : 1.f;
+      uint16_t* dst = static_cast<uint16_t*>(isK ? p.dk : p.dv) + off;
+      const uint32_t col0 = (isK ? tdK : tdV) + lane_off;
+      const float mul = isK ? p.scale : 1.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = c * (D / 2) + 32 * cc;
         uint32_t r[32];
         if (nsteps > 0) {
-          tmem_ld32(col0 + 32 * c, r);
+          tmem_ld32(col0 + col, r);
           tmem_ld_wait(r);
         } else {
 #pragma unroll
@@ -453,7 +467,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int x = 0; x < 16; ++x)
           w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
         if (j < p.N) {
-          uint4* g = reinterpret_cast<uint4*>(dst + 32 * c);
+          uint4* g = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
         }
@@ -479,7 +493,7 @@ static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, c
   if (e != cudaSuccess) return e;
   const int tiles = (p.N + kRowsKV - 1) / kRowsKV;
   const unsigned grid = (unsigned)(tiles * p.B * p.H);
-  kern<<<grid, 384, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, kKVThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }
 
