@@ -89,6 +89,117 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
   }
 }
 
+// 16-bit tensors with d in {64, 128}: a group of d/8 lanes owns one row and
+// each lane reads 16 bytes of O and of dO, so a warp moves whole 128-byte lines.
+// Rows are enumerated in [B*H, n_pad] order (i fastest), which makes the
+// workspace vectors and L contiguous; every thread takes kVecRows rows and
+// issues all of their loads before reducing, to keep enough bytes in flight.
+constexpr int kVecRows = 4;
+
+template <int D>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = D / 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const T* a2 = reinterpret_cast<const T*>(&aw[x]);
+    const T* b2 = reinterpret_cast<const T*>(&bw[x]);
+    acc = fmaf(to_f32(a2[0]), to_f32(b2[0]), acc);
+    acc = fmaf(to_f32(a2[1]), to_f32(b2[1]), acc);
+  }
+  return acc;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int G = D / 8;            // lanes per row
+  constexpr int kRowsPerWarp = 32 / G;
+  const long long rows = (long long)p.B * p.H * p.n_pad;
+  const int lane = threadIdx.x & 31;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long row0 = warp * (kRowsPerWarp * kVecRows) + lane / G;
+  const int e0 = (lane % G) * 8;
+  uint4 ov[kVecRows], gv[kVecRows];
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const long long row = row0 + (long long)r * kRowsPerWarp;
+    ov[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows) {
+      const int i = (int)(row % p.n_pad);
+      const int bh = (int)(row / p.n_pad);
+      if (i < p.N) {
+        const long long off = (long long)(bh / p.H) * p.sb + (long long)i * p.sn + (long long)(bh % p.H) * p.sh + e0;
+        ov[r] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off));
+        gv[r] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off));
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const long long row = row0 + (long long)r * kRowsPerWarp;
+    const float acc = group_sum<D>(dot8<T>(ov[r], gv[r], 0.f));
+    if (row >= rows) continue;
+    if (e0 == 0) {
+      const int i = (int)(row % p.n_pad);
+      const long long bh = row / p.n_pad;
+      p.ws_D[row] = acc;
+      p.ws_L2[row] = (i < p.N) ? p.lse[bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
+    }
+    if (p.ws_dq != nullptr) {
+      float4* dq = reinterpret_cast<float4*>(p.ws_dq + row * D + e0);
+      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// dQ = scale * dQ_accum for 16-bit outputs with d in {64, 128}, eight elements a lane.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) dq_convert_vec_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int G = D / 8;
+  constexpr int kRowsPerWarp = 32 / G;
+  const long long rows = (long long)p.B * p.H * p.n_pad;
+  const int lane = threadIdx.x & 31;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long row0 = warp * (kRowsPerWarp * kVecRows) + lane / G;
+  const int e0 = (lane % G) * 8;
+  float4 a[kVecRows], c[kVecRows];
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const long long row = row0 + (long long)r * kRowsPerWarp;
+    if (row < rows && (int)(row % p.n_pad) < p.N) {
+      const float4* src = reinterpret_cast<const float4*>(p.ws_dq + row * D + e0);
+      a[r] = __ldg(src);
+      c[r] = __ldg(src + 1);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const long long row = row0 + (long long)r * kRowsPerWarp;
+    if (row >= rows) continue;
+    const int i = (int)(row % p.n_pad);
+    const int bh = (int)(row / p.n_pad);
+    if (i >= p.N) continue;
+    const float v[8] = {a[r].x, a[r].y, a[r].z, a[r].w, c[r].x, c[r].y, c[r].z, c[r].w};
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const T lo = from_f32<T>(v[2 * x] * p.scale), hi = from_f32<T>(v[2 * x + 1] * p.scale);
+      w[x] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
+             ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+    }
+    T* dst = static_cast<T*>(p.out) + (long long)(bh / p.H) * p.sb + (long long)i * p.sn +
+             (long long)(bh % p.H) * p.sh + e0;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const __grid_constant__ AttnParams p) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -293,6 +404,17 @@ static inline unsigned grid_for_rows(long long rows, int rows_per_block) {
 
 cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
   const long long rows = (long long)p.B * p.n_pad * p.H;
+  if (dtype != 0 && (p.d == 64 || p.d == 128)) {
+    // 256 threads = 8 warps, each covering (32 / (d/8)) * kVecRows rows
+    const unsigned g = grid_for_rows(rows, 8 * (32 / (p.d / 8)) * kVecRows);
+    if (p.d == 128)
+      dtype == 1 ? preprocess_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
+                 : preprocess_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);
+    else
+      dtype == 1 ? preprocess_vec_kernel<__half, 64><<<g, 256, 0, st>>>(p)
+                 : preprocess_vec_kernel<__nv_bfloat16, 64><<<g, 256, 0, st>>>(p);
+    return cudaGetLastError();
+  }
   const unsigned grid = grid_for_rows(rows, 8);
   if (dtype == 0) preprocess_kernel<float><<<grid, 256, 0, st>>>(p);
   else if (dtype == 1) preprocess_kernel<__half><<<grid, 256, 0, st>>>(p);
@@ -301,6 +423,17 @@ cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
 }
 
 cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st) {
+  if (dtype != 0 && (p.d == 64 || p.d == 128)) {
+    const long long prow = (long long)p.B * p.n_pad * p.H;
+    const unsigned g = grid_for_rows(prow, 8 * (32 / (p.d / 8)) * kVecRows);
+    if (p.d == 128)
+      dtype == 1 ? dq_convert_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
+                 : dq_convert_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);
+    else
+      dtype == 1 ? dq_convert_vec_kernel<__half, 64><<<g, 256, 0, st>>>(p)
+                 : dq_convert_vec_kernel<__nv_bfloat16, 64><<<g, 256, 0, st>>>(p);
+    return cudaGetLastError();
+  }
   const long long rows = (long long)p.B * p.N * p.H;
   const unsigned grid = grid_for_rows(rows, 8);
   if (dtype == 0) dq_convert_kernel<float><<<grid, 256, 0, st>>>(p);

@@ -21,9 +21,12 @@
 // rotates over three TMEM buffers, so the S MMA of step it + 3 waits only for
 // the accumulating MMA of step it; dP rotates over two buffers that the row
 // math releases as soon as it has read them.
-// Warp 0 issues TMA loads, warp 1 owns TMEM and issues the S (and dP) MMAs,
-// warp 2 issues the accumulating MMAs, two row-math warpgroups (warps 4-7,
-// 8-11) take alternate key steps and split the epilogue columns.
+// Warp 0 issues TMA loads, warp 1 owns TMEM and issues the S MMAs, warp 3 the
+// dP MMAs (one thread issues at most about one MMA per 60 cycles, so the two
+// streams go out in parallel) and warp 2 the accumulating MMAs. Four row-math
+// warpgroups (warps 4-19) work in pairs on alternate key steps, each
+// warpgroup of a pair on half of the step's key columns, and split the
+// epilogue columns four ways.
 //
 // TMEM columns: [0,192) three S buffers, [192,320) two dP buffers (dQ mode),
 // [320,320+d) the O or dQ accumulator.
@@ -34,6 +37,8 @@ namespace fa {
 constexpr int kModeFwd = 0;
 constexpr int kModeDq = 1;
 
+constexpr int kQThreads = 640;  // 4 role warps + 4 row-math warpgroups
+
 template <int D, int kMode>
 struct QCfg {
   static constexpr int kPanels = D / 64;
@@ -42,7 +47,7 @@ struct QCfg {
   static constexpr uint32_t kKVPanel = kStepKV * 128;          // 8 KB
   static constexpr uint32_t kKVTile = kPanels * kKVPanel;
   static constexpr uint32_t kResident = (kMode == kModeDq ? 2 : 1) * kRowTile;
-  static constexpr uint32_t kStats = kMode == kModeFwd ? 2 * 2 * kRowsQ * 4 : 0;
+  static constexpr uint32_t kStats = kMode == kModeFwd ? 4 * 2 * kRowsQ * 4 : 0;
   static constexpr uint32_t kBudget = 225u * 1024u;
   static constexpr int kNSraw = (int)((kBudget - kResident - kStats - 2048) / (2 * kKVTile));
   static constexpr int kNS = kNSraw > 6 ? 6 : kNSraw;          // K/V pipeline stages
@@ -50,7 +55,7 @@ struct QCfg {
   static constexpr uint32_t oDO = oQ + kRowTile;
   static constexpr uint32_t oK = kResident;
   static constexpr uint32_t oV = oK + kNS * kKVTile;
-  static constexpr uint32_t oStats = oV + kNS * kKVTile;       // forward: [wg][m | l][row]
+  static constexpr uint32_t oStats = oV + kNS * kKVTile;       // forward: [warpgroup][m | l][row]
   static constexpr uint32_t oBar = oStats + kStats;
   static constexpr int bRes = 0;
   static constexpr int bKVFull = 1;
@@ -59,14 +64,15 @@ struct QCfg {
   static constexpr int bSEmpty = bSFull + 3;
   static constexpr int bDPEmpty = bSEmpty + 3;
   static constexpr int bPFull = bDPEmpty + 2;
-  static constexpr int bAcc = bPFull + 2;
+  static constexpr int bPCons = bPFull + 2;                    // issuer has read step t's split votes
+  static constexpr int bAcc = bPCons + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
-  static constexpr int bStats = bDrain + 2;
+  static constexpr int bStats = bDrain + 3;
   static constexpr int kBars = bStats + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
-  static constexpr uint32_t kSmem = oFlags + 32 + 1024;
+  static constexpr uint32_t kSmem = oFlags + 64 + 1024;
   static_assert(kNS >= 2, "shared memory budget leaves fewer than two K/V stages");
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
@@ -78,7 +84,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
 }
 
 template <int D, bool kBf16, int kMode, bool kDrop>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     qmajor_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmDO) {
@@ -113,17 +119,17 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::bKVEmpty + s), 1);
     }
     for (int x = 0; x < 3; ++x) {
-      mbar_init(bar(C::bSFull + x), 1);
+      mbar_init(bar(C::bSFull + x), kDq ? 2 : 1);              // S (and dP) landed
       mbar_init(bar(C::bSEmpty + x), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::bDPEmpty + x), 128);
-      mbar_init(bar(C::bPFull + x), 128);
+      mbar_init(bar(C::bDPEmpty + x), 256);                   // two warpgroups per step
+      mbar_init(bar(C::bPFull + x), 256);
+      mbar_init(bar(C::bPCons + x), 1);
     }
     mbar_init(bar(C::bAcc), 1);
-    mbar_init(bar(C::bDrain), 1);
-    mbar_init(bar(C::bDrain + 1), 1);
-    mbar_init(bar(C::bStats), 256);
+    for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
+    mbar_init(bar(C::bStats), 512);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -175,41 +181,55 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------------------- S / dP MMA issuer ---------------------------
+    // ------------------------------ S MMA issuer ------------------------------
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
-      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
-      const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
+      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dK0 = make_sdesc(sb + C::oK, 16, 1024);
       bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int s = it % C::kNS, bb = it & 1, bs = it % 3;
+        const int s = it % C::kNS, bs = it % 3;
         if (!mbar_wait(bar(C::bKVFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
             !mbar_wait(bar(C::bSEmpty + bs), ((it / 3) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t kd = desc_add(dK0, s * C::kKVTile), vd = desc_add(dV0, s * C::kKVTile);
+        const uint64_t kd = desc_add(dK0, s * C::kKVTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ss(tS + 64 * bs, desc_add(dQ0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
                     desc_add(kd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        if constexpr (kDq) {
-          if (!mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            tc_mma_ss(tdP + 64 * bb, desc_add(dO0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
-                      desc_add(vd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        }
         tc_commit(bar(C::bSFull + bs));
       }
       if (!ok) {
         tc_commit(bar(C::bDrain));
         mbar_wait_drain(bar(C::bDrain), 0, p.status);
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------- dP MMA issuer (dQ mode only) ----------------------
+    if (kDq && lane == 0) {
+      constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
+      const uint64_t dO0 = make_sdesc(sb + C::oDO, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
+      bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
+      for (int it = 0; ok && it < nsteps; ++it) {
+        const int s = it % C::kNS, bb = it & 1;
+        if (!mbar_wait(bar(C::bKVFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t vd = desc_add(dV0, s * C::kKVTile);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          tc_mma_ss(tdP + 64 * bb, desc_add(dO0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
+                    desc_add(vd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit(bar(C::bSFull + it % 3));
+      }
+      if (!ok) {
+        tc_commit(bar(C::bDrain + 2));
+        mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
       }
     }
   } else if (warp == 2) {
@@ -229,7 +249,10 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         if (t >= first_out) {
           const uint32_t first = t > first_out ? 1u : 0u;
-          const bool split = (flags[4 * bt] | flags[4 * bt + 1] | flags[4 * bt + 2] | flags[4 * bt + 3]) != 0;
+          bool split = false;
+#pragma unroll
+          for (int x = 0; x < 8; ++x) split |= flags[8 * bt + x] != 0;
+          mbar_arrive(bar(C::bPCons + bt));
           const uint64_t bop = desc_add(b0, st * C::kKVTile);
 #pragma unroll
           for (int k = 0; k < kStepKV / 16; ++k)
@@ -239,6 +262,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; k < kStepKV / 16; ++k)
               tc_mma_ts(tAcc, tS + 64 * bs + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
           }
+        } else {
+          mbar_arrive(bar(C::bPCons + bt));
         }
         tc_commit(bar(C::bSEmpty + bs));
         tc_commit(bar(C::bKVEmpty + st));
@@ -250,148 +275,169 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp >= 4) {
-    // ------------- row-math warpgroups (alternate key steps) + epilogue -------
-    const int wg = (warp - 4) >> 2;
+    // ---------------- row-math warpgroups + epilogue ----------------------
+    // rg = 0, 1 take the even key steps and rg = 2, 3 the odd ones; within a
+    // pair, warpgroup rg & 1 takes key columns [32 (rg & 1), 32 (rg & 1) + 32)
+    // of the step, in halves of 16 columns (one MMA K step).
+    const int rg = (warp - 4) >> 2;
     const int wq = warp & 3;
+    const int c = rg & 1;
+    const int pr = rg >> 1;
     const int il = wq * 32 + lane;
     const int i = i0 + il;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tdPb = tdP + lane_off + 64 * wg;
+    const uint32_t tdPc = tdP + lane_off + 64 * pr + 32 * c;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
     float L2 = INFINITY, Dv = 0.f;
     if (kDq) {
       L2 = p.ws_L2[ws];
       Dv = p.ws_D[ws];
     }
-    float m = -INFINITY, l = 0.f;  // forward statistics of this warpgroup's steps, log2 domain
+    float m = -INFINITY, l = 0.f;  // forward statistics of this warpgroup's columns, log2 domain
     bool merged = kDq;
     bool ok = true;
-    for (int it = wg; it < nsteps; it += 2) {
+    // Forward: merge the four warpgroups' partial row statistics into L (log2 domain).
+    auto merge_stats = [&]() -> bool {
+      float* st = reinterpret_cast<float*>(smem + C::oStats);
+      st[(2 * rg) * kRowsQ + il] = m;
+      st[(2 * rg + 1) * kRowsQ + il] = l;
+      mbar_arrive(bar(C::bStats));
+      if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) return false;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) mm = fmaxf(mm, st[(2 * g) * kRowsQ + il]);
+      float ll = 0.f;
+      if (mm != -INFINITY) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) ll += st[(2 * g + 1) * kRowsQ + il] * ex2_approx(st[(2 * g) * kRowsQ + il] - mm);
+      }
+      L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
+      return true;
+    };
+    for (int it = pr; it < nsteps; it += 2) {
       const int jt = it >= nkv ? it - nkv : it;
-      const int jj0 = j_first + jt * kStepKV;
+      const int base = j_first + jt * kStepKV + 32 * c;
       if (!kDq && it >= first_out && !merged) {
-        // Combine the two warpgroups' partial row statistics into L.
-        float* st = reinterpret_cast<float*>(smem + C::oStats);
-        st[(2 * wg) * kRowsQ + il] = m;
-        st[(2 * wg + 1) * kRowsQ + il] = l;
-        mbar_arrive(bar(C::bStats));
-        if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) {
+        if (!merge_stats()) {
           ok = false;
           break;
         }
-        const float mo = st[(2 * (1 - wg)) * kRowsQ + il], lo = st[(2 * (1 - wg) + 1) * kRowsQ + il];
-        const float mm = fmaxf(m, mo);
-        const float ll = (mm == -INFINITY) ? 0.f
-                                           : l * ex2_approx(m - mm) + lo * ex2_approx(mo - mm);
-        L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
         merged = true;
       }
-      const uint32_t tSb = tS + lane_off + 64 * (it % 3);
+      const uint32_t tSc = tS + lane_off + 64 * (it % 3) + 32 * c;
       if (!mbar_wait(bar(C::bSFull + it % 3), (it / 3) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // allowed keys of this warpgroup's 32 columns (bit x <-> key base + x)
+      const uint32_t allow =
+          bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
       if (!kDq && it < first_out) {
         // statistics step
 #pragma unroll
-        for (int c = 0; c < kStepKV / 32; ++c) {
-          const int base = jj0 + 32 * c;
-          const uint32_t allow =
-              bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
-          uint32_t sr[32];
-          tmem_ld32(tSb + 32 * c, sr);
-          tmem_ld_wait(sr);
-          float x[32];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[16];
+          tmem_ld16(tSc + 16 * hh, sr);
+          tmem_ld_wait16(sr);
+          float x[16];
           float mx = m;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            x[e] = ((allow >> e) & 1u) ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
+          for (int e = 0; e < 16; ++e) {
+            x[e] = ((allow >> (16 * hh + e)) & 1u) ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
             mx = fmaxf(mx, x[e]);
           }
           if (mx != -INFINITY) {
             float acc = l * ex2_approx(m - mx);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc += ex2_approx(x[e] - mx);
+            for (int e = 0; e < 16; ++e) acc += ex2_approx(x[e] - mx);
             l = acc;
             m = mx;
           }
         }
+        // the issuer must have taken step it - 2 before this buffer's barrier moves on
+        if (it >= 2 && !mbar_wait(bar(C::bPCons + pr), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_before();
-        mbar_arrive(bar(C::bPFull + wg));
+        mbar_arrive(bar(C::bPFull + pr));
         continue;
       }
+      uint32_t keep = 0xFFFFFFFFu;
+      if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
       bool lo_any = false;
 #pragma unroll
-      for (int c = 0; c < kStepKV / 32; ++c) {
-        const int base = jj0 + 32 * c;
-        const uint32_t allow =
-            bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
-        uint32_t keep = 0xFFFFFFFFu;
-        if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tSb + 32 * c, sr);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[16], dr[16];
+        tmem_ld16(tSc + 16 * hh, sr);
         if constexpr (kDq) {
-          tmem_ld32(tdPb + 32 * c, dr);
-          tmem_ld_wait2(sr, dr);
-          if (c == kStepKV / 32 - 1) {
-            // every dP column of this buffer is in registers: the next dP may land
+          tmem_ld16(tdPc + 16 * hh, dr);
+          tmem_ld_wait16x2(sr, dr);
+          if (hh == 1) {
+            // this warpgroup's dP columns are in registers: the next dP may land
             tc_fence_before();
-            mbar_arrive(bar(C::bDPEmpty + wg));
+            mbar_arrive(bar(C::bDPEmpty + pr));
           }
         } else {
-          tmem_ld_wait(sr);
+          tmem_ld_wait16(sr);
         }
-        float outv[32];
+        float outv[16];
         float cmax = 0.f;
+        auto elementwise = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool on = (allow >> e) & 1u;
-          const float pv = on ? ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, -L2)) : 0.f;
-          cmax = fmaxf(cmax, pv);
-          const bool kept = !kDrop || ((keep >> e) & 1u);
-          const float rp = kDrop ? p.drop.rp : 1.f;
-          if constexpr (kDq) {
-            const float dpv = kept ? __uint_as_float(dr[e]) * rp : 0.f;
-            outv[e] = pv * (dpv - Dv);
-          } else {
-            outv[e] = kept ? pv * rp : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            const int bit = 16 * hh + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, -L2));
+            if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
+            cmax = fmaxf(cmax, pv);
+            const bool kept = !kDrop || ((keep >> bit) & 1u);
+            const float rp = kDrop ? p.drop.rp : 1.f;
+            if constexpr (kDq) {
+              const float dpv = kept ? __uint_as_float(dr[e]) * rp : 0.f;
+              outv[e] = pv * (dpv - Dv);
+            } else {
+              outv[e] = kept ? pv * rp : 0.f;
+            }
           }
-        }
-        uint32_t hv[16], ev[16];
+        };
+        // L2 = +inf (a row with no allowed key) gives exp2(-inf) = 0 on the fast path too.
+        if (allow == 0xFFFFFFFFu)
+          elementwise(std::false_type{});
+        else
+          elementwise(std::true_type{});
+        uint32_t hv[8], ev[8];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
-        const bool split_c = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
-        lo_any |= split_c;
-        if (split_c) {
+        for (int x = 0; x < 8; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
+        const bool split_h = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        lo_any |= split_h;
+        if (split_h) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) ev[x] = pack2_residual<kBf16>(outv[2 * x], outv[2 * x + 1], hv[x]);
+          for (int x = 0; x < 8; ++x) ev[x] = pack2_residual<kBf16>(outv[2 * x], outv[2 * x + 1], hv[x]);
         } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) ev[x] = 0u;
+          for (int x = 0; x < 8; ++x) ev[x] = 0u;
         }
-        uint32_t img[32];
-        interleave_split(hv, ev, img);
-        tmem_st32(tSb + 32 * c, img);
+        // this K step's image: 8 rounded columns, then 8 residual columns
+        tmem_st8<0>(tSc + 16 * hh, hv);
+        tmem_st8<0>(tSc + 16 * hh + 8, ev);
       }
       tmem_st_wait();
-      if (lane == 0) flags[4 * wg + wq] = lo_any ? 1 : 0;
+      // The issuer must have read step it - 2's votes (and taken that phase of
+      // bPFull) before this step's votes overwrite them.
+      if (it >= 2 && !mbar_wait(bar(C::bPCons + pr), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) flags[8 * pr + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
-      mbar_arrive(bar(C::bPFull + wg));
+      mbar_arrive(bar(C::bPFull + pr));
     }
     if (!kDq && ok && !merged) {
       // This warpgroup saw no output step (tiny key ranges): still publish its statistics.
-      float* st = reinterpret_cast<float*>(smem + C::oStats);
-      st[(2 * wg) * kRowsQ + il] = m;
-      st[(2 * wg + 1) * kRowsQ + il] = l;
-      mbar_arrive(bar(C::bStats));
-      if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) ok = false;
-      const float mo = st[(2 * (1 - wg)) * kRowsQ + il], lo = st[(2 * (1 - wg) + 1) * kRowsQ + il];
-      const float mm = fmaxf(m, mo);
-      const float ll = (mm == -INFINITY) ? 0.f : l * ex2_approx(m - mm) + lo * ex2_approx(mo - mm);
-      L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
+      ok = merge_stats();
     }
-    // Epilogue: O (forward) or scale * dQ; warpgroup w writes columns [w*d/2, (w+1)*d/2).
+    // Epilogue: O (forward) or scale * dQ; warpgroup rg writes columns [rg*d/4, (rg+1)*d/4).
     const bool have_acc = nsteps > first_out;
     if (ok && have_acc) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
@@ -400,27 +446,27 @@ __global__ void __launch_bounds__(384, 1)
       uint16_t* dst = static_cast<uint16_t*>(p.out) + off;
       const float mul = kDq ? p.scale : 1.f;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const int col = wg * (D / 2) + 32 * c;
-        uint32_t r[32];
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = rg * (D / 4) + 16 * cc;
+        uint32_t r[16];
         if (have_acc) {
-          tmem_ld32(tAcc + lane_off + col, r);
-          tmem_ld_wait(r);
+          tmem_ld16(tAcc + lane_off + col, r);
+          tmem_ld_wait16(r);
         } else {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = 0u;
+          for (int x = 0; x < 16; ++x) r[x] = 0u;
         }
-        uint32_t w[16];
+        uint32_t w[8];
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
+        for (int x = 0; x < 8; ++x)
           w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
         if (i < p.N) {
           uint4* g = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+          g[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          g[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      if (!kDq && wg == 0 && i < p.N)
+      if (!kDq && rg == 0 && i < p.N)
         p.lse_out[(long long)bh * p.N + i] = (L2 == INFINITY) ? -INFINITY : L2 * 0.6931471805599453f;
     }
   }
@@ -443,7 +489,7 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
   if (e != cudaSuccess) return e;
   const int tiles = (p.N + kRowsQ - 1) / kRowsQ;
   const unsigned grid = (unsigned)(tiles * p.B * p.H);
-  kern<<<grid, 384, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, kQThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }
 
