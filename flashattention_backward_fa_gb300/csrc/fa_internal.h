@@ -13,7 +13,7 @@ namespace fa {
 constexpr int kRowsKV = 128;    // keys per CTA in the key/value-major kernel (TMEM lanes)
 constexpr int kStepQ = 64;      // queries per inner step of that kernel
 constexpr int kRowsQ = 128;     // queries per CTA in the query-major kernels (TMEM lanes)
-constexpr int kStepKV = 64;     // keys per inner step of those kernels
+constexpr int kStepKV = 128;    // keys per inner step of those kernels
 constexpr int kPadRows = 128;   // per-head row padding of the L / D workspace vectors
 // Every tensor-core CTA allocates all 512 TMEM columns; requesting more than half
 // of the SM's shared memory keeps it alone on its SM.

@@ -183,14 +183,14 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------ S^T MMA issuer -----------------------------
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
       const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
-      bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait(bar(C::bKV), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !warp_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -198,25 +198,26 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const uint64_t q = desc_add(dQ0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
-                    desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit(bar(C::bSFull + bb));
+          tc_mma_ss_w(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                      desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit_w(bar(C::bSFull + bb));
       }
       if (!ok) {
-        tc_commit(bar(C::bDrain));
-        mbar_wait_drain(bar(C::bDrain), 0, p.status);
+        tc_commit_w(bar(C::bDrain));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp == 3) {
     // ----------------------------- dP^T MMA issuer -----------------------------
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
       const uint64_t dV0 = make_sdesc(sb + C::oV, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
-      bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait(bar(C::bKV), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !warp_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -224,18 +225,19 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const uint64_t g = desc_add(dO0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
-                    desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit(bar(C::bSFull + bb));
+          tc_mma_ss_w(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                      desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit_w(bar(C::bSFull + bb));
       }
       if (!ok) {
-        tc_commit(bar(C::bDrain + 2));
-        mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+        tc_commit_w(bar(C::bDrain + 2));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp == 2) {
     // ----------------------- dV / dK (/ dQ^T) MMA issuer ----------------------
-    if (lane == 0) {
+    {
       constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);         // dV, dK
       constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);     // dQ^T
       const uint64_t mQ0 = make_sdesc(sb + C::oQ, C::kQPanel, 1024), mO0 = make_sdesc(sb + C::oDO, C::kQPanel, 1024);
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1, st = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -257,24 +259,24 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         // and, on split tiles, the 8 residual columns at 16k + 8.
 #pragma unroll
         for (int k = 0; k < kStepQ / 16; ++k)
-          tc_mma_ts(tdV, tS + 64 * bt + 16 * k, desc_add(g, 2048 * k), idG, k > 0 ? 1u : first);
+          tc_mma_ts_w(tdV, tS + 64 * bt + 16 * k, desc_add(g, 2048 * k), idG, k > 0 ? 1u : first);
         if (split) {
 #pragma unroll
           for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ts(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
+            tc_mma_ts_w(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
         }
-        tc_commit(bar(C::bSEmpty + bt));
+        tc_commit_w(bar(C::bSEmpty + bt));
         if constexpr (!kAtomic) {
           // dK += dS^T Q from the dS^T image over the dP^T columns.
 #pragma unroll
           for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ts(tdK, tdP + 64 * bt + 16 * k, desc_add(q, 2048 * k), idG, k > 0 ? 1u : first);
+            tc_mma_ts_w(tdK, tdP + 64 * bt + 16 * k, desc_add(q, 2048 * k), idG, k > 0 ? 1u : first);
           if (split) {
 #pragma unroll
             for (int k = 0; k < kStepQ / 16; ++k)
-              tc_mma_ts(tdK, tdP + 64 * bt + 16 * k + 8, desc_add(q, 2048 * k), idG, 1u);
+              tc_mma_ts_w(tdK, tdP + 64 * bt + 16 * k + 8, desc_add(q, 2048 * k), idG, 1u);
           }
-          tc_commit(bar(C::bDPEmpty + bt));
+          tc_commit_w(bar(C::bDPEmpty + bt));
         } else {
           // dK += dS^T Q and dQ^T = K^T dS^T from the shared dS^T tiles; dQ^T lands in
           // this buffer's dP^T columns, which the row math has consumed. For d = 64
@@ -284,24 +286,25 @@ __global__ void __launch_bounds__(kKVThreads, 1)
           for (int part = 0; part < (split ? 2 : 1); ++part) {
 #pragma unroll
             for (int k = 0; k < kStepQ / 16; ++k)
-              tc_mma_ss(tdK, desc_add(aK, part * C::kPTile + 32 * k), desc_add(q, 2048 * k), idG,
-                        (k > 0 || part > 0) ? 1u : first);
+              tc_mma_ss_w(tdK, desc_add(aK, part * C::kPTile + 32 * k), desc_add(q, 2048 * k), idG,
+                          (k > 0 || part > 0) ? 1u : first);
           }
           for (int part = 0; part < (split ? 2 : 1); ++part) {
 #pragma unroll
             for (int k = 0; k < kRowsKV / 16; ++k)
-              tc_mma_ss(tdP + 64 * bt, desc_add(mK0, 2048 * k), desc_add(bQT, part * C::kPTile + 2048 * k), idQ,
-                        (k > 0 || part > 0) ? 1u : 0u);
+              tc_mma_ss_w(tdP + 64 * bt, desc_add(mK0, 2048 * k), desc_add(bQT, part * C::kPTile + 2048 * k), idQ,
+                          (k > 0 || part > 0) ? 1u : 0u);
           }
-          tc_commit(bar(C::bDQFull + bt));
-          tc_commit(bar(C::bPEmpty + bt));
+          tc_commit_w(bar(C::bDQFull + bt));
+          tc_commit_w(bar(C::bPEmpty + bt));
         }
-        tc_commit(bar(C::bQEmpty + st));
+        tc_commit_w(bar(C::bQEmpty + st));
       }
-      tc_commit(bar(C::bAcc));
+      tc_commit_w(bar(C::bAcc));
       if (!ok) {
-        tc_commit(bar(C::bDrain + 1));
-        mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+        tc_commit_w(bar(C::bDrain + 1));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp >= 4) {

@@ -15,65 +15,67 @@
 // so O never needs rescaling — and accumulates O += (P o Z/(1-p)) V.
 //
 // Queries sit on the 128 TMEM lanes: one thread owns one query row, so L_i and
-// D_i are per-thread scalars. The row math writes dS (or P~) back over the S
-// columns it has read, rounded to 16 bits with the rounding residual beside
-// it (see interleave_split), and the accumulating MMA reads it from TMEM. S
-// rotates over three TMEM buffers, so the S MMA of step it + 3 waits only for
-// the accumulating MMA of step it; dP rotates over two buffers that the row
-// math releases as soon as it has read them.
-// Warp 0 issues TMA loads, warp 1 owns TMEM and issues the S MMAs, warp 3 the
-// dP MMAs (one thread issues at most about one MMA per 60 cycles, so the two
-// streams go out in parallel) and warp 2 the accumulating MMAs. Four row-math
-// warpgroups (warps 4-19) work in pairs on alternate key steps, each
-// warpgroup of a pair on half of the step's key columns, and split the
-// epilogue columns four ways.
+// D_i are per-thread scalars. A step covers 128 keys, so every S, dP and
+// accumulating MMA has N = 128 (N = 64 MMAs are limited by shared-memory
+// operand reads to about two thirds of the tensor rate). The row math writes
+// dS (or P~) back over the S columns it has read, rounded to 16 bits with the
+// rounding residual beside it (see interleave_split), and the accumulating MMA
+// reads it from TMEM. S alternates between two TMEM buffers; dP has one, which
+// the row math releases as soon as it has read it.
 //
-// TMEM columns: [0,192) three S buffers, [192,320) two dP buffers (dQ mode),
-// [320,320+d) the O or dQ accumulator.
+// Shared memory holds Q (and dO) for the whole kernel and two rings of key
+// tiles: ring E for the tile only the first MMAs read (V for dP; K in the
+// forward) and ring L for the tile the accumulating MMA reads (K, which S
+// also reads; V in the forward), so that E tiles are recycled early.
+//
+// Warp 0 issues TMA loads, warp 1 owns TMEM and issues the S MMAs, warp 3 the
+// dP MMAs and warp 2 the accumulating MMAs, so the three streams go out in
+// parallel. Four row-math warpgroups (warps 4-19) each take 32 of the step's
+// 128 key columns and a quarter of the epilogue columns.
+//
+// TMEM columns: [0,256) two S buffers, [256,384) the dP buffer (dQ mode),
+// [384,384+d) the O or dQ accumulator.
 #include "fa_internal.h"
 
 namespace fa {
 
 constexpr int kModeFwd = 0;
 constexpr int kModeDq = 1;
-
 constexpr int kQThreads = 640;  // 4 role warps + 4 row-math warpgroups
 
 template <int D, int kMode>
 struct QCfg {
+  static constexpr bool kDq = kMode == kModeDq;
   static constexpr int kPanels = D / 64;
-  static constexpr uint32_t kRowPanel = kRowsQ * 128;          // 16 KB
-  static constexpr uint32_t kRowTile = kPanels * kRowPanel;
-  static constexpr uint32_t kKVPanel = kStepKV * 128;          // 8 KB
-  static constexpr uint32_t kKVTile = kPanels * kKVPanel;
-  static constexpr uint32_t kResident = (kMode == kModeDq ? 2 : 1) * kRowTile;
-  static constexpr uint32_t kStats = kMode == kModeFwd ? 4 * 2 * kRowsQ * 4 : 0;
-  static constexpr uint32_t kBudget = 225u * 1024u;
-  static constexpr int kNSraw = (int)((kBudget - kResident - kStats - 2048) / (2 * kKVTile));
-  static constexpr int kNS = kNSraw > 6 ? 6 : kNSraw;          // K/V pipeline stages
+  static constexpr uint32_t kPanel = 128 * 128;                // 16 KB: 128 rows x 64 elements
+  static constexpr uint32_t kTile = kPanels * kPanel;          // one 128-row tile of Q, dO, K or V
+  static constexpr uint32_t kResident = (kDq ? 2 : 1) * kTile;
+  static constexpr uint32_t kStats = kDq ? 0 : 4 * 2 * kRowsQ * 4;
+  static constexpr int kNE = kDq ? 2 : (D == 64 ? 4 : 3);      // ring E stages
+  static constexpr int kNL = kDq ? (D == 64 ? 4 : 3) : 2;      // ring L stages
   static constexpr uint32_t oQ = 0;
-  static constexpr uint32_t oDO = oQ + kRowTile;
-  static constexpr uint32_t oK = kResident;
-  static constexpr uint32_t oV = oK + kNS * kKVTile;
-  static constexpr uint32_t oStats = oV + kNS * kKVTile;       // forward: [warpgroup][m | l][row]
+  static constexpr uint32_t oDO = oQ + kTile;
+  static constexpr uint32_t oE = kResident;
+  static constexpr uint32_t oL = oE + kNE * kTile;
+  static constexpr uint32_t oStats = oL + kNL * kTile;         // forward: [warpgroup][m | l][row]
   static constexpr uint32_t oBar = oStats + kStats;
   static constexpr int bRes = 0;
-  static constexpr int bKVFull = 1;
-  static constexpr int bKVEmpty = bKVFull + kNS;
-  static constexpr int bSFull = bKVEmpty + kNS;
-  static constexpr int bSEmpty = bSFull + 3;
-  static constexpr int bDPEmpty = bSEmpty + 3;
-  static constexpr int bPFull = bDPEmpty + 2;
-  static constexpr int bPCons = bPFull + 2;                    // issuer has read step t's split votes
-  static constexpr int bAcc = bPCons + 2;
+  static constexpr int bEFull = 1;
+  static constexpr int bEEmpty = bEFull + kNE;
+  static constexpr int bLFull = bEEmpty + kNE;
+  static constexpr int bLEmpty = bLFull + kNL;
+  static constexpr int bSFull = bLEmpty + kNL;                 // [2]: S (and dP) landed
+  static constexpr int bSEmpty = bSFull + 2;                   // [2]: accumulating MMA done with the image
+  static constexpr int bDPEmpty = bSEmpty + 2;                 // row math has read dP
+  static constexpr int bPFull = bDPEmpty + 1;                  // [2]: image written
+  static constexpr int bAcc = bPFull + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
   static constexpr int bStats = bDrain + 3;
   static constexpr int kBars = bStats + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
-  static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
-  static constexpr uint32_t kSmem = oFlags + 64 + 1024;
-  static_assert(kNS >= 2, "shared memory budget leaves fewer than two K/V stages");
+  static constexpr uint32_t oFlags = (oAbort + 8 + 15) & ~15u;  // [buffer][16 warps] split votes
+  static constexpr uint32_t kSmem = oFlags + 2 * 16 * 4 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
 
@@ -114,19 +116,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bRes), 1);
-    for (int s = 0; s < C::kNS; ++s) {
-      mbar_init(bar(C::bKVFull + s), 1);
-      mbar_init(bar(C::bKVEmpty + s), 1);
+    for (int s = 0; s < C::kNE; ++s) {
+      mbar_init(bar(C::bEFull + s), 1);
+      mbar_init(bar(C::bEEmpty + s), 1);
     }
-    for (int x = 0; x < 3; ++x) {
-      mbar_init(bar(C::bSFull + x), kDq ? 2 : 1);              // S (and dP) landed
-      mbar_init(bar(C::bSEmpty + x), 1);
+    for (int s = 0; s < C::kNL; ++s) {
+      mbar_init(bar(C::bLFull + s), 1);
+      mbar_init(bar(C::bLEmpty + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::bDPEmpty + x), 256);                   // two warpgroups per step
-      mbar_init(bar(C::bPFull + x), 256);
-      mbar_init(bar(C::bPCons + x), 1);
+      mbar_init(bar(C::bSFull + x), kDq ? 2 : 1);
+      mbar_init(bar(C::bSEmpty + x), 1);
+      mbar_init(bar(C::bPFull + x), 512);
     }
+    mbar_init(bar(C::bDPEmpty), 512);
     mbar_init(bar(C::bAcc), 1);
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bStats), 512);
@@ -147,146 +150,169 @@ __global__ void __launch_bounds__(kQThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::oTmemSlot);
-  const uint32_t tS = tmem, tdP = tmem + 192, tAcc = tmem + 320;
+  const uint32_t tS = tmem, tdP = tmem + 256, tAcc = tmem + 384;
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
+    // Step it: ring E gets V (dQ) or K (forward); ring L gets K (dQ) or, on
+    // forward output steps, V. L tiles are counted from the first output step.
     if (lane == 0) {
+      const CUtensorMap* mE = kDq ? &tmV : &tmK;
+      const CUtensorMap* mL = kDq ? &tmK : &tmV;
       mbar_arrive_expect_tx(bar(C::bRes), C::kResident);
       for (int pn = 0; pn < C::kPanels; ++pn) {
-        tma_load_4d(sb + C::oQ + pn * C::kRowPanel, &tmQ, bar(C::bRes), 64 * pn, i0, h, b);
-        if (kDq) tma_load_4d(sb + C::oDO + pn * C::kRowPanel, &tmDO, bar(C::bRes), 64 * pn, i0, h, b);
+        tma_load_4d(sb + C::oQ + pn * C::kPanel, &tmQ, bar(C::bRes), 64 * pn, i0, h, b);
+        if (kDq) tma_load_4d(sb + C::oDO + pn * C::kPanel, &tmDO, bar(C::bRes), 64 * pn, i0, h, b);
       }
-      int issued = 0;
-      for (int it = 0; it < nsteps; ++it) {
-        const int s = it % C::kNS;
-        if (!mbar_wait(bar(C::bKVEmpty + s), ((it / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
+      int issuedE = 0, issuedL = 0;
+      bool ok = true;
+      for (int it = 0; ok && it < nsteps; ++it) {
         const int jt = it >= nkv ? it - nkv : it;
         const int jj = j_first + jt * kStepKV;
-        const bool need_v = kDq || it >= first_out;
-        mbar_arrive_expect_tx(bar(C::bKVFull + s), (need_v ? 2 : 1) * C::kKVTile);
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_load_4d(sb + C::oK + s * C::kKVTile + pn * C::kKVPanel, &tmK, bar(C::bKVFull + s), 64 * pn, jj,
-                      h, b);
-          if (need_v)
-            tma_load_4d(sb + C::oV + s * C::kKVTile + pn * C::kKVPanel, &tmV, bar(C::bKVFull + s), 64 * pn,
-                        jj, h, b);
+        const int se = it % C::kNE;
+        if (!mbar_wait(bar(C::bEEmpty + se), ((it / C::kNE) & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(bar(C::bEFull + se), C::kTile);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_4d(sb + C::oE + se * C::kTile + pn * C::kPanel, mE, bar(C::bEFull + se), 64 * pn, jj, h, b);
+        issuedE = it + 1;
+        if (it >= first_out) {
+          const int li = it - first_out, sl = li % C::kNL;
+          if (!mbar_wait(bar(C::bLEmpty + sl), ((li / C::kNL) & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::bLFull + sl), C::kTile);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn, jj, h, b);
+          issuedL = li + 1;
         }
-        issued = it + 1;
       }
       if (*abort_flag) {
+        // Let every copy this thread started land before the CTA exits.
         mbar_wait_drain(bar(C::bRes), 0, p.status);
-        for (int it = max(0, issued - C::kNS); it < issued; ++it)
-          mbar_wait_drain(bar(C::bKVFull + it % C::kNS), (it / C::kNS) & 1, p.status);
+        for (int it = max(0, issuedE - C::kNE); it < issuedE; ++it)
+          mbar_wait_drain(bar(C::bEFull + it % C::kNE), (it / C::kNE) & 1, p.status);
+        for (int li = max(0, issuedL - C::kNL); li < issuedL; ++li)
+          mbar_wait_drain(bar(C::bLFull + li % C::kNL), (li / C::kNL) & 1, p.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------ S MMA issuer ------------------------------
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
-      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024), dK0 = make_sdesc(sb + C::oK, 16, 1024);
-      bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
+      const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
+      const uint64_t dK0 = make_sdesc(sb + (kDq ? C::oL : C::oE), 16, 1024);
+      bool ok = warp_wait(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int s = it % C::kNS, bs = it % 3;
-        if (!mbar_wait(bar(C::bKVFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bSEmpty + bs), ((it / 3) & 1) ^ 1, abort_flag, p.status)) {
+        const int bb = it & 1;
+        // K lives in ring L (dQ; one tile per step) or ring E (forward)
+        const int ks = kDq ? it % C::kNL : it % C::kNE;
+        const uint32_t kpar = kDq ? (it / C::kNL) & 1 : (it / C::kNE) & 1;
+        if (!warp_wait(bar((kDq ? C::bLFull : C::bEFull) + ks), kpar, abort_flag, p.status) ||
+            !warp_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t kd = desc_add(dK0, s * C::kKVTile);
+        const uint64_t kd = desc_add(dK0, ks * C::kTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss(tS + 64 * bs, desc_add(dQ0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
-                    desc_add(kd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit(bar(C::bSFull + bs));
+          tc_mma_ss_w(tS + 128 * bb, desc_add(dQ0, (k >> 2) * C::kPanel + (k & 3) * 32),
+                      desc_add(kd, (k >> 2) * C::kPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit_w(bar(C::bSFull + bb));
+        if (!kDq) tc_commit_w(bar(C::bEEmpty + ks));   // forward: K is done once S is
       }
       if (!ok) {
-        tc_commit(bar(C::bDrain));
-        mbar_wait_drain(bar(C::bDrain), 0, p.status);
+        tc_commit_w(bar(C::bDrain));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp == 3) {
     // ---------------------- dP MMA issuer (dQ mode only) ----------------------
-    if (kDq && lane == 0) {
+    if (kDq) {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
-      const uint64_t dO0 = make_sdesc(sb + C::oDO, 16, 1024), dV0 = make_sdesc(sb + C::oV, 16, 1024);
-      bool ok = mbar_wait(bar(C::bRes), 0, abort_flag, p.status);
+      const uint64_t dO0 = make_sdesc(sb + C::oDO, 16, 1024), dV0 = make_sdesc(sb + C::oE, 16, 1024);
+      bool ok = warp_wait(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int s = it % C::kNS, bb = it & 1;
-        if (!mbar_wait(bar(C::bKVFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !mbar_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        const int se = it % C::kNE;
+        if (!warp_wait(bar(C::bEFull + se), (it / C::kNE) & 1, abort_flag, p.status) ||
+            (it > 0 && !warp_wait(bar(C::bDPEmpty), (it - 1) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t vd = desc_add(dV0, s * C::kKVTile);
+        const uint64_t vd = desc_add(dV0, se * C::kTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss(tdP + 64 * bb, desc_add(dO0, (k >> 2) * C::kRowPanel + (k & 3) * 32),
-                    desc_add(vd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit(bar(C::bSFull + it % 3));
+          tc_mma_ss_w(tdP, desc_add(dO0, (k >> 2) * C::kPanel + (k & 3) * 32),
+                      desc_add(vd, (k >> 2) * C::kPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        tc_commit_w(bar(C::bSFull + (it & 1)));
+        tc_commit_w(bar(C::bEEmpty + se));
       }
       if (!ok) {
-        tc_commit(bar(C::bDrain + 2));
-        mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+        tc_commit_w(bar(C::bDrain + 2));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp == 2) {
     // ------------------ accumulating MMA issuer (O or dQ) ---------------------
     // After the row math of step t: acc += (P~ or dS) . (V_j or K_j) on output
-    // steps, then release the S buffer and the K/V stage.
-    if (lane == 0) {
+    // steps, then release the S buffer and the ring-L tile.
+    {
       constexpr uint32_t idO = make_idesc(128, D, kBf16, false, true);
-      const uint64_t b0 = make_sdesc(sb + (kDq ? C::oK : C::oV), C::kKVPanel, 1024);
+      const uint64_t b0 = make_sdesc(sb + C::oL, C::kPanel, 1024);
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
-        const int bt = t & 1, bs = t % 3, st = t % C::kNS;
-        if (!mbar_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        const int bt = t & 1;
+        if (!warp_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (t >= first_out) {
+          const int li = t - first_out, sl = li % C::kNL;
           const uint32_t first = t > first_out ? 1u : 0u;
-          bool split = false;
+          const int4* f4 = reinterpret_cast<const int4*>(const_cast<const int*>(flags) + 16 * bt);
+          int any = 0;
 #pragma unroll
-          for (int x = 0; x < 8; ++x) split |= flags[8 * bt + x] != 0;
-          mbar_arrive(bar(C::bPCons + bt));
-          const uint64_t bop = desc_add(b0, st * C::kKVTile);
+          for (int x = 0; x < 4; ++x) {
+            const int4 v = f4[x];
+            any |= v.x | v.y | v.z | v.w;
+          }
+          const uint64_t bop = desc_add(b0, sl * C::kTile);
 #pragma unroll
           for (int k = 0; k < kStepKV / 16; ++k)
-            tc_mma_ts(tAcc, tS + 64 * bs + 16 * k, desc_add(bop, 2048 * k), idO, k > 0 ? 1u : first);
-          if (split) {
+            tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k, desc_add(bop, 2048 * k), idO, k > 0 ? 1u : first);
+          if (any) {
 #pragma unroll
             for (int k = 0; k < kStepKV / 16; ++k)
-              tc_mma_ts(tAcc, tS + 64 * bs + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
+              tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
           }
+          tc_commit_w(bar(C::bSEmpty + bt));
+          tc_commit_w(bar(C::bLEmpty + sl));
         } else {
-          mbar_arrive(bar(C::bPCons + bt));
+          tc_commit_w(bar(C::bSEmpty + bt));
         }
-        tc_commit(bar(C::bSEmpty + bs));
-        tc_commit(bar(C::bKVEmpty + st));
       }
-      tc_commit(bar(C::bAcc));
+      tc_commit_w(bar(C::bAcc));
       if (!ok) {
-        tc_commit(bar(C::bDrain + 1));
-        mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+        tc_commit_w(bar(C::bDrain + 1));
+        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+        __syncwarp();
       }
     }
   } else if (warp >= 4) {
     // ---------------- row-math warpgroups + epilogue ----------------------
-    // rg = 0, 1 take the even key steps and rg = 2, 3 the odd ones; within a
-    // pair, warpgroup rg & 1 takes key columns [32 (rg & 1), 32 (rg & 1) + 32)
-    // of the step, in halves of 16 columns (one MMA K step).
-    const int rg = (warp - 4) >> 2;
+    // Warpgroup c takes key columns [32c, 32c + 32) of every step, in halves of
+    // 16 columns (one MMA K step).
+    const int c = (warp - 4) >> 2;
     const int wq = warp & 3;
-    const int c = rg & 1;
-    const int pr = rg >> 1;
     const int il = wq * 32 + lane;
     const int i = i0 + il;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tdPc = tdP + lane_off + 64 * pr + 32 * c;
+    const uint32_t tdPc = tdP + lane_off + 32 * c;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
     float L2 = INFINITY, Dv = 0.f;
     if (kDq) {
@@ -299,8 +325,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // Forward: merge the four warpgroups' partial row statistics into L (log2 domain).
     auto merge_stats = [&]() -> bool {
       float* st = reinterpret_cast<float*>(smem + C::oStats);
-      st[(2 * rg) * kRowsQ + il] = m;
-      st[(2 * rg + 1) * kRowsQ + il] = l;
+      st[(2 * c) * kRowsQ + il] = m;
+      st[(2 * c + 1) * kRowsQ + il] = l;
       mbar_arrive(bar(C::bStats));
       if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) return false;
       float mm = -INFINITY;
@@ -314,7 +340,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
       return true;
     };
-    for (int it = pr; it < nsteps; it += 2) {
+    for (int it = 0; it < nsteps; ++it) {
+      const int bb = it & 1;
       const int jt = it >= nkv ? it - nkv : it;
       const int base = j_first + jt * kStepKV + 32 * c;
       if (!kDq && it >= first_out && !merged) {
@@ -324,8 +351,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         merged = true;
       }
-      const uint32_t tSc = tS + lane_off + 64 * (it % 3) + 32 * c;
-      if (!mbar_wait(bar(C::bSFull + it % 3), (it / 3) & 1, abort_flag, p.status)) {
+      const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
+      if (!mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -355,13 +382,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             m = mx;
           }
         }
-        // the issuer must have taken step it - 2 before this buffer's barrier moves on
-        if (it >= 2 && !mbar_wait(bar(C::bPCons + pr), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
         tc_fence_before();
-        mbar_arrive(bar(C::bPFull + pr));
+        mbar_arrive(bar(C::bPFull + bb));
         continue;
       }
       uint32_t keep = 0xFFFFFFFFu;
@@ -377,7 +399,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (hh == 1) {
             // this warpgroup's dP columns are in registers: the next dP may land
             tc_fence_before();
-            mbar_arrive(bar(C::bDPEmpty + pr));
+            mbar_arrive(bar(C::bDPEmpty));
           }
         } else {
           tmem_ld_wait16(sr);
@@ -423,21 +445,17 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_st8<0>(tSc + 16 * hh + 8, ev);
       }
       tmem_st_wait();
-      // The issuer must have read step it - 2's votes (and taken that phase of
-      // bPFull) before this step's votes overwrite them.
-      if (it >= 2 && !mbar_wait(bar(C::bPCons + pr), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) flags[8 * pr + 4 * c + wq] = lo_any ? 1 : 0;
+      // Step it - 2 used these vote slots; its accumulating MMAs were issued
+      // (the votes read) before S(it) could land in this buffer.
+      if (lane == 0) flags[16 * bb + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
-      mbar_arrive(bar(C::bPFull + pr));
+      mbar_arrive(bar(C::bPFull + bb));
     }
     if (!kDq && ok && !merged) {
-      // This warpgroup saw no output step (tiny key ranges): still publish its statistics.
+      // No output step (empty key range): still publish the statistics.
       ok = merge_stats();
     }
-    // Epilogue: O (forward) or scale * dQ; warpgroup rg writes columns [rg*d/4, (rg+1)*d/4).
+    // Epilogue: O (forward) or scale * dQ; warpgroup c writes columns [c*d/4, (c+1)*d/4).
     const bool have_acc = nsteps > first_out;
     if (ok && have_acc) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
@@ -447,7 +465,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const float mul = kDq ? p.scale : 1.f;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
-        const int col = rg * (D / 4) + 16 * cc;
+        const int col = c * (D / 4) + 16 * cc;
         uint32_t r[16];
         if (have_acc) {
           tmem_ld16(tAcc + lane_off + col, r);
@@ -466,7 +484,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           g[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      if (!kDq && rg == 0 && i < p.N)
+      if (!kDq && c == 0 && i < p.N)
         p.lse_out[(long long)bh * p.N + i] = (L2 == INFINITY) ? -INFINITY : L2 * 0.6931471805599453f;
     }
   }
