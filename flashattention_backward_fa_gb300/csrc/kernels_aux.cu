@@ -97,11 +97,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
 // issues all of their loads before reducing, to keep enough bytes in flight.
 constexpr int kVecRows = 4;
 
-// Row r of the enumeration -> (bh, i).
-__device__ __forceinline__ void vec_row(const AttnParams& p, long long r, int& bh, int& i) {
-  i = (int)(r % p.n_pad);
-  bh = (int)(r / p.n_pad);
-}
+// Rows of one (batch, head) per block: 8 warps x (32 / (d/8)) rows x kVecRows.
+template <int D>
+constexpr int vec_block_rows() { return 8 * (32 / (D / 8)) * kVecRows; }
 
 template <int D>
 __device__ __forceinline__ float group_sum(float v) {
@@ -123,76 +121,70 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
   return acc;
 }
 
+// Grid: x = block of vec_block_rows<D>() positions, y = batch * head.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_constant__ AttnParams p) {
   constexpr int G = D / 8;            // lanes per row
   constexpr int kRowsPerWarp = 32 / G;
-  const long long rows = (long long)p.B * p.H * p.n_pad;
-  const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long row0 = warp * (kRowsPerWarp * kVecRows) + lane / G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bh = blockIdx.y;
+  const int ib = blockIdx.x * vec_block_rows<D>() + warp * (kRowsPerWarp * kVecRows) + lane / G;
   const int e0 = (lane % G) * 8;
+  const T* o = static_cast<const T*>(p.o) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh + e0;
+  const T* g = static_cast<const T*>(p.dout) + (o - static_cast<const T*>(p.o));
   uint4 ov[kVecRows], gv[kVecRows];
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
-    const long long row = row0 + (long long)r * kRowsPerWarp;
+    const int i = ib + r * kRowsPerWarp;
     ov[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
-    if (row < rows) {
-      int bh, i;
-      vec_row(p, row, bh, i);
-      if (i < p.N) {
-        const long long off = (long long)(bh / p.H) * p.sb + (long long)i * p.sn + (long long)(bh % p.H) * p.sh + e0;
-        ov[r] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + off));
-        gv[r] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off));
-      }
+    if (i < p.N) {
+      ov[r] = __ldg(reinterpret_cast<const uint4*>(o + (long long)i * p.sn));
+      gv[r] = __ldg(reinterpret_cast<const uint4*>(g + (long long)i * p.sn));
     }
   }
+  const long long ws0 = (long long)bh * p.n_pad;
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
-    const long long row = row0 + (long long)r * kRowsPerWarp;
+    const int i = ib + r * kRowsPerWarp;
     const float acc = group_sum<D>(dot8<T>(ov[r], gv[r], 0.f));
-    if (row >= rows) continue;
-    int bh, i;
-    vec_row(p, row, bh, i);
-    const long long ws = (long long)bh * p.n_pad + i;
+    if (i >= p.n_pad) continue;
     if (e0 == 0) {
-      p.ws_D[ws] = acc;
-      p.ws_L2[ws] = (i < p.N) ? p.lse[(long long)bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
+      p.ws_D[ws0 + i] = acc;
+      p.ws_L2[ws0 + i] = (i < p.N) ? p.lse[(long long)bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
     }
     if (p.ws_dq != nullptr) {
-      float4* dq = reinterpret_cast<float4*>(p.ws_dq + ws * D + e0);
+      float4* dq = reinterpret_cast<float4*>(p.ws_dq + (ws0 + i) * D + e0);
       dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
 
-// dQ = scale * dQ_accum for 16-bit outputs with d in {64, 128}, eight elements a lane.
+// dQ = scale * dQ_accum for 16-bit outputs with d in {64, 128}, eight elements a
+// lane; the grid is laid out as for preprocess_vec_kernel.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) dq_convert_vec_kernel(const __grid_constant__ AttnParams p) {
   constexpr int G = D / 8;
   constexpr int kRowsPerWarp = 32 / G;
-  const long long rows = (long long)p.B * p.H * p.n_pad;
-  const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long row0 = warp * (kRowsPerWarp * kVecRows) + lane / G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bh = blockIdx.y;
+  const int ib = blockIdx.x * vec_block_rows<D>() + warp * (kRowsPerWarp * kVecRows) + lane / G;
   const int e0 = (lane % G) * 8;
+  const float* src = p.ws_dq + (long long)bh * p.n_pad * D + e0;
+  T* dst = static_cast<T*>(p.out) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh + e0;
   float4 a[kVecRows], c[kVecRows];
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
-    const long long row = row0 + (long long)r * kRowsPerWarp;
-    if (row < rows && (int)(row % p.n_pad) < p.N) {
-      const float4* src = reinterpret_cast<const float4*>(p.ws_dq + row * D + e0);
-      a[r] = __ldg(src);
-      c[r] = __ldg(src + 1);
+    const int i = ib + r * kRowsPerWarp;
+    if (i < p.N) {
+      const float4* s4 = reinterpret_cast<const float4*>(src + (long long)i * D);
+      a[r] = __ldg(s4);
+      c[r] = __ldg(s4 + 1);
     }
   }
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
-    const long long row = row0 + (long long)r * kRowsPerWarp;
-    if (row >= rows) continue;
-    const int i = (int)(row % p.n_pad);
-    const int bh = (int)(row / p.n_pad);
+    const int i = ib + r * kRowsPerWarp;
     if (i >= p.N) continue;
     const float v[8] = {a[r].x, a[r].y, a[r].z, a[r].w, c[r].x, c[r].y, c[r].z, c[r].w};
     uint32_t w[4];
@@ -202,9 +194,7 @@ __global__ void __launch_bounds__(256) dq_convert_vec_kernel(const __grid_consta
       w[x] = (uint32_t)(*reinterpret_cast<const uint16_t*>(&lo)) |
              ((uint32_t)(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
     }
-    T* dst = static_cast<T*>(p.out) + (long long)(bh / p.H) * p.sb + (long long)i * p.sn +
-             (long long)(bh % p.H) * p.sh + e0;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + (long long)i * p.sn) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -412,15 +402,15 @@ static inline unsigned grid_for_rows(long long rows, int rows_per_block) {
 
 cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
   const long long rows = (long long)p.B * p.n_pad * p.H;
-  if (dtype != 0 && (p.d == 64 || p.d == 128)) {
-    // 256 threads = 8 warps, each covering (32 / (d/8)) * kVecRows rows
-    const unsigned g = grid_for_rows(rows, 8 * (32 / (p.d / 8)) * kVecRows);
+  if (dtype != 0 && (p.d == 64 || p.d == 128) && p.B * p.H <= 65535) {
+    const dim3 g((unsigned)((p.n_pad + vec_block_rows<128>() - 1) / vec_block_rows<128>()), (unsigned)(p.B * p.H));
+    const dim3 g64((unsigned)((p.n_pad + vec_block_rows<64>() - 1) / vec_block_rows<64>()), (unsigned)(p.B * p.H));
     if (p.d == 128)
       dtype == 1 ? preprocess_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
                  : preprocess_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);
     else
-      dtype == 1 ? preprocess_vec_kernel<__half, 64><<<g, 256, 0, st>>>(p)
-                 : preprocess_vec_kernel<__nv_bfloat16, 64><<<g, 256, 0, st>>>(p);
+      dtype == 1 ? preprocess_vec_kernel<__half, 64><<<g64, 256, 0, st>>>(p)
+                 : preprocess_vec_kernel<__nv_bfloat16, 64><<<g64, 256, 0, st>>>(p);
     return cudaGetLastError();
   }
   const unsigned grid = grid_for_rows(rows, 8);
@@ -431,15 +421,15 @@ cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
 }
 
 cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st) {
-  if (dtype != 0 && (p.d == 64 || p.d == 128)) {
-    const long long prow = (long long)p.B * p.n_pad * p.H;
-    const unsigned g = grid_for_rows(prow, 8 * (32 / (p.d / 8)) * kVecRows);
+  if (dtype != 0 && (p.d == 64 || p.d == 128) && p.B * p.H <= 65535) {
+    const dim3 g((unsigned)((p.n_pad + vec_block_rows<128>() - 1) / vec_block_rows<128>()), (unsigned)(p.B * p.H));
+    const dim3 g64((unsigned)((p.n_pad + vec_block_rows<64>() - 1) / vec_block_rows<64>()), (unsigned)(p.B * p.H));
     if (p.d == 128)
       dtype == 1 ? dq_convert_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
                  : dq_convert_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);
     else
-      dtype == 1 ? dq_convert_vec_kernel<__half, 64><<<g, 256, 0, st>>>(p)
-                 : dq_convert_vec_kernel<__nv_bfloat16, 64><<<g, 256, 0, st>>>(p);
+      dtype == 1 ? dq_convert_vec_kernel<__half, 64><<<g64, 256, 0, st>>>(p)
+                 : dq_convert_vec_kernel<__nv_bfloat16, 64><<<g64, 256, 0, st>>>(p);
     return cudaGetLastError();
   }
   const long long rows = (long long)p.B * p.N * p.H;
