@@ -219,8 +219,8 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
   p.dk = dk;
   p.dv = dv;
   char* ws = static_cast<char*>(workspace);
-  p.ws_L2 = reinterpret_cast<float*>(ws + w.off_L2);
-  p.ws_D = reinterpret_cast<float*>(ws + w.off_D);
+  p.ws_nL2 = reinterpret_cast<float*>(ws + w.off_L2);
+  p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
   if ((rc = status_ptr(&p.status))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -38,8 +38,8 @@ struct AttnParams {
   void* dk;
   void* dv;
   float* lse_out;         // forward: L written here
-  float* ws_L2;           // [B*H, n_pad]  L * log2(e), +inf past N
-  float* ws_D;            // [B*H, n_pad]  rowsum(dO o O), 0 past N
+  float* ws_nL2;          // [B*H, n_pad]  -L * log2(e), -inf past N (negated: feeds an FMA addend)
+  float* ws_nD;           // [B*H, n_pad]  -rowsum(dO o O), 0 past N (negated: feeds an add)
   float* ws_dq;           // [B*H, n_pad, d] fp32 dQ accumulator (atomic mode) or null
   unsigned int* status;   // device status word (timeout bits)
 };

@@ -2,9 +2,11 @@
 //
 // * preprocess: D_i = rowsum(dO o O) in fp32 ("FlashAttention backward",
 //   §The gradients, and the one scalar that makes them local: one cheap pass
-//   over dO and O before the main loop), plus L*log2(e) into a padded
-//   workspace vector and, in atomic-dQ mode, the zero fill of the fp32 dQ
-//   accumulator.
+//   over dO and O before the main loop), stored negated, plus -L*log2(e) into
+//   a padded workspace vector and, in atomic-dQ mode, the zero fill of the
+//   fp32 dQ accumulator. Both vectors are kept negated so that the consumers
+//   use them as addends (S*scale*log2e + (-L*log2e) is one FMA, dP + (-D) one
+//   add, also in packed two-wide form).
 // * dq_convert: dQ = scale * dQ_accum, rounded to the tensor dtype (atomic mode).
 // * fp32 kernels: forward (two passes: row statistics, then O) and the
 //   key-major dK/dV plus query-major dQ kernels of the backward, on CUDA cores.
@@ -80,8 +82,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
     acc = warp_sum(acc);
   }
   if (lane == 0) {
-    p.ws_D[ws] = acc;
-    p.ws_L2[ws] = (i < p.N) ? p.lse[(long long)bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
+    p.ws_nD[ws] = -acc;
+    p.ws_nL2[ws] = (i < p.N) ? -(p.lse[(long long)bh * p.N + i] * kLog2e) : __int_as_float(0xff800000);
   }
   if (p.ws_dq != nullptr) {
     float* dq = p.ws_dq + ws * p.d;
@@ -149,8 +151,8 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_consta
     const float acc = group_sum<D>(dot8<T>(ov[r], gv[r], 0.f));
     if (i >= p.n_pad) continue;
     if (e0 == 0) {
-      p.ws_D[ws0 + i] = acc;
-      p.ws_L2[ws0 + i] = (i < p.N) ? p.lse[(long long)bh * p.N + i] * kLog2e : __int_as_float(0x7f800000);
+      p.ws_nD[ws0 + i] = -acc;
+      p.ws_nL2[ws0 + i] = (i < p.N) ? -(p.lse[(long long)bh * p.N + i] * kLog2e) : __int_as_float(0xff800000);
     }
     if (p.ws_dq != nullptr) {
       float4* dq = reinterpret_cast<float4*>(p.ws_dq + (ws0 + i) * D + e0);
@@ -304,14 +306,14 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __gr
   __syncwarp();
   const int ilo = p.causal ? j : 0;
   const int ihi = p.window > 0 ? min(p.N - 1, j + p.window - 1) : p.N - 1;
-  const float* L2 = p.ws_L2 + (long long)bh * p.n_pad;
-  const float* Dv = p.ws_D + (long long)bh * p.n_pad;
+  const float* nL2 = p.ws_nL2 + (long long)bh * p.n_pad;
+  const float* nD = p.ws_nD + (long long)bh * p.n_pad;
   float dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
   for (int ib = ilo; ib <= ihi; ib += 32) {
     const int i = ib + lane;
     float pt = 0.f, ds = 0.f;
     if (i <= ihi) {
-      const float pv = ex2_approx(dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2 - L2[i]);
+      const float pv = ex2_approx(dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2 + nL2[i]);
       float dp = dot_row(vrow[w], row_ptr(p, p.dout, b, i, h), p.d);
       pt = pv;
       if (p.drop.threshold) {
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __gr
         pt = keep ? pv * p.drop.rp : 0.f;
         dp = keep ? dp * p.drop.rp : 0.f;
       }
-      ds = pv * (dp - Dv[i]);
+      ds = pv * (dp + nD[i]);
     }
     const int cnt = min(32, ihi - ib + 1);
     for (int t = 0; t < cnt; ++t) {
@@ -364,17 +366,17 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid
   __syncwarp();
   const int jlo = p.window > 0 ? max(0, i - p.window + 1) : 0;
   const int jhi = p.causal ? i : p.N - 1;
-  const float L2 = p.ws_L2[(long long)bh * p.n_pad + i];
-  const float Dv = p.ws_D[(long long)bh * p.n_pad + i];
+  const float nL2 = p.ws_nL2[(long long)bh * p.n_pad + i];
+  const float nD = p.ws_nD[(long long)bh * p.n_pad + i];
   float dq[4] = {0.f, 0.f, 0.f, 0.f};
   for (int jb = jlo; jb <= jhi; jb += 32) {
     const int j = jb + lane;
     float ds = 0.f;
     if (j <= jhi) {
-      const float pv = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 - L2);
+      const float pv = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 + nL2);
       float dp = dot_row(grow[w], row_ptr(p, p.v, b, j, h), p.d);
       if (p.drop.threshold) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
-      ds = pv * (dp - Dv);
+      ds = pv * (dp + nD);
     }
     const int cnt = min(32, jhi - jb + 1);
     for (int t = 0; t < cnt; ++t) {

@@ -15,6 +15,9 @@
 //   with red.add ("FlashAttention backward" §The loop structure, choice (a)).
 //
 // Keys sit on the 128 TMEM lanes: one thread owns one key row of S^T and dP^T.
+// Row-math warps wait warp-wide (warp_wait) and reconverge after per-lane
+// branches, because the TMEM loads and stores are warp-collective (.aligned)
+// and must not run on a split warp.
 // The row math turns them into P~T and dS^T, each rounded to 16 bits plus the
 // rounding residual where a tile holds probabilities above kSplitThreshold
 // (see interleave_split), and writes them back over the TMEM columns it has
@@ -170,8 +173,8 @@ __global__ void __launch_bounds__(kKVThreads, 1)
                       i0, h, b);
         }
         const long long ws = (long long)bh * p.n_pad + i0;
-        bulk_load(sb + C::oL + s * kStepQ * 4, p.ws_L2 + ws, kStepQ * 4, bar(C::bQFull + s));
-        bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_D + ws, kStepQ * 4, bar(C::bQFull + s));
+        bulk_load(sb + C::oL + s * kStepQ * 4, p.ws_nL2 + ws, kStepQ * 4, bar(C::bQFull + s));
+        bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_nD + ws, kStepQ * 4, bar(C::bQFull + s));
         issued = it + 1;
       }
       if (*abort_flag) {
@@ -202,11 +205,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
                       desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
         tc_commit_w(bar(C::bSFull + bb));
       }
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
+      __syncwarp();
     }
   } else if (warp == 3) {
     // ----------------------------- dP^T MMA issuer -----------------------------
@@ -229,11 +231,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
                       desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
         tc_commit_w(bar(C::bSFull + bb));
       }
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain + 2));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain + 2));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+      __syncwarp();
     }
   } else if (warp == 2) {
     // ----------------------- dV / dK (/ dQ^T) MMA issuer ----------------------
@@ -301,11 +302,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tc_commit_w(bar(C::bQEmpty + st));
       }
       tc_commit_w(bar(C::bAcc));
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain + 1));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain + 1));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ------------------------- row-math warpgroups --------------------------
@@ -326,9 +326,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
       const int i0 = i_first + it * kStepQ;
-      if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
-          (kAtomic && !mbar_wait(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
+      if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+          !warp_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
+          (kAtomic && !warp_wait(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -350,33 +350,54 @@ __global__ void __launch_bounds__(kKVThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t sr[16], dr[16];
+        __syncwarp();  // per-lane mask branches above: converge for the TMEM loads
         tmem_ld16(tSc + 16 * hh, sr);
         tmem_ld16(tdPc + 16 * hh, dr);
         tmem_ld_wait16x2(sr, dr);
         float cmax = 0.f;
         float pt[16], ds[16];
         // P, dropout and dS for the 16 pairs; the unmasked variant skips the
-        // per-pair mask test on full tiles.
+        // per-pair mask test on full tiles. L and D arrive negated, so
+        // P = exp2(S * scale*log2e + (-L*log2e)) and dS = P * (dP + (-D)); without
+        // dropout the FMA, add and multiply run on pairs of columns.
         auto elementwise = [&](auto masked) {
 #pragma unroll
           for (int x = 0; x < 16; x += 4) {
             const float4 l4 = L4[(16 * hh + x) >> 2], d4 = D4[(16 * hh + x) >> 2];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+            if constexpr (!kDrop) {
+              const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+              float pv[4];
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), c2, f2_pack(l4.x, l4.y)),
+                        pv[0], pv[1]);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3])), c2,
+                               f2_pack(l4.z, l4.w)),
+                        pv[2], pv[3]);
 #pragma unroll
-            for (int y = 0; y < 4; ++y) {
-              const int bit = 16 * hh + x + y;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, -lv[y]));
-              if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
-              cmax = fmaxf(cmax, pv);
-              float dpv = __uint_as_float(dr[x + y]);
-              float ptv = pv;
-              if constexpr (kDrop) {
-                const bool kept = (keep >> bit) & 1u;
-                dpv = kept ? dpv * p.drop.rp : 0.f;
-                ptv = kept ? pv * p.drop.rp : 0.f;
+              for (int y = 0; y < 4; ++y) {
+                pv[y] = ex2_approx(pv[y]);
+                if constexpr (decltype(masked)::value) pv[y] = ((allow >> (16 * hh + x + y)) & 1u) ? pv[y] : 0.f;
+                pt[x + y] = pv[y];
               }
-              ds[x + y] = pv * (dpv - dv[y]);
-              pt[x + y] = ptv;
+              cmax = fmax3(cmax, pv[0], pv[1]);
+              cmax = fmax3(cmax, pv[2], pv[3]);
+              const uint64_t d01 = f2_add(f2_pack(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), f2_pack(d4.x, d4.y));
+              const uint64_t d23 =
+                  f2_add(f2_pack(__uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3])), f2_pack(d4.z, d4.w));
+              f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), d01), ds[x], ds[x + 1]);
+              f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), d23), ds[x + 2], ds[x + 3]);
+            } else {
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+              for (int y = 0; y < 4; ++y) {
+                const int bit = 16 * hh + x + y;
+                float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, lv[y]));
+                if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
+                cmax = fmaxf(cmax, pv);
+                const bool kept = (keep >> bit) & 1u;
+                const float dpv = kept ? __uint_as_float(dr[x + y]) * p.drop.rp : 0.f;
+                ds[x + y] = pv * (dpv + dv[y]);
+                pt[x + y] = kept ? pv * p.drop.rp : 0.f;
+              }
             }
           }
         };
@@ -384,6 +405,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
           elementwise(std::false_type{});
         else
           elementwise(std::true_type{});
+        // The lanes may have split over the two variants: reconverge before the
+        // warp-collective vote and TMEM stores below.
+        __syncwarp();
         uint32_t hp[8], hd[8], ep[8], ed[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
@@ -428,7 +452,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       mbar_arrive(bar(C::bPFull + bb));
       if constexpr (kAtomic) {
         // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
-        if (!mbar_wait(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -446,7 +470,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       }
     }
     // Epilogue: warpgroups 0, 1 write dV and 2, 3 write scale * dK, each half of the columns.
-    if (ok && nsteps > 0) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
+    if (ok && nsteps > 0) ok = warp_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const bool isK = rg >= 2;

@@ -15,7 +15,9 @@
 // so O never needs rescaling — and accumulates O += (P o Z/(1-p)) V.
 //
 // Queries sit on the 128 TMEM lanes: one thread owns one query row, so L_i and
-// D_i are per-thread scalars. A step covers 128 keys, so every S, dP and
+// D_i are per-thread scalars. Row-math warps wait warp-wide (warp_wait) and
+// reconverge after per-lane branches: TMEM loads and stores are warp-collective
+// (.aligned) and must not run on a split warp. A step covers 128 keys, so every S, dP and
 // accumulating MMA has N = 128 (N = 64 MMAs are limited by shared-memory
 // operand reads to about two thirds of the tensor rate). The row math writes
 // dS (or P~) back over the S columns it has read, rounded to 16 bits with the
@@ -222,11 +224,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tc_commit_w(bar(C::bSFull + bb));
         if (!kDq) tc_commit_w(bar(C::bEEmpty + ks));   // forward: K is done once S is
       }
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
+      __syncwarp();
     }
   } else if (warp == 3) {
     // ---------------------- dP MMA issuer (dQ mode only) ----------------------
@@ -250,11 +251,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tc_commit_w(bar(C::bSFull + (it & 1)));
         tc_commit_w(bar(C::bEEmpty + se));
       }
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain + 2));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain + 2));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
+      __syncwarp();
     }
   } else if (warp == 2) {
     // ------------------ accumulating MMA issuer (O or dQ) ---------------------
@@ -297,11 +297,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
       tc_commit_w(bar(C::bAcc));
-      if (!ok) {
-        tc_commit_w(bar(C::bDrain + 1));
-        if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
-        __syncwarp();
-      }
+      // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
+      tc_commit_w(bar(C::bDrain + 1));
+      if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // ---------------- row-math warpgroups + epilogue ----------------------
@@ -314,10 +313,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tdPc = tdP + lane_off + 32 * c;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
-    float L2 = INFINITY, Dv = 0.f;
+    // -L*log2(e) (-inf for a row with no allowed key) and -D: the negated forms
+    // are addends of one FMA / add (packed two-wide below).
+    float nL2 = -INFINITY, nD = 0.f;
     if (kDq) {
-      L2 = p.ws_L2[ws];
-      Dv = p.ws_D[ws];
+      nL2 = p.ws_nL2[ws];
+      nD = p.ws_nD[ws];
     }
     float m = -INFINITY, l = 0.f;  // forward statistics of this warpgroup's columns, log2 domain
     bool merged = kDq;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       st[(2 * c) * kRowsQ + il] = m;
       st[(2 * c + 1) * kRowsQ + il] = l;
       mbar_arrive(bar(C::bStats));
-      if (!mbar_wait(bar(C::bStats), 0, abort_flag, p.status)) return false;
+      if (!warp_wait(bar(C::bStats), 0, abort_flag, p.status)) return false;
       float mm = -INFINITY;
 #pragma unroll
       for (int g = 0; g < 4; ++g) mm = fmaxf(mm, st[(2 * g) * kRowsQ + il]);
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int g = 0; g < 4; ++g) ll += st[(2 * g + 1) * kRowsQ + il] * ex2_approx(st[(2 * g) * kRowsQ + il] - mm);
       }
-      L2 = (ll > 0.f) ? mm + lg2_approx(ll) : INFINITY;
+      nL2 = (ll > 0.f) ? -(mm + lg2_approx(ll)) : -INFINITY;
       return true;
     };
     for (int it = 0; it < nsteps; ++it) {
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         merged = true;
       }
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
-      if (!mbar_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+      if (!warp_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -365,6 +366,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t sr[16];
+          __syncwarp();  // the statistics update branches per lane: converge for the TMEM load
           tmem_ld16(tSc + 16 * hh, sr);
           tmem_ld_wait16(sr);
           float x[16];
@@ -389,45 +391,79 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
       bool lo_any = false;
+      // dQ: both halves of this warpgroup's dP columns come in with the first S
+      // half, so the dP buffer is released (and the next dP MMAs may run) before
+      // any of the step's arithmetic.
+      uint32_t dr2[2][16];
+      uint32_t sr[16];
+      tmem_ld16(tSc, sr);
+      if constexpr (kDq) {
+        tmem_ld16(tdPc, dr2[0]);
+        tmem_ld16(tdPc + 16, dr2[1]);
+        tmem_ld_wait16x3(sr, dr2[0], dr2[1]);
+        tc_fence_before();
+        mbar_arrive(bar(C::bDPEmpty));
+      } else {
+        tmem_ld_wait16(sr);
+      }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[16], dr[16];
-        tmem_ld16(tSc + 16 * hh, sr);
-        if constexpr (kDq) {
-          tmem_ld16(tdPc + 16 * hh, dr);
-          tmem_ld_wait16x2(sr, dr);
-          if (hh == 1) {
-            // this warpgroup's dP columns are in registers: the next dP may land
-            tc_fence_before();
-            mbar_arrive(bar(C::bDPEmpty));
-          }
-        } else {
+        if (hh == 1) {
+          __syncwarp();
+          tmem_ld16(tSc + 16, sr);
           tmem_ld_wait16(sr);
         }
+        const uint32_t (&dr)[16] = dr2[hh];
         float outv[16];
         float cmax = 0.f;
         auto elementwise = [&](auto masked) {
+          if constexpr (!kDrop) {
+            // pairs of columns through the packed FMA / add / multiply
+            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), l2 = f2_pack(nL2, nL2);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int bit = 16 * hh + e;
-            float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, -L2));
-            if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
-            cmax = fmaxf(cmax, pv);
-            const bool kept = !kDrop || ((keep >> bit) & 1u);
-            const float rp = kDrop ? p.drop.rp : 1.f;
-            if constexpr (kDq) {
-              const float dpv = kept ? __uint_as_float(dr[e]) * rp : 0.f;
-              outv[e] = pv * (dpv - Dv);
-            } else {
-              outv[e] = kept ? pv * rp : 0.f;
+            for (int e = 0; e < 16; e += 2) {
+              float p0, p1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, l2), p0, p1);
+              p0 = ex2_approx(p0);
+              p1 = ex2_approx(p1);
+              if constexpr (decltype(masked)::value) {
+                p0 = ((allow >> (16 * hh + e)) & 1u) ? p0 : 0.f;
+                p1 = ((allow >> (16 * hh + e + 1)) & 1u) ? p1 : 0.f;
+              }
+              cmax = fmax3(cmax, p0, p1);
+              if constexpr (kDq) {
+                const uint64_t dd = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(nD, nD));
+                f2_unpack(f2_mul(f2_pack(p0, p1), dd), outv[e], outv[e + 1]);
+              } else {
+                outv[e] = p0;
+                outv[e + 1] = p1;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int bit = 16 * hh + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, nL2));
+              if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
+              cmax = fmaxf(cmax, pv);
+              const bool kept = (keep >> bit) & 1u;
+              if constexpr (kDq) {
+                const float dpv = kept ? __uint_as_float(dr[e]) * p.drop.rp : 0.f;
+                outv[e] = pv * (dpv + nD);
+              } else {
+                outv[e] = kept ? pv * p.drop.rp : 0.f;
+              }
             }
           }
         };
-        // L2 = +inf (a row with no allowed key) gives exp2(-inf) = 0 on the fast path too.
+        // nL2 = -inf (a row with no allowed key) gives exp2(-inf) = 0 on the fast path too.
         if (allow == 0xFFFFFFFFu)
           elementwise(std::false_type{});
         else
           elementwise(std::true_type{});
+        // The lanes may have split over the two variants: reconverge before the
+        // warp-collective vote and TMEM stores below.
+        __syncwarp();
         uint32_t hv[8], ev[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
@@ -457,7 +493,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     // Epilogue: O (forward) or scale * dQ; warpgroup c writes columns [c*d/4, (c+1)*d/4).
     const bool have_acc = nsteps > first_out;
-    if (ok && have_acc) ok = mbar_wait(bar(C::bAcc), 0, abort_flag, p.status);
+    if (ok && have_acc) ok = warp_wait(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
@@ -485,7 +521,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
       if (!kDq && c == 0 && i < p.N)
-        p.lse_out[(long long)bh * p.N + i] = (L2 == INFINITY) ? -INFINITY : L2 * 0.6931471805599453f;
+        p.lse_out[(long long)bh * p.N + i] = (nL2 == -INFINITY) ? -INFINITY : -nL2 * 0.6931471805599453f;
     }
   }
 
