@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_host.h"
 #include "fa_internal.h"
 
 namespace fa {
@@ -141,6 +142,34 @@ void fill_params(AttnParams& p, int B, int H, int N, int d, fa_strides s, float 
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// A second stream per device on which the deterministic backward runs its dQ
+// kernel beside the dK/dV kernel (fork after the preprocess, join before
+// returning), so that the two grids share the tail of each other's last wave
+// instead of running back to back. Created on first use and kept.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+// Guards g_side and serialises each fork/join enqueue sequence. Distinct from
+// g_mu, which the stage launches below take themselves.
+std::mutex g_side_mu;
+
+// Caller holds g_side_mu.
+int side_stream_locked(SideStream** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  *out = &ss;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,13 +276,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
            int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
-  const fa_bwd_stage_id stages[3] = {FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ};
-  for (fa_bwd_stage_id s : stages) {
-    const int rc = fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal,
-                                window, dropout_p, seed, offset, deterministic, workspace, workspace_bytes, stream);
-    if (rc) return rc;
-  }
-  return FA_OK;
+  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                     dropout_p, seed, offset, deterministic, workspace, workspace_bytes, stream, true);
 }
 
 int fa_get_device_status(unsigned int* status, int clear) {
@@ -268,3 +292,37 @@ int fa_get_device_status(unsigned int* status, int clear) {
 }
 
 }  // extern "C"
+
+namespace fa {
+
+int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream) {
+  auto stage = [&](fa_bwd_stage_id s, void* st) {
+    return fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                        dropout_p, seed, offset, deterministic, workspace, workspace_bytes, st);
+  };
+  int rc = stage(FA_BWD_PREPROCESS, stream);
+  if (rc) return rc;
+  if (!allow_side_stream || !deterministic || dtype == FA_F32) {
+    if ((rc = stage(FA_BWD_DKDV, stream))) return rc;
+    return stage(FA_BWD_DQ, stream);
+  }
+  // Fork: the dQ kernel waits for the preprocess on the side stream while the
+  // dK/dV kernel follows it on the caller's stream; join before returning. The
+  // enqueue sequence is serialised because the fork/join events are shared.
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = nullptr;
+  if ((rc = side_stream_locked(&ss))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaEventRecord(ss->fork, st) != cudaSuccess || cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if ((rc = stage(FA_BWD_DKDV, stream))) return rc;
+  if ((rc = stage(FA_BWD_DQ, ss->stream))) return rc;
+  if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess || cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // namespace fa

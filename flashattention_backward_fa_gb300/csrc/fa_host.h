@@ -1,0 +1,17 @@
+// Host-side entry shared by the C-ABI translation units.
+#pragma once
+#include "fa.h"
+
+namespace fa {
+
+// The whole backward (preprocess, dK/dV, dQ) on `stream`. With
+// allow_side_stream, the deterministic 16-bit path runs its dQ kernel on a
+// second, library-owned stream beside the dK/dV kernel (fork after the
+// preprocess, join before returning); without it every kernel goes on `stream`
+// and nothing is created.
+int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream);
+
+}  // namespace fa

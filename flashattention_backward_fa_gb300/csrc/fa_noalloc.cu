@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_host.h"
 #include "fa_internal.h"
 
 namespace {
@@ -64,6 +65,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   void* scratch = nullptr;
   const int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window, dropout_p,
-                seed, offset, 1, scratch, kNoAllocScratchBytes, stream);
+  // Single stream: this entry point creates nothing, not even the side stream.
+  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                     dropout_p, seed, offset, 1, scratch, kNoAllocScratchBytes, stream, false);
 }

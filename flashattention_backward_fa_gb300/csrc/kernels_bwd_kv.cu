@@ -189,11 +189,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     {
       constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
       const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
-      bool ok = warp_wait(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !warp_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        if (!warp_wait<kIssuerPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !warp_wait<kIssuerPoll>(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -215,11 +215,11 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     {
       constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
       const uint64_t dV0 = make_sdesc(sb + C::oV, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
-      bool ok = warp_wait(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
-        if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-            !warp_wait(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        if (!warp_wait<kIssuerPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            !warp_wait<kIssuerPoll>(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1, st = t % C::kNS;
-        if (!warp_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kIssuerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -326,9 +326,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
       const int i0 = i_first + it * kStepQ;
-      if (!warp_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !warp_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
-          (kAtomic && !warp_wait(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
+      if (!warp_wait<kRowMathPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+          !warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
+          (kAtomic && !warp_wait<kRowMathPoll>(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       mbar_arrive(bar(C::bPFull + bb));
       if constexpr (kAtomic) {
         // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
-        if (!warp_wait(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kRowMathPoll>(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       }
     }
     // Epilogue: warpgroups 0, 1 write dV and 2, 3 write scale * dK, each half of the columns.
-    if (ok && nsteps > 0) ok = warp_wait(bar(C::bAcc), 0, abort_flag, p.status);
+    if (ok && nsteps > 0) ok = warp_wait<kRowMathPoll>(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const bool isK = rg >= 2;

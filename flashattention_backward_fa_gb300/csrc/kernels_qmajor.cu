@@ -204,14 +204,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
       const uint64_t dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
       const uint64_t dK0 = make_sdesc(sb + (kDq ? C::oL : C::oE), 16, 1024);
-      bool ok = warp_wait(bar(C::bRes), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int bb = it & 1;
         // K lives in ring L (dQ; one tile per step) or ring E (forward)
         const int ks = kDq ? it % C::kNL : it % C::kNE;
         const uint32_t kpar = kDq ? (it / C::kNL) & 1 : (it / C::kNE) & 1;
-        if (!warp_wait(bar((kDq ? C::bLFull : C::bEFull) + ks), kpar, abort_flag, p.status) ||
-            !warp_wait(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+        if (!warp_wait<kIssuerPoll>(bar((kDq ? C::bLFull : C::bEFull) + ks), kpar, abort_flag, p.status) ||
+            !warp_wait<kIssuerPoll>(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -234,11 +234,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (kDq) {
       constexpr uint32_t idS = make_idesc(128, kStepKV, kBf16, false, false);
       const uint64_t dO0 = make_sdesc(sb + C::oDO, 16, 1024), dV0 = make_sdesc(sb + C::oE, 16, 1024);
-      bool ok = warp_wait(bar(C::bRes), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
         const int se = it % C::kNE;
-        if (!warp_wait(bar(C::bEFull + se), (it / C::kNE) & 1, abort_flag, p.status) ||
-            (it > 0 && !warp_wait(bar(C::bDPEmpty), (it - 1) & 1, abort_flag, p.status))) {
+        if (!warp_wait<kIssuerPoll>(bar(C::bEFull + se), (it / C::kNE) & 1, abort_flag, p.status) ||
+            (it > 0 && !warp_wait<kIssuerPoll>(bar(C::bDPEmpty), (it - 1) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1;
-        if (!warp_wait(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kIssuerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       st[(2 * c) * kRowsQ + il] = m;
       st[(2 * c + 1) * kRowsQ + il] = l;
       mbar_arrive(bar(C::bStats));
-      if (!warp_wait(bar(C::bStats), 0, abort_flag, p.status)) return false;
+      if (!warp_wait<kRowMathPoll>(bar(C::bStats), 0, abort_flag, p.status)) return false;
       float mm = -INFINITY;
 #pragma unroll
       for (int g = 0; g < 4; ++g) mm = fmaxf(mm, st[(2 * g) * kRowsQ + il]);
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         merged = true;
       }
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
-      if (!warp_wait(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+      if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     // Epilogue: O (forward) or scale * dQ; warpgroup c writes columns [c*d/4, (c+1)*d/4).
     const bool have_acc = nsteps > first_out;
-    if (ok && have_acc) ok = warp_wait(bar(C::bAcc), 0, abort_flag, p.status);
+    if (ok && have_acc) ok = warp_wait<kRowMathPoll>(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
