@@ -528,11 +528,12 @@ __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t b
   return sel >= dp.threshold;
 }
 
-// Keep bits (bit x <-> query i0 + x) of 32 consecutive queries for one key j.
-static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
+// Keep bits (bit x <-> query i0 + x) of n <= 32 consecutive queries for one key j.
+static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j,
+                                                          int n = 32) {
   uint32_t bits = 0;
 #pragma unroll 1
-  for (int x = 0; x < 32; ++x) bits |= (uint32_t)dropout_keep(dp, bh, N, i0 + x, j) << x;
+  for (int x = 0; x < n; ++x) bits |= (uint32_t)dropout_keep(dp, bh, N, i0 + x, j) << x;
   return bits;
 }
 

@@ -273,6 +273,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tc_fence_after();
         if (t >= first_out) {
           const int li = t - first_out, sl = li % C::kNL;
+          // Forward: V (ring L) must have landed before the MMA reads it. In the dQ
+          // kernel ring L holds K, whose arrival the S issuer waited for before S.
+          if (!kDq && !warp_wait<kIssuerPoll>(bar(C::bLFull + sl), (li / C::kNL) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           const uint32_t first = t > first_out ? 1u : 0u;
           const int4* f4 = reinterpret_cast<const int4*>(const_cast<const int*>(flags) + 16 * bt);
           int any = 0;
