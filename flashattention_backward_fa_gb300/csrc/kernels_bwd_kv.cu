@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       if (lane == 0) flags[8 * bb + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
       if constexpr (kAtomic) fence_proxy_async_smem();
-      mbar_arrive(bar(C::bPFull + bb));
+      warp_arrive(bar(C::bPFull + bb));
       if constexpr (kAtomic) {
         // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
         if (!warp_wait<kRowMathPoll>(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tmem_ld32(tdPc, r0);
         tmem_ld_wait(r0);
         tc_fence_before();
-        mbar_arrive(bar(C::bDPEmpty + bb));
+        warp_arrive(bar(C::bDPEmpty + bb));
         if (jl < D) {
           float* dst = p.ws_dq + ((long long)bh * p.n_pad + base) * D + jl;
 #pragma unroll

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       float* st = reinterpret_cast<float*>(smem + C::oStats);
       st[(2 * c) * kRowsQ + il] = m;
       st[(2 * c + 1) * kRowsQ + il] = l;
-      mbar_arrive(bar(C::bStats));
+      warp_arrive(bar(C::bStats));
       if (!warp_wait<kRowMathPoll>(bar(C::bStats), 0, abort_flag, p.status)) return false;
       float mm = -INFINITY;
 #pragma unroll
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(bar(C::bPFull + bb));
+        warp_arrive(bar(C::bPFull + bb));
         continue;
       }
       uint32_t keep = 0xFFFFFFFFu;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld16(tdPc + 16, dr2[1]);
         tmem_ld_wait16x3(sr, dr2[0], dr2[1]);
         tc_fence_before();
-        mbar_arrive(bar(C::bDPEmpty));
+        warp_arrive(bar(C::bDPEmpty));
       } else {
         tmem_ld_wait16(sr);
       }
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // (the votes read) before S(it) could land in this buffer.
       if (lane == 0) flags[16 * bb + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
-      mbar_arrive(bar(C::bPFull + bb));
+      warp_arrive(bar(C::bPFull + bb));
     }
     if (!kDq && ok && !merged) {
       // No output step (empty key range): still publish the statistics.
