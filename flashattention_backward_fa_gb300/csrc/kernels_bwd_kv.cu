@@ -65,11 +65,13 @@ struct KVCfg {
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kNS;
-  static constexpr int bSFull = bQEmpty + kNS;
-  static constexpr int bSEmpty = bSFull + 2;
+  static constexpr int bSFull = bQEmpty + kNS;                // [2]: S^T landed
+  static constexpr int bDPFull = bSFull + 2;                   // [2]: dP^T landed
+  static constexpr int bSEmpty = bDPFull + 2;
   static constexpr int bDPEmpty = bSEmpty + 2;
   static constexpr int bPFull = bDPEmpty + 2;
-  static constexpr int bPEmpty = bPFull + 2;
+  static constexpr int bDSFull = bPFull + 2;                   // [2]: dS^T image written
+  static constexpr int bPEmpty = bDSFull + 2;
   static constexpr int bDQFull = bPEmpty + 2;
   static constexpr int bAcc = bDQFull + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
@@ -124,10 +126,12 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       mbar_init(bar(C::bQEmpty + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::bSFull + x), 2);                       // S^T and dP^T both landed
+      mbar_init(bar(C::bSFull + x), 1);                        // S^T landed
+      mbar_init(bar(C::bDPFull + x), 1);                       // dP^T landed
       mbar_init(bar(C::bSEmpty + x), 1);                       // dV done with the P~T image
       mbar_init(bar(C::bDPEmpty + x), kAtomic ? 256 : 1);     // dK done / dQ^T drained
-      mbar_init(bar(C::bPFull + x), 256);                      // two warpgroups per step
+      mbar_init(bar(C::bPFull + x), 256);                      // P~T image of two warpgroups
+      mbar_init(bar(C::bDSFull + x), 256);                     // dS^T image of two warpgroups
       mbar_init(bar(C::bPEmpty + x), 1);                       // atomic: shared dS^T free
       mbar_init(bar(C::bDQFull + x), 1);
     }
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ss_w(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
                       desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit_w(bar(C::bSFull + bb));
+        tc_commit_w(bar(C::bDPFull + bb));
       }
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
       tc_commit_w(bar(C::bDrain + 2));
@@ -267,6 +271,12 @@ __global__ void __launch_bounds__(kKVThreads, 1)
             tc_mma_ts_w(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
         }
         tc_commit_w(bar(C::bSEmpty + bt));
+        // dK (and dQ^T) once the dS^T image is in place; dV above only needed P~T.
+        if (!warp_wait<kIssuerPoll>(bar(C::bDSFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         if constexpr (!kAtomic) {
           // dK += dS^T Q from the dS^T image over the dP^T columns.
 #pragma unroll
@@ -311,8 +321,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     // ------------------------- row-math warpgroups --------------------------
     // Four warpgroups: rg = 0, 1 take the even query steps (TMEM buffer 0) and
     // rg = 2, 3 the odd ones (buffer 1); within a pair, warpgroup rg & 1 takes
-    // query columns [32 (rg & 1), 32 (rg & 1) + 32) of the step. Each works in
-    // halves of 16 columns (one MMA K step).
+    // query columns [32 (rg & 1), 32 (rg & 1) + 32) of the step, in halves of 16
+    // columns (one MMA K step). Each step runs in two phases: P~T from S^T
+    // (released to the dV MMA at once), then dS^T from dP^T and the kept fp32 P.
     const int rg = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int c = rg & 1;
@@ -346,92 +357,114 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       }
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
-      bool lo_any = false;
+      float P[32];          // P (before dropout) of this thread's 32 pairs, for the dS phase
+      bool split_h[2];
+      // ---- phase 1: P~T image over the S^T columns ----
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[16], dr[16];
-        __syncwarp();  // per-lane mask branches above: converge for the TMEM loads
+        uint32_t sr[16];
+        __syncwarp();  // per-lane branches above: converge for the TMEM load
         tmem_ld16(tSc + 16 * hh, sr);
-        tmem_ld16(tdPc + 16 * hh, dr);
-        tmem_ld_wait16x2(sr, dr);
+        tmem_ld_wait16(sr);
         float cmax = 0.f;
-        float pt[16], ds[16];
-        // P, dropout and dS for the 16 pairs; the unmasked variant skips the
-        // per-pair mask test on full tiles. L and D arrive negated, so
-        // P = exp2(S * scale*log2e + (-L*log2e)) and dS = P * (dP + (-D)); without
-        // dropout the FMA, add and multiply run on pairs of columns.
-        auto elementwise = [&](auto masked) {
+        float pt[16];
+        // P = exp2(S * scale*log2e + (-L*log2e)) on pairs of columns; the unmasked
+        // variant skips the per-pair mask test on full tiles.
+        auto p_phase = [&](auto masked) {
 #pragma unroll
           for (int x = 0; x < 16; x += 4) {
-            const float4 l4 = L4[(16 * hh + x) >> 2], d4 = D4[(16 * hh + x) >> 2];
-            if constexpr (!kDrop) {
-              const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
-              float pv[4];
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), c2, f2_pack(l4.x, l4.y)),
-                        pv[0], pv[1]);
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3])), c2,
-                               f2_pack(l4.z, l4.w)),
-                        pv[2], pv[3]);
+            const float4 l4 = L4[(16 * hh + x) >> 2];
+            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+            float pv[4];
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x]), __uint_as_float(sr[x + 1])), c2, f2_pack(l4.x, l4.y)),
+                      pv[0], pv[1]);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[x + 2]), __uint_as_float(sr[x + 3])), c2, f2_pack(l4.z, l4.w)),
+                      pv[2], pv[3]);
 #pragma unroll
-              for (int y = 0; y < 4; ++y) {
-                pv[y] = ex2_approx(pv[y]);
-                if constexpr (decltype(masked)::value) pv[y] = ((allow >> (16 * hh + x + y)) & 1u) ? pv[y] : 0.f;
+            for (int y = 0; y < 4; ++y) {
+              const int bit = 16 * hh + x + y;
+              pv[y] = ex2_approx(pv[y]);
+              if constexpr (decltype(masked)::value) pv[y] = ((allow >> bit) & 1u) ? pv[y] : 0.f;
+              P[bit] = pv[y];
+              if constexpr (kDrop)
+                pt[x + y] = ((keep >> bit) & 1u) ? pv[y] * p.drop.rp : 0.f;
+              else
                 pt[x + y] = pv[y];
-              }
-              cmax = fmax3(cmax, pv[0], pv[1]);
-              cmax = fmax3(cmax, pv[2], pv[3]);
-              const uint64_t d01 = f2_add(f2_pack(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), f2_pack(d4.x, d4.y));
-              const uint64_t d23 =
-                  f2_add(f2_pack(__uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3])), f2_pack(d4.z, d4.w));
-              f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), d01), ds[x], ds[x + 1]);
-              f2_unpack(f2_mul(f2_pack(pv[2], pv[3]), d23), ds[x + 2], ds[x + 3]);
-            } else {
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-              for (int y = 0; y < 4; ++y) {
-                const int bit = 16 * hh + x + y;
-                float pv = ex2_approx(fmaf(__uint_as_float(sr[x + y]), p.scale_log2, lv[y]));
-                if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
-                cmax = fmaxf(cmax, pv);
-                const bool kept = (keep >> bit) & 1u;
-                const float dpv = kept ? __uint_as_float(dr[x + y]) * p.drop.rp : 0.f;
-                ds[x + y] = pv * (dpv + dv[y]);
-                pt[x + y] = kept ? pv * p.drop.rp : 0.f;
-              }
             }
+            cmax = fmax3(cmax, pv[0], pv[1]);
+            cmax = fmax3(cmax, pv[2], pv[3]);
           }
         };
         if (allow == 0xFFFFFFFFu)
-          elementwise(std::false_type{});
+          p_phase(std::false_type{});
         else
-          elementwise(std::true_type{});
+          p_phase(std::true_type{});
         // The lanes may have split over the two variants: reconverge before the
         // warp-collective vote and TMEM stores below.
         __syncwarp();
-        uint32_t hp[8], hd[8], ep[8], ed[8];
+        uint32_t hp[8], ep[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          hp[x] = pack2<kBf16>(pt[2 * x], pt[2 * x + 1]);
-          hd[x] = pack2<kBf16>(ds[2 * x], ds[2 * x + 1]);
-        }
+        for (int x = 0; x < 8; ++x) hp[x] = pack2<kBf16>(pt[2 * x], pt[2 * x + 1]);
         // Residuals only where this warp's rows hold a probability above the
         // split threshold; zeros elsewhere keep the residual image well defined.
-        const bool split_h = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
-        lo_any |= split_h;
-        if (split_h) {
+        split_h[hh] = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        if (split_h[hh]) {
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            ep[x] = pack2_residual<kBf16>(pt[2 * x], pt[2 * x + 1], hp[x]);
-            ed[x] = pack2_residual<kBf16>(ds[2 * x], ds[2 * x + 1], hd[x]);
-          }
+          for (int x = 0; x < 8; ++x) ep[x] = pack2_residual<kBf16>(pt[2 * x], pt[2 * x + 1], hp[x]);
         } else {
 #pragma unroll
-          for (int x = 0; x < 8; ++x) ep[x] = ed[x] = 0u;
+          for (int x = 0; x < 8; ++x) ep[x] = 0u;
         }
-        // This K step's image: 8 rounded columns, then 8 residual columns, over the
-        // 16 S^T (and dP^T) columns just read.
+        // This K step's image: 8 rounded columns, then 8 residual columns.
         tmem_st8<0>(tSc + 16 * hh, hp);
         tmem_st8<0>(tSc + 16 * hh + 8, ep);
+      }
+      tmem_st_wait();
+      if (lane == 0) flags[8 * bb + 4 * c + wq] = (split_h[0] || split_h[1]) ? 1 : 0;
+      tc_fence_before();
+      warp_arrive(bar(C::bPFull + bb));
+      // ---- phase 2: dS^T = P o (dP^T (o Z/(1-p)) + (-D)) ----
+      if (!warp_wait<kRowMathPoll>(bar(C::bDPFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t dr[16];
+        tmem_ld16(tdPc + 16 * hh, dr);
+        tmem_ld_wait16(dr);
+        float ds[16];
+#pragma unroll
+        for (int x = 0; x < 16; x += 4) {
+          const float4 d4 = D4[(16 * hh + x) >> 2];
+          if constexpr (!kDrop) {
+            const uint64_t d01 =
+                f2_add(f2_pack(__uint_as_float(dr[x]), __uint_as_float(dr[x + 1])), f2_pack(d4.x, d4.y));
+            const uint64_t d23 =
+                f2_add(f2_pack(__uint_as_float(dr[x + 2]), __uint_as_float(dr[x + 3])), f2_pack(d4.z, d4.w));
+            f2_unpack(f2_mul(f2_pack(P[16 * hh + x], P[16 * hh + x + 1]), d01), ds[x], ds[x + 1]);
+            f2_unpack(f2_mul(f2_pack(P[16 * hh + x + 2], P[16 * hh + x + 3]), d23), ds[x + 2], ds[x + 3]);
+          } else {
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+              const int bit = 16 * hh + x + y;
+              const float dpv = ((keep >> bit) & 1u) ? __uint_as_float(dr[x + y]) * p.drop.rp : 0.f;
+              ds[x + y] = P[bit] * (dpv + dv[y]);
+            }
+          }
+        }
+        uint32_t hd[8], ed[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) hd[x] = pack2<kBf16>(ds[2 * x], ds[2 * x + 1]);
+        if (split_h[hh]) {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) ed[x] = pack2_residual<kBf16>(ds[2 * x], ds[2 * x + 1], hd[x]);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) ed[x] = 0u;
+        }
         if constexpr (!kAtomic) {
           tmem_st8<0>(tdPc + 16 * hh, hd);
           tmem_st8<0>(tdPc + 16 * hh + 8, ed);
@@ -445,11 +478,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
           }
         }
       }
-      tmem_st_wait();
-      if (lane == 0) flags[8 * bb + 4 * c + wq] = lo_any ? 1 : 0;
+      if constexpr (!kAtomic) tmem_st_wait();
       tc_fence_before();
       if constexpr (kAtomic) fence_proxy_async_smem();
-      warp_arrive(bar(C::bPFull + bb));
+      warp_arrive(bar(C::bDSFull + bb));
       if constexpr (kAtomic) {
         // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
         if (!warp_wait<kRowMathPoll>(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
