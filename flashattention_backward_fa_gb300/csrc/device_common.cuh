@@ -425,6 +425,17 @@ __device__ __forceinline__ void tmem_ld_wait16x3(uint32_t (&a)[16], uint32_t (&b
                :
                : "memory");
 }
+// Wait for four outstanding 16-column loads.
+__device__ __forceinline__ void tmem_ld_wait16x4(uint32_t (&a)[16], uint32_t (&b)[16], uint32_t (&c)[16],
+                                                 uint32_t (&d)[16]) {
+  tmem_ld_wait16x3(a, b, c);
+  asm volatile(""
+               : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3]), "+r"(d[4]), "+r"(d[5]), "+r"(d[6]), "+r"(d[7]),
+                 "+r"(d[8]), "+r"(d[9]), "+r"(d[10]), "+r"(d[11]), "+r"(d[12]), "+r"(d[13]), "+r"(d[14]),
+                 "+r"(d[15])
+               :
+               : "memory");
+}
 
 // Wait for outstanding tcgen05.ld; the registers are tied in so that no use of
 // them can be scheduled before the wait.
