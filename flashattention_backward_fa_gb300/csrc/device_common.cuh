@@ -91,6 +91,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // warps (which share schedulers with row-math warps) lengthens it by ~5%.
 constexpr bool kIssuerPoll = false;
 constexpr bool kRowMathPoll = true;
+// The warp that issues the MMAs consuming the row math's images (dV/dK, or the
+// dQ / O accumulation) waits on the row math: its own choice.
+constexpr bool kConsumerPoll = false;
 
 // Returns false (after setting the timeout status bit and *abort) when the
 // wall-clock limit passes or another role of the CTA has already aborted.

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1, st = t % C::kNS;
-        if (!warp_wait<kIssuerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kConsumerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         }
         tc_commit_w(bar(C::bSEmpty + bt));
         // dK (and dQ^T) once the dS^T image is in place; dV above only needed P~T.
-        if (!warp_wait<kIssuerPoll>(bar(C::bDSFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kConsumerPoll>(bar(C::bDSFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }

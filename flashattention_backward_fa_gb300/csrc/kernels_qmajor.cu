@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1;
-        if (!warp_wait<kIssuerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kConsumerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
