@@ -554,12 +554,33 @@ __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t b
   return sel >= dp.threshold;
 }
 
-// Keep bits (bit x <-> query i0 + x) of n <= 32 consecutive queries for one key j.
-static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j,
-                                                          int n = 32) {
-  uint32_t bits = 0;
+// Keep bits (bit x <-> query i0 + x) of 32 consecutive queries for this lane's
+// key j, computed by the whole (converged) warp, whose lanes hold 32
+// consecutive keys with j % 4 == lane % 4. One Philox call yields the words of
+// four keys (one 4-lane group) for one query, so lane 4g + r evaluates the
+// queries i0 + 4t + r (t < 8) for its group and the four lanes trade their
+// results through shuffles: 8 calls per lane instead of 32.
+static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
+  const int lane = threadIdx.x & 31, r = lane & 3;
+  const uint64_t n4 = (uint64_t)((N + 3) >> 2);
+  const uint64_t row0 = (uint64_t)bh * (uint64_t)N;
+  uint32_t mine = 0;  // nibble t: keep bits of the group's four keys for query i0 + 4t + r
 #pragma unroll 1
-  for (int x = 0; x < n; ++x) bits |= (uint32_t)dropout_keep(dp, bh, N, i0 + x, j) << x;
+  for (int t = 0; t < 8; ++t) {
+    const uint64_t g = (row0 + (uint64_t)(i0 + 4 * t + r)) * n4 + (uint64_t)(j >> 2);
+    const uint4 w =
+        philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi), dp.seed_lo, dp.seed_hi);
+    const uint32_t nib = (uint32_t)(w.x >= dp.threshold) | ((uint32_t)(w.y >= dp.threshold) << 1) |
+                         ((uint32_t)(w.z >= dp.threshold) << 2) | ((uint32_t)(w.w >= dp.threshold) << 3);
+    mine |= nib << (4 * t);
+  }
+  uint32_t bits = 0;
+#pragma unroll
+  for (int rs = 0; rs < 4; ++rs) {
+    const uint32_t v = __shfl_sync(0xffffffffu, mine, (lane & ~3) + rs);  // queries i0 + 4t + rs
+#pragma unroll
+    for (int t = 0; t < 8; ++t) bits |= ((v >> (4 * t + r)) & 1u) << (4 * t + rs);
+  }
   return bits;
 }
 

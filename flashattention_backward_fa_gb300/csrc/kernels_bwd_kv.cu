@@ -356,7 +356,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         allow = bit_range(lo, hi);
       }
       uint32_t keep = 0xFFFFFFFFu;
-      if constexpr (kDrop) keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
+      if constexpr (kDrop) {
+        __syncwarp();  // warp-collective (shuffles)
+        keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
+      }
       float P[32];          // P (before dropout) of this thread's 32 pairs, for the dS phase
       bool split_h[2];
       // ---- phase 1: P~T image over the S^T columns ----
