@@ -231,7 +231,20 @@ def time_ours(w, steps, warmup, deterministic, world):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+    # The forward that produced O and L (support for the backward; not in `value`),
+    # for the forward / backward speed ratio.
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    for _ in range(2):
+        fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = f0.elapsed_time(f1) / e2e_steps
+    return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, fwd_ms=fwd_ms)
 
 
 def time_oracle(w, max_seconds=20.0):
@@ -332,6 +345,9 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": 3 * a.steps,
+        # forward: 4*d FLOP per allowed pair (QK^T and PV), the usual forward count
+        "forward": {"ms": r["fwd_ms"], "tflops": 0.4 * flops / (r["fwd_ms"] * 1e-3) / 1e12,
+                    "bwd_over_fwd_speed": (flops / (r["ms"] * 1e-3)) / (0.4 * flops / (r["fwd_ms"] * 1e-3))},
         "clocks": r["clocks"],
     }
     if rank == 0 and not a.no_cpu_baseline:

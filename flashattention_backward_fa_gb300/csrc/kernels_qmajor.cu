@@ -52,14 +52,16 @@ struct QCfg {
   static constexpr uint32_t kPanel = 128 * 128;                // 16 KB: 128 rows x 64 elements
   static constexpr uint32_t kTile = kPanels * kPanel;          // one 128-row tile of Q, dO, K or V
   static constexpr uint32_t kResident = (kDq ? 2 : 1) * kTile;
-  static constexpr uint32_t kStats = kDq ? 0 : 4 * 2 * kRowsQ * 4;
+  // forward: per-step chunk maxima [2 steps][4 warpgroups][rows], then the
+  // final partial sums [4 warpgroups][rows]
+  static constexpr uint32_t kStats = kDq ? 0 : (2 * 4 + 4) * kRowsQ * 4;
   static constexpr int kNE = kDq ? 2 : (D == 64 ? 4 : 3);      // ring E stages
   static constexpr int kNL = kDq ? (D == 64 ? 4 : 3) : 2;      // ring L stages
   static constexpr uint32_t oQ = 0;
   static constexpr uint32_t oDO = oQ + kTile;
   static constexpr uint32_t oE = kResident;
   static constexpr uint32_t oL = oE + kNE * kTile;
-  static constexpr uint32_t oStats = oL + kNL * kTile;         // forward: [warpgroup][m | l][row]
+  static constexpr uint32_t oStats = oL + kNL * kTile;         // forward: row-statistics exchange
   static constexpr uint32_t oBar = oStats + kStats;
   static constexpr int bRes = 0;
   static constexpr int bEFull = 1;
@@ -72,14 +74,20 @@ struct QCfg {
   static constexpr int bPFull = bDPEmpty + 1;                  // [2]: image written
   static constexpr int bAcc = bPFull + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
-  static constexpr int bStats = bDrain + 3;
-  static constexpr int kBars = bStats + 1;
+  static constexpr int bStats = bDrain + 3;                    // forward: final sums exchanged
+  static constexpr int bXchg = bStats + 1;                     // [2] forward: chunk maxima of step it exchanged
+  static constexpr int bODone = bXchg + 2;                     // forward: O MMA of a step done
+  static constexpr int kBars = bODone + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = (oAbort + 8 + 15) & ~15u;  // [buffer][16 warps] split votes
   static constexpr uint32_t kSmem = oFlags + 2 * 16 * 4 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
+
+// Forward: the reference maximum of a row moves only when the row maximum grows by
+// more than this (log2 units), bounding relative probabilities by 2^8.
+constexpr float kRescaleLog2 = 8.f;
 
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
@@ -112,9 +120,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int j_last = p.causal ? min(p.N - 1, i0 + kRowsQ - 1) : p.N - 1;
   const int j_first = p.window > 0 ? (max(0, i0 - p.window + 1) / kStepKV) * kStepKV : 0;
   const int nkv = (j_last >= j_first) ? (j_last - j_first) / kStepKV + 1 : 0;
-  // Forward: nkv statistics steps, then nkv output steps. dQ: nkv steps.
-  const int nsteps = kDq ? nkv : 2 * nkv;
-  const int first_out = kDq ? 0 : nkv;
+  // One pass over the key blocks in both modes.
+  const int nsteps = nkv;
+  const int first_out = 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bRes), 1);
@@ -135,6 +143,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(bar(C::bAcc), 1);
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bStats), 512);
+    mbar_init(bar(C::bXchg), 512);
+    mbar_init(bar(C::bXchg + 1), 512);
+    mbar_init(bar(C::bODone), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -298,6 +309,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
           tc_commit_w(bar(C::bSEmpty + bt));
           tc_commit_w(bar(C::bLEmpty + sl));
+          if (!kDq) tc_commit_w(bar(C::bODone));
         } else {
           tc_commit_w(bar(C::bSEmpty + bt));
         }
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else if (warp >= 4) {
     // ---------------- row-math warpgroups + epilogue ----------------------
     // Warpgroup c takes key columns [32c, 32c + 32) of every step, in halves of
-    // 16 columns (one MMA K step).
+    // 16 columns (one MMA K step), and a quarter of the epilogue columns.
     const int c = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int il = wq * 32 + lane;
@@ -319,45 +331,22 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tdPc = tdP + lane_off + 32 * c;
     const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
-    // -L*log2(e) (-inf for a row with no allowed key) and -D: the negated forms
-    // are addends of one FMA / add (packed two-wide below).
+    // dQ: -L*log2(e) (-inf for a row with no allowed key) and -D, read; the
+    // negated forms are addends of one FMA / add (packed two-wide below).
+    // Forward: mref, the running reference maximum of S*scale*log2e over the
+    // keys seen so far (log2 domain), shared by the four warpgroups, and lsum,
+    // this warpgroup's sum of exp2(S*scale*log2e - mref) over its columns.
     float nL2 = -INFINITY, nD = 0.f;
     if (kDq) {
       nL2 = p.ws_nL2[ws];
       nD = p.ws_nD[ws];
     }
-    float m = -INFINITY, l = 0.f;  // forward statistics of this warpgroup's columns, log2 domain
-    bool merged = kDq;
+    float mref = -INFINITY, lsum = 0.f;
+    float* xchg = reinterpret_cast<float*>(smem + C::oStats);
     bool ok = true;
-    // Forward: merge the four warpgroups' partial row statistics into L (log2 domain).
-    auto merge_stats = [&]() -> bool {
-      float* st = reinterpret_cast<float*>(smem + C::oStats);
-      st[(2 * c) * kRowsQ + il] = m;
-      st[(2 * c + 1) * kRowsQ + il] = l;
-      warp_arrive(bar(C::bStats));
-      if (!warp_wait<kRowMathPoll>(bar(C::bStats), 0, abort_flag, p.status)) return false;
-      float mm = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) mm = fmaxf(mm, st[(2 * g) * kRowsQ + il]);
-      float ll = 0.f;
-      if (mm != -INFINITY) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) ll += st[(2 * g + 1) * kRowsQ + il] * ex2_approx(st[(2 * g) * kRowsQ + il] - mm);
-      }
-      nL2 = (ll > 0.f) ? -(mm + lg2_approx(ll)) : -INFINITY;
-      return true;
-    };
     for (int it = 0; it < nsteps; ++it) {
       const int bb = it & 1;
-      const int jt = it >= nkv ? it - nkv : it;
-      const int base = j_first + jt * kStepKV + 32 * c;
-      if (!kDq && it >= first_out && !merged) {
-        if (!merge_stats()) {
-          ok = false;
-          break;
-        }
-        merged = true;
-      }
+      const int base = j_first + it * kStepKV + 32 * c;
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
       if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
@@ -367,61 +356,62 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // allowed keys of this warpgroup's 32 columns (bit x <-> key base + x)
       const uint32_t allow =
           bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
-      if (!kDq && it < first_out) {
-        // statistics step
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sr[16];
-          __syncwarp();  // the statistics update branches per lane: converge for the TMEM load
-          tmem_ld16(tSc + 16 * hh, sr);
-          tmem_ld_wait16(sr);
-          float x[16];
-          float mx = m;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            x[e] = ((allow >> (16 * hh + e)) & 1u) ? __uint_as_float(sr[e]) * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, x[e]);
-          }
-          if (mx != -INFINITY) {
-            float acc = l * ex2_approx(m - mx);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc += ex2_approx(x[e] - mx);
-            l = acc;
-            m = mx;
-          }
-        }
-        tc_fence_before();
-        warp_arrive(bar(C::bPFull + bb));
-        continue;
-      }
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
-      bool lo_any = false;
-      // dQ: both halves of this warpgroup's dP columns come in with the first S
-      // half, so the dP buffer is released (and the next dP MMAs may run) before
-      // any of the step's arithmetic.
-      uint32_t dr2[2][16];
-      uint32_t sr[16];
-      tmem_ld16(tSc, sr);
+      // dQ: both halves of this warpgroup's dP columns come in with S, so the dP
+      // buffer is released (and the next dP MMAs may run) before any arithmetic.
+      // Forward: all of S comes in, for the row maximum.
+      uint32_t sr2[2][16], dr2[2][16];
+      __syncwarp();
+      tmem_ld16(tSc, sr2[0]);
+      tmem_ld16(tSc + 16, sr2[1]);
       if constexpr (kDq) {
         tmem_ld16(tdPc, dr2[0]);
         tmem_ld16(tdPc + 16, dr2[1]);
-        tmem_ld_wait16x3(sr, dr2[0], dr2[1]);
+        tmem_ld_wait16x4(sr2[0], sr2[1], dr2[0], dr2[1]);
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty));
       } else {
-        tmem_ld_wait16(sr);
+        tmem_ld_wait16x2(sr2[0], sr2[1]);
       }
+      bool resc = false;
+      float alpha = 1.f;
+      if constexpr (!kDq) {
+        // Online softmax: the maximum of this step's 128 columns of the row,
+        // from the four warpgroups' chunk maxima exchanged through shared memory.
+        float cm = -INFINITY;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if ((allow >> (16 * hh + e)) & 1u) cm = fmaxf(cm, __uint_as_float(sr2[hh][e]) * p.scale_log2);
+        xchg[(bb * 4 + c) * kRowsQ + il] = cm;
+        warp_arrive(bar(C::bXchg + bb));
+        if (!warp_wait<kRowMathPoll>(bar(C::bXchg + bb), (it >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        float mstep = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) mstep = fmaxf(mstep, xchg[(bb * 4 + g) * kRowsQ + il]);
+        // The reference moves only when the maximum grows by more than 2^8 (or
+        // the row sees its first allowed key): probabilities relative to a stale
+        // reference stay below 2^8, and the O accumulator is rescaled rarely.
+        if (mstep > mref + kRescaleLog2) {
+          resc = mref != -INFINITY;
+          alpha = resc ? ex2_approx(mref - mstep) : 1.f;
+          lsum *= alpha;
+          mref = mstep;
+        }
+        nL2 = -mref;  // P = exp2(S*scale*log2e + (-mref)); +inf only where every key so far is masked
+      }
+      bool lo_any = false;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        if (hh == 1) {
-          __syncwarp();
-          tmem_ld16(tSc + 16, sr);
-          tmem_ld_wait16(sr);
-        }
+        const uint32_t (&sr)[16] = sr2[hh];
         const uint32_t (&dr)[16] = dr2[hh];
         float outv[16];
-        float cmax = 0.f;
+        float cmax = 0.f, psum = 0.f;
         auto elementwise = [&](auto masked) {
           if constexpr (!kDrop) {
             // pairs of columns through the packed FMA / add / multiply
@@ -441,6 +431,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 const uint64_t dd = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(nD, nD));
                 f2_unpack(f2_mul(f2_pack(p0, p1), dd), outv[e], outv[e + 1]);
               } else {
+                psum += p0 + p1;
                 outv[e] = p0;
                 outv[e + 1] = p1;
               }
@@ -457,6 +448,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 const float dpv = kept ? __uint_as_float(dr[e]) * p.drop.rp : 0.f;
                 outv[e] = pv * (dpv + nD);
               } else {
+                psum += pv;
                 outv[e] = kept ? pv * p.drop.rp : 0.f;
               }
             }
@@ -470,9 +462,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // The lanes may have split over the two variants: reconverge before the
         // warp-collective vote and TMEM stores below.
         __syncwarp();
+        if constexpr (!kDq) lsum += psum;
         uint32_t hv[8], ev[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
+        // Residuals where the (relative) probability exceeds the split threshold;
+        // in the forward the probabilities are relative to mref, which keeps the
+        // test conservative.
         const bool split_h = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
         lo_any |= split_h;
         if (split_h) {
@@ -486,6 +482,27 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_st8<0>(tSc + 16 * hh, hv);
         tmem_st8<0>(tSc + 16 * hh + 8, ev);
       }
+      if constexpr (!kDq) {
+        // Rescale this warpgroup's quarter of the O columns of rows whose
+        // reference moved, once the O MMA of the previous step has finished.
+        if (__any_sync(0xFFFFFFFFu, resc)) {
+          if (it > 0 && !warp_wait<kRowMathPoll>(bar(C::bODone), (it - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) {
+            const uint32_t ta = tAcc + lane_off + c * (D / 4) + 16 * cc;
+            uint32_t r[16];
+            tmem_ld16(ta, r);
+            tmem_ld_wait16(r);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+            tmem_st16(ta, r);
+          }
+        }
+      }
       tmem_st_wait();
       // Step it - 2 used these vote slots; its accumulating MMAs were issued
       // (the votes read) before S(it) could land in this buffer.
@@ -493,18 +510,29 @@ __global__ void __launch_bounds__(kQThreads, 1)
       tc_fence_before();
       warp_arrive(bar(C::bPFull + bb));
     }
-    if (!kDq && ok && !merged) {
-      // No output step (empty key range): still publish the statistics.
-      ok = merge_stats();
+    float scale_out = kDq ? p.scale : 1.f;  // forward: 1 / (row sum), below
+    float lse_row = -INFINITY;
+    if constexpr (!kDq) {
+      if (ok) {
+        // The row sum over the four warpgroups' columns.
+        float* xl = xchg + 8 * kRowsQ;
+        xl[c * kRowsQ + il] = lsum;
+        warp_arrive(bar(C::bStats));
+        ok = warp_wait<kRowMathPoll>(bar(C::bStats), 0, abort_flag, p.status);
+        float ltot = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) ltot += xl[g * kRowsQ + il];
+        scale_out = ltot > 0.f ? 1.f / ltot : 0.f;
+        lse_row = ltot > 0.f ? (mref + lg2_approx(ltot)) * 0.6931471805599453f : -INFINITY;
+      }
     }
     // Epilogue: O (forward) or scale * dQ; warpgroup c writes columns [c*d/4, (c+1)*d/4).
-    const bool have_acc = nsteps > first_out;
+    const bool have_acc = nsteps > 0;
     if (ok && have_acc) ok = warp_wait<kRowMathPoll>(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
       const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
       uint16_t* dst = static_cast<uint16_t*>(p.out) + off;
-      const float mul = kDq ? p.scale : 1.f;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int col = c * (D / 4) + 16 * cc;
@@ -519,15 +547,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         uint32_t w[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x)
-          w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
+          w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * scale_out, __uint_as_float(r[2 * x + 1]) * scale_out);
         if (i < p.N) {
           uint4* g = reinterpret_cast<uint4*>(dst + col);
           g[0] = make_uint4(w[0], w[1], w[2], w[3]);
           g[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      if (!kDq && c == 0 && i < p.N)
-        p.lse_out[(long long)bh * p.N + i] = (nL2 == -INFINITY) ? -INFINITY : -nL2 * 0.6931471805599453f;
+      if (!kDq && c == 0 && i < p.N) p.lse_out[(long long)bh * p.N + i] = lse_row;
     }
   }
 
