@@ -9,10 +9,15 @@
 // The reduction order over key blocks is fixed, so dQ is bit-reproducible.
 //
 // Forward ("FlashAttention backward", §What the forward left behind): the
-// output O and the per-row log-sum-exp L = m + log(l) (natural log). It runs
-// two passes over the key blocks: the first keeps the running row maximum and
-// sum of exponentials, the second forms P = exp(S - L) with L already known —
-// so O never needs rescaling — and accumulates O += (P o Z/(1-p)) V.
+// output O and the per-row log-sum-exp L = m + log(l) (natural log), in one
+// pass with an online softmax. Per key block the four row-math warpgroups
+// exchange their chunk maxima of each row through shared memory; a row's
+// reference maximum moves only when the maximum grows by more than 2^8 (so the
+// probabilities relative to it stay below 2^8), and then the O accumulator's
+// row is rescaled in TMEM once the previous O MMA has finished. Each warpgroup
+// keeps its columns' partial sum l relative to the reference; at the end
+// O = acc / l and L = (reference + log2 l) * ln 2. Dropout: O += (P o Z/(1-p)) V,
+// with l taken before dropout.
 //
 // Queries sit on the 128 TMEM lanes: one thread owns one query row, so L_i and
 // D_i are per-thread scalars. Row-math warps wait warp-wide (warp_wait) and
@@ -22,8 +27,9 @@
 // operand reads to about two thirds of the tensor rate). The row math writes
 // dS (or P~) back over the S columns it has read, rounded to 16 bits with the
 // rounding residual beside it (see interleave_split), and the accumulating MMA
-// reads it from TMEM. S alternates between two TMEM buffers; dP has one, which
-// the row math releases as soon as it has read it.
+// reads it from TMEM. In the dQ kernel S alternates between two TMEM buffers
+// and dP has one, which the row math releases as soon as it has read it; the
+// forward, with no dP, rotates S over three buffers.
 //
 // Shared memory holds Q (and dO) for the whole kernel and two rings of key
 // tiles: ring E for the tile only the first MMAs read (V for dP; K in the
@@ -35,8 +41,8 @@
 // parallel. Four row-math warpgroups (warps 4-19) each take 32 of the step's
 // 128 key columns and a quarter of the epilogue columns.
 //
-// TMEM columns: [0,256) two S buffers, [256,384) the dP buffer (dQ mode),
-// [384,384+d) the O or dQ accumulator.
+// TMEM columns: dQ kernel [0,256) two S buffers, [256,384) the dP buffer;
+// forward [0,384) three S buffers; then [384,384+d) the dQ or O accumulator.
 #include "fa_internal.h"
 
 namespace fa {
@@ -57,6 +63,9 @@ struct QCfg {
   static constexpr uint32_t kStats = kDq ? 0 : (2 * 4 + 4) * kRowsQ * 4;
   static constexpr int kNE = kDq ? 2 : (D == 64 ? 4 : 3);      // ring E stages
   static constexpr int kNL = kDq ? (D == 64 ? 4 : 3) : 2;      // ring L stages
+  // S buffers in TMEM: two beside the dP buffer in the dQ kernel; three in the
+  // forward, which has no dP.
+  static constexpr int kSBuf = kDq ? 2 : 3;
   static constexpr uint32_t oQ = 0;
   static constexpr uint32_t oDO = oQ + kTile;
   static constexpr uint32_t oE = kResident;
@@ -68,11 +77,11 @@ struct QCfg {
   static constexpr int bEEmpty = bEFull + kNE;
   static constexpr int bLFull = bEEmpty + kNE;
   static constexpr int bLEmpty = bLFull + kNL;
-  static constexpr int bSFull = bLEmpty + kNL;                 // [2]: S (and dP) landed
-  static constexpr int bSEmpty = bSFull + 2;                   // [2]: accumulating MMA done with the image
-  static constexpr int bDPEmpty = bSEmpty + 2;                 // row math has read dP
-  static constexpr int bPFull = bDPEmpty + 1;                  // [2]: image written
-  static constexpr int bAcc = bPFull + 2;
+  static constexpr int bSFull = bLEmpty + kNL;                 // [kSBuf]: S (and dP) landed
+  static constexpr int bSEmpty = bSFull + kSBuf;               // [kSBuf]: accumulating MMA done with the image
+  static constexpr int bDPEmpty = bSEmpty + kSBuf;             // row math has read dP
+  static constexpr int bPFull = bDPEmpty + 1;                  // [kSBuf]: image written
+  static constexpr int bAcc = bPFull + kSBuf;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
   static constexpr int bStats = bDrain + 3;                    // forward: final sums exchanged
   static constexpr int bXchg = bStats + 1;                     // [2] forward: chunk maxima of step it exchanged
@@ -81,7 +90,7 @@ struct QCfg {
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = (oAbort + 8 + 15) & ~15u;  // [buffer][16 warps] split votes
-  static constexpr uint32_t kSmem = oFlags + 2 * 16 * 4 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t kSmem = oFlags + kSBuf * 16 * 4 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
 
@@ -134,7 +143,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(bar(C::bLFull + s), 1);
       mbar_init(bar(C::bLEmpty + s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < C::kSBuf; ++x) {
       mbar_init(bar(C::bSFull + x), kDq ? 2 : 1);
       mbar_init(bar(C::bSEmpty + x), 1);
       mbar_init(bar(C::bPFull + x), 512);
@@ -217,12 +226,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t dK0 = make_sdesc(sb + (kDq ? C::oL : C::oE), 16, 1024);
       bool ok = warp_wait<kIssuerPoll>(bar(C::bRes), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int bb = it & 1;
+        const int bb = it % C::kSBuf;
         // K lives in ring L (dQ; one tile per step) or ring E (forward)
         const int ks = kDq ? it % C::kNL : it % C::kNE;
         const uint32_t kpar = kDq ? (it / C::kNL) & 1 : (it / C::kNE) & 1;
         if (!warp_wait<kIssuerPoll>(bar((kDq ? C::bLFull : C::bEFull) + ks), kpar, abort_flag, p.status) ||
-            !warp_wait<kIssuerPoll>(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
+            !warp_wait<kIssuerPoll>(bar(C::bSEmpty + bb), ((it / C::kSBuf) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ss_w(tdP, desc_add(dO0, (k >> 2) * C::kPanel + (k & 3) * 32),
                       desc_add(vd, (k >> 2) * C::kPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit_w(bar(C::bSFull + (it & 1)));
+        tc_commit_w(bar(C::bSFull + it % C::kSBuf));
         tc_commit_w(bar(C::bEEmpty + se));
       }
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
@@ -276,8 +285,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t b0 = make_sdesc(sb + C::oL, C::kPanel, 1024);
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
-        const int bt = t & 1;
-        if (!warp_wait<kConsumerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        const int bt = t % C::kSBuf;
+        if (!warp_wait<kConsumerPoll>(bar(C::bPFull + bt), (t / C::kSBuf) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -345,10 +354,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     float* xchg = reinterpret_cast<float*>(smem + C::oStats);
     bool ok = true;
     for (int it = 0; it < nsteps; ++it) {
-      const int bb = it & 1;
+      const int bb = it % C::kSBuf, xb = it & 1;
       const int base = j_first + it * kStepKV + 32 * c;
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
-      if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+      if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it / C::kSBuf) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -361,17 +370,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // dQ: both halves of this warpgroup's dP columns come in with S, so the dP
       // buffer is released (and the next dP MMAs may run) before any arithmetic.
       // Forward: all of S comes in, for the row maximum.
+      // (dQ: the second S half comes in after the first half's arithmetic,
+      // which keeps fewer registers live.)
       uint32_t sr2[2][16], dr2[2][16];
       __syncwarp();
       tmem_ld16(tSc, sr2[0]);
-      tmem_ld16(tSc + 16, sr2[1]);
       if constexpr (kDq) {
         tmem_ld16(tdPc, dr2[0]);
         tmem_ld16(tdPc + 16, dr2[1]);
-        tmem_ld_wait16x4(sr2[0], sr2[1], dr2[0], dr2[1]);
+        tmem_ld_wait16x3(sr2[0], dr2[0], dr2[1]);
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty));
       } else {
+        tmem_ld16(tSc + 16, sr2[1]);
         tmem_ld_wait16x2(sr2[0], sr2[1]);
       }
       bool resc = false;
@@ -379,21 +390,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if constexpr (!kDq) {
         // Online softmax: the maximum of this step's 128 columns of the row,
         // from the four warpgroups' chunk maxima exchanged through shared memory.
+        // (Full tiles with a positive scale take the maximum on S and scale it
+        // once, without the per-column mask.)
         float cm = -INFINITY;
+        if (allow == 0xFFFFFFFFu && p.scale_log2 > 0.f) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
+          for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if ((allow >> (16 * hh + e)) & 1u) cm = fmaxf(cm, __uint_as_float(sr2[hh][e]) * p.scale_log2);
-        xchg[(bb * 4 + c) * kRowsQ + il] = cm;
-        warp_arrive(bar(C::bXchg + bb));
-        if (!warp_wait<kRowMathPoll>(bar(C::bXchg + bb), (it >> 1) & 1, abort_flag, p.status)) {
+            for (int e = 0; e < 16; e += 2)
+              cm = fmax3(cm, __uint_as_float(sr2[hh][e]), __uint_as_float(sr2[hh][e + 1]));
+          cm = cm * p.scale_log2;
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              cm = ((allow >> (16 * hh + e)) & 1u) ? fmaxf(cm, __uint_as_float(sr2[hh][e]) * p.scale_log2) : cm;
+        }
+        xchg[(xb * 4 + c) * kRowsQ + il] = cm;
+        warp_arrive(bar(C::bXchg + xb));
+        if (!warp_wait<kRowMathPoll>(bar(C::bXchg + xb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         float mstep = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) mstep = fmaxf(mstep, xchg[(bb * 4 + g) * kRowsQ + il]);
+        for (int g = 0; g < 4; ++g) mstep = fmaxf(mstep, xchg[(xb * 4 + g) * kRowsQ + il]);
         // The reference moves only when the maximum grows by more than 2^8 (or
         // the row sees its first allowed key): probabilities relative to a stale
         // reference stay below 2^8, and the O accumulator is rescaled rarely.
@@ -408,10 +430,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
       bool lo_any = false;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        if (kDq && hh == 1) {
+          __syncwarp();
+          tmem_ld16(tSc + 16, sr2[1]);
+          tmem_ld_wait16(sr2[1]);
+        }
         const uint32_t (&sr)[16] = sr2[hh];
         const uint32_t (&dr)[16] = dr2[hh];
         float outv[16];
         float cmax = 0.f, psum = 0.f;
+        uint64_t psum2 = f2_pack(0.f, 0.f);
         auto elementwise = [&](auto masked) {
           if constexpr (!kDrop) {
             // pairs of columns through the packed FMA / add / multiply
@@ -431,7 +459,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 const uint64_t dd = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(nD, nD));
                 f2_unpack(f2_mul(f2_pack(p0, p1), dd), outv[e], outv[e + 1]);
               } else {
-                psum += p0 + p1;
+                psum2 = f2_add(psum2, f2_pack(p0, p1));
                 outv[e] = p0;
                 outv[e + 1] = p1;
               }
@@ -462,7 +490,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // The lanes may have split over the two variants: reconverge before the
         // warp-collective vote and TMEM stores below.
         __syncwarp();
-        if constexpr (!kDq) lsum += psum;
+        if constexpr (!kDq) {
+          float s0, s1;
+          f2_unpack(psum2, s0, s1);
+          lsum += psum + (s0 + s1);
+        }
         uint32_t hv[8], ev[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
@@ -504,7 +536,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
       tmem_st_wait();
-      // Step it - 2 used these vote slots; its accumulating MMAs were issued
+      // Step it - kSBuf used these vote slots; its accumulating MMAs were issued
       // (the votes read) before S(it) could land in this buffer.
       if (lane == 0) flags[16 * bb + 4 * c + wq] = lo_any ? 1 : 0;
       tc_fence_before();
