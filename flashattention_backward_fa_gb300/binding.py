@@ -65,6 +65,13 @@ def load_library(path: str = LIB_PATH):
     lib.fa_get_device_status.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp]
     lib.fa_bwd_noalloc.restype = i
+    i64 = ctypes.c_int64
+    lib.fa_varlen_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.fa_varlen_bwd_workspace_size.restype = sz
+    lib.fa_varlen_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, i64, i64, i, f, i, i, vp]
+    lib.fa_varlen_fwd.restype = i
+    lib.fa_varlen_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i64, i64, i, f, i, i, i, vp, sz, vp]
+    lib.fa_varlen_bwd.restype = i
     _lib = lib
     return lib
 
@@ -209,6 +216,77 @@ def attention_backward(q, k, v, o, do, lse, scale=None, causal=False, window=0, 
         workspace = alloc_workspace(q, deterministic)
     fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, window, dropout_p, seed, offset,
            deterministic)
+    return dq, dk, dv
+
+
+# ----------------------- packed variable-length input -----------------------
+def _varlen_layout(ref: torch.Tensor, cu_seqlens: torch.Tensor, *others: torch.Tensor):
+    """Checks packed [total, H, d] tensors and the int32 cu_seqlens; returns (total, H, d, sn, sh, nseq)."""
+    if ref.dim() != 3 or not ref.is_cuda or ref.stride(2) != 1:
+        raise ValueError("packed tensors are CUDA [total, H, d] with a contiguous head dimension")
+    for o in others:
+        if tuple(o.shape) != tuple(ref.shape) or o.stride() != ref.stride() or o.dtype != ref.dtype:
+            raise ValueError("all packed tensors must share shape, strides and dtype")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda \
+            or not cu_seqlens.is_contiguous() or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor of nseq + 1 offsets")
+    total, H, d = ref.shape
+    return total, H, d, ref.stride(0), ref.stride(1), cu_seqlens.numel() - 1
+
+
+def _varlen_lse_check(lse, H, total):
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (H, total) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total] tensor")
+
+
+def fa_varlen_bwd_workspace_size(nseq: int, max_seqlen: int, total: int, H: int, d: int, dtype,
+                                 deterministic: bool = True) -> int:
+    code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().fa_varlen_bwd_workspace_size(nseq, max_seqlen, total, H, d, code,
+                                                           int(bool(deterministic))))
+
+
+def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0, stream=None):
+    """Forward over packed sequences: fills o ([total, H, d]) and lse ([H, total] fp32)."""
+    total, H, d, sn, sh, nseq = _varlen_layout(q, cu_seqlens, k, v, o)
+    _varlen_lse_check(lse, H, total)
+    _check(load_library().fa_varlen_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), cu_seqlens.data_ptr(), nseq,
+        int(max_seqlen), total, H, d, sn, sh, _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else
+        float(scale), int(causal), int(window), _stream(stream)))
+
+
+def fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, workspace, scale=None, causal=False,
+                  window=0, deterministic=True, stream=None):
+    """Backward over packed sequences: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor."""
+    total, H, d, sn, sh, nseq = _varlen_layout(q, cu_seqlens, k, v, o, do, dq, dk, dv)
+    _varlen_lse_check(lse, H, total)
+    _check(load_library().fa_varlen_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+        dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(), nseq, int(max_seqlen), total, H, d, sn, sh,
+        _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
+        int(bool(deterministic)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def varlen_attention_forward(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, window=0):
+    """Allocate O and L and run the packed forward; returns (o, lse)."""
+    total, H, _ = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale, causal, window)
+    return o, lse
+
+
+def varlen_attention_backward(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0,
+                              deterministic=True):
+    """Allocate dQ, dK, dV and the workspace and run the packed backward."""
+    total, H, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = fa_varlen_bwd_workspace_size(cu_seqlens.numel() - 1, max_seqlen, total, H, d, q.dtype, deterministic)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, ws, scale, causal, window,
+                  deterministic)
     return dq, dk, dv
 
 

@@ -142,6 +142,28 @@ void fill_params(AttnParams& p, int B, int H, int N, int d, fa_strides s, float 
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// Launches one backward stage for fully validated and filled parameters.
+int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (stage == FA_BWD_PREPROCESS) return cuda_rc(fa::launch_preprocess(p, dtype, st));
+  if (dtype == FA_F32)
+    return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
+  const bool bf16 = dtype == FA_BF16;
+  if (stage == FA_BWD_DKDV) {
+    CUtensorMap maps[4];
+    if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
+        !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
+      return FA_ERR_CUDA;
+    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
+  }
+  if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], p.k, p, bf16, fa::kStepKV) ||
+      !make_map(&maps[2], p.v, p, bf16, fa::kStepKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kRowsQ))
+    return FA_ERR_CUDA;
+  return cuda_rc(fa::launch_qmajor_tc(p, bf16, true, maps, st));
+}
+
 // A second stream per device on which the deterministic backward runs its dQ
 // kernel beside the dK/dV kernel (fork after the preprocess, join before
 // returning), so that the two grids share the tail of each other's last wave
@@ -252,24 +274,7 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
   p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
   if ((rc = status_ptr(&p.status))) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stage == FA_BWD_PREPROCESS) return cuda_rc(fa::launch_preprocess(p, dtype, st));
-  if (dtype == FA_F32)
-    return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
-  const bool bf16 = dtype == FA_BF16;
-  if (stage == FA_BWD_DKDV) {
-    CUtensorMap maps[4];
-    if (!make_map(&maps[0], q, p, bf16, fa::kStepQ) || !make_map(&maps[1], k, p, bf16, fa::kRowsKV) ||
-        !make_map(&maps[2], v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], dout, p, bf16, fa::kStepQ))
-      return FA_ERR_CUDA;
-    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
-  }
-  if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
-  CUtensorMap maps[4];
-  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
-      !make_map(&maps[2], v, p, bf16, fa::kStepKV) || !make_map(&maps[3], dout, p, bf16, fa::kRowsQ))
-    return FA_ERR_CUDA;
-  return cuda_rc(fa::launch_qmajor_tc(p, bf16, true, maps, st));
+  return launch_stage(stage, p, dtype, deterministic, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -293,16 +298,12 @@ int fa_get_device_status(unsigned int* status, int clear) {
 
 }  // extern "C"
 
-namespace fa {
+namespace {
 
-int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
-            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream) {
-  auto stage = [&](fa_bwd_stage_id s, void* st) {
-    return fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                        dropout_p, seed, offset, deterministic, workspace, workspace_bytes, st);
-  };
+// The three stages in order; the deterministic 16-bit backward forks its dQ
+// kernel onto the side stream (see SideStream).
+template <typename StageFn>
+int run_backward(StageFn stage, int deterministic, int dtype, bool allow_side_stream, void* stream) {
   int rc = stage(FA_BWD_PREPROCESS, stream);
   if (rc) return rc;
   if (!allow_side_stream || !deterministic || dtype == FA_F32) {
@@ -325,4 +326,136 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
   return FA_OK;
 }
 
+}  // namespace
+
+namespace fa {
+
+int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream) {
+  auto stage = [&](fa_bwd_stage_id s, void* st) {
+    return fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                        dropout_p, seed, offset, deterministic, workspace, workspace_bytes, st);
+  };
+  return run_backward(stage, deterministic, dtype, allow_side_stream, stream);
+}
+
 }  // namespace fa
+
+// ------------------------- packed variable-length -------------------------
+namespace {
+
+struct VarlenWs {
+  int seq_pad, acc_rows;
+  size_t off_L2, off_D, off_dq, total;
+};
+
+VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int deterministic) {
+  VarlenWs w;
+  w.seq_pad = pad_rows(max_seqlen);
+  w.acc_rows = pad_rows(total) + fa::kPadRows;  // a tile may run past its sequence's last row
+  const size_t vec = (size_t)H * nseq * w.seq_pad * 4;
+  w.off_L2 = 0;
+  w.off_D = round256(vec);
+  w.off_dq = w.off_D + round256(vec);
+  w.total = w.off_dq + (deterministic ? 0 : round256((size_t)H * w.acc_rows * d * 4));
+  return w;
+}
+
+// Validation and parameters common to the varlen forward and backward.
+int varlen_params(AttnParams& p, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H, int d,
+                  int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window) {
+  if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
+  if (nseq < 1 || max_seqlen < 1 || total < 1 || H < 1) return FA_ERR_INVALID_ARG;
+  if ((long long)nseq * H > 65535) return FA_ERR_UNSUPPORTED;
+  // one CTA per (128-row tile of max_seqlen, sequence, head) in a 1-D grid
+  if ((long long)pad_rows(max_seqlen) / fa::kPadRows * nseq * H > 0x7fffffffll) return FA_ERR_UNSUPPORTED;
+  const fa_strides s = {stride_n, stride_n, stride_h};  // B = 1: the batch stride is never used
+  int rc = check_common(1, H, total, d, s, dtype, scale, window, 0.f);
+  if (rc) return rc;
+  fill_params(p, 1, H, total, d, s, scale, causal, window, 0.f, 0, 0);
+  p.cu_seqlens = cu_seqlens;
+  p.nseq = nseq;
+  p.max_seqlen = max_seqlen;
+  p.seq_pad = pad_rows(max_seqlen);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, int d, fa_dtype dtype,
+                                    int deterministic) {
+  if (nseq < 1 || max_seqlen < 1 || total < 1 || H < 1 || (d != 64 && d != 128)) return 0;
+  if (dtype != FA_F16 && dtype != FA_BF16) return 0;
+  return varlen_ws_layout(nseq, max_seqlen, total, H, d, deterministic).total;
+}
+
+int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens, int nseq,
+                  int max_seqlen, int total, int H, int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype,
+                  float scale, int causal, int window, void* stream) {
+  AttnParams p;
+  int rc = varlen_params(p, cu_seqlens, nseq, max_seqlen, total, H, d, stride_n, stride_h, dtype, scale, causal,
+                         window);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = o;
+  p.lse_out = lse;
+  if ((rc = status_ptr(&p.status))) return rc;
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
+      !make_map(&maps[2], v, p, bf16, fa::kStepKV))
+    return FA_ERR_CUDA;
+  maps[3] = maps[0];
+  return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H,
+                  int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window,
+                  int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  AttnParams p;
+  int rc = varlen_params(p, cu_seqlens, nseq, max_seqlen, total, H, d, stride_n, stride_h, dtype, scale, causal,
+                         window);
+  if (rc) return rc;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return FA_ERR_ALIGNMENT;
+  const VarlenWs w = varlen_ws_layout(nseq, max_seqlen, total, H, d, deterministic);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.out = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.n_pad = w.acc_rows;  // dQ accumulator rows per head (packed rows + tail)
+  char* ws = static_cast<char*>(workspace);
+  p.ws_nL2 = reinterpret_cast<float*>(ws + w.off_L2);
+  p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
+  p.ws_dq = deterministic ? nullptr : reinterpret_cast<float*>(ws + w.off_dq);
+  if ((rc = status_ptr(&p.status))) return rc;
+  const size_t acc_bytes = (size_t)H * w.acc_rows * d * 4;
+  auto stage = [&](fa_bwd_stage_id s, void* st) {
+    if (s == FA_BWD_PREPROCESS && p.ws_dq &&
+        cudaMemsetAsync(p.ws_dq, 0, acc_bytes, static_cast<cudaStream_t>(st)) != cudaSuccess)
+      return (int)FA_ERR_CUDA;
+    return launch_stage(s, p, dtype, deterministic, st);
+  };
+  return run_backward(stage, deterministic, dtype, true, stream);
+}
+
+}  // extern "C"

@@ -42,7 +42,64 @@ struct AttnParams {
   float* ws_nD;           // [B*H, n_pad]  -rowsum(dO o O), 0 past N (negated: feeds an add)
   float* ws_dq;           // [B*H, n_pad, d] fp32 dQ accumulator (atomic mode) or null
   unsigned int* status;   // device status word (timeout bits)
+  // Packed variable-length input (null cu_seqlens otherwise): the tensors are
+  // [total, H, d] (B = 1, N = total), sequence s occupies packed rows
+  // [cu_seqlens[s], cu_seqlens[s+1]), attention stays within a sequence, L is
+  // [H, total], and the L / D workspace rows of (h, s) start at
+  // (h * nseq + s) * seq_pad (seq_pad = max_seqlen rounded up to kPadRows).
+  const int* cu_seqlens;
+  int nseq;
+  int max_seqlen;
+  int seq_pad;
 };
+
+// One CTA's unit: a tile of rows of one (batch, head), or of one (sequence,
+// head) with packed variable-length input. Rows are local to the unit; row0 is
+// the unit's first row in the [B, N, H, d] (or packed) tensors, n its length,
+// ws its L / D workspace row base, acc its dQ-accumulator row base, lse its
+// base index in L.
+struct Unit {
+  int tile, b, h, bh, row0, n;
+  long long ws, acc, lse;
+};
+
+// Decodes block `idx`: tiles outermost, units in (batch, head) or (sequence,
+// head) order within a tile. reverse_tiles = n > 0 numbers the tiles n-1, n-2,
+// ... in launch order (heaviest first for the query-major kernels). Returns
+// false for tiles past the end of a short sequence (the CTA has no work).
+__device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int tile_rows, int reverse_tiles,
+                                            Unit& u) {
+  if (p.cu_seqlens == nullptr) {
+    const int BH = p.B * p.H;
+    u.tile = idx / BH;
+    if (reverse_tiles > 0) u.tile = reverse_tiles - 1 - u.tile;
+    u.bh = idx % BH;
+    u.b = u.bh / p.H;
+    u.h = u.bh % p.H;
+    u.row0 = 0;
+    u.n = p.N;
+    u.ws = (long long)u.bh * p.n_pad;
+    u.acc = u.ws;
+    u.lse = (long long)u.bh * p.N;
+    return true;
+  }
+  const int SH = p.nseq * p.H;
+  u.tile = idx / SH;
+  if (reverse_tiles > 0) u.tile = reverse_tiles - 1 - u.tile;
+  const int sh = idx % SH, sq = sh / p.H;
+  u.h = sh % p.H;
+  u.b = 0;
+  u.bh = u.h;
+  // Clamp the offsets into [0, N] and the length to max_seqlen, so that a
+  // malformed cu_seqlens cannot move any access outside the tensors.
+  const int s0 = min(max(p.cu_seqlens[sq], 0), p.N), s1 = min(max(p.cu_seqlens[sq + 1], s0), p.N);
+  u.row0 = s0;
+  u.n = min(s1 - s0, p.max_seqlen);
+  u.ws = ((long long)u.h * p.nseq + sq) * p.seq_pad;
+  u.acc = (long long)u.h * p.n_pad + s0;
+  u.lse = (long long)u.h * p.N + s0;
+  return u.tile * tile_rows < u.n;
+}
 
 // Allowed (query i, key j) pair under the causal / sliding-window mask.
 __device__ __forceinline__ bool pair_allowed(const AttnParams& p, int i, int j) {

@@ -129,32 +129,50 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_consta
   constexpr int G = D / 8;            // lanes per row
   constexpr int kRowsPerWarp = 32 / G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int bh = blockIdx.y;
   const int ib = blockIdx.x * vec_block_rows<D>() + warp * (kRowsPerWarp * kVecRows) + lane / G;
   const int e0 = (lane % G) * 8;
-  const T* o = static_cast<const T*>(p.o) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh + e0;
+  // y = batch * head, or sequence * head for packed variable-length input; rows
+  // below are local to it (n of them, padded to `pad` workspace rows).
+  int bh, row0 = 0, n = p.N, pad = p.n_pad;
+  long long ws0, lse0;
+  if (p.cu_seqlens == nullptr) {
+    bh = blockIdx.y;
+    ws0 = (long long)bh * p.n_pad;
+    lse0 = (long long)bh * p.N;
+  } else {
+    const int sq = blockIdx.y / p.H, h = blockIdx.y % p.H;
+    const int s0 = min(max(p.cu_seqlens[sq], 0), p.N), s1 = min(max(p.cu_seqlens[sq + 1], s0), p.N);
+    bh = h;  // B = 1
+    row0 = s0;
+    n = min(s1 - s0, p.max_seqlen);
+    pad = p.seq_pad;
+    ws0 = ((long long)h * p.nseq + sq) * p.seq_pad;
+    lse0 = (long long)h * p.N + s0;
+  }
+  const T* o = static_cast<const T*>(p.o) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh +
+               (long long)row0 * p.sn + e0;
   const T* g = static_cast<const T*>(p.dout) + (o - static_cast<const T*>(p.o));
   uint4 ov[kVecRows], gv[kVecRows];
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
     const int i = ib + r * kRowsPerWarp;
     ov[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < p.N) {
+    if (i < n) {
       ov[r] = __ldg(reinterpret_cast<const uint4*>(o + (long long)i * p.sn));
       gv[r] = __ldg(reinterpret_cast<const uint4*>(g + (long long)i * p.sn));
     }
   }
-  const long long ws0 = (long long)bh * p.n_pad;
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
     const int i = ib + r * kRowsPerWarp;
     const float acc = group_sum<D>(dot8<T>(ov[r], gv[r], 0.f));
-    if (i >= p.n_pad) continue;
+    if (i >= pad) continue;
     if (e0 == 0) {
       p.ws_nD[ws0 + i] = -acc;
-      p.ws_nL2[ws0 + i] = (i < p.N) ? -(p.lse[(long long)bh * p.N + i] * kLog2e) : __int_as_float(0xff800000);
+      p.ws_nL2[ws0 + i] = (i < n) ? -(p.lse[lse0 + i] * kLog2e) : __int_as_float(0xff800000);
     }
-    if (p.ws_dq != nullptr) {
+    // (packed input: the dQ accumulator is zeroed separately)
+    if (p.ws_dq != nullptr && p.cu_seqlens == nullptr) {
       float4* dq = reinterpret_cast<float4*>(p.ws_dq + (ws0 + i) * D + e0);
       dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -404,9 +422,12 @@ static inline unsigned grid_for_rows(long long rows, int rows_per_block) {
 
 cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
   const long long rows = (long long)p.B * p.n_pad * p.H;
-  if (dtype != 0 && (p.d == 64 || p.d == 128) && p.B * p.H <= 65535) {
-    const dim3 g((unsigned)((p.n_pad + vec_block_rows<128>() - 1) / vec_block_rows<128>()), (unsigned)(p.B * p.H));
-    const dim3 g64((unsigned)((p.n_pad + vec_block_rows<64>() - 1) / vec_block_rows<64>()), (unsigned)(p.B * p.H));
+  // packed variable-length input: y = sequence * head, x over seq_pad rows
+  const int prow = p.cu_seqlens ? p.seq_pad : p.n_pad;
+  const int units = p.cu_seqlens ? p.nseq * p.H : p.B * p.H;
+  if (dtype != 0 && (p.d == 64 || p.d == 128) && units <= 65535) {
+    const dim3 g((unsigned)((prow + vec_block_rows<128>() - 1) / vec_block_rows<128>()), (unsigned)units);
+    const dim3 g64((unsigned)((prow + vec_block_rows<64>() - 1) / vec_block_rows<64>()), (unsigned)units);
     if (p.d == 128)
       dtype == 1 ? preprocess_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
                  : preprocess_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);

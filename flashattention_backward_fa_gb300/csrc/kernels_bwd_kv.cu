@@ -108,14 +108,16 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
   auto bar = [&](int idx) -> uint32_t { return sb + C::oBar + 8u * idx; };
 
-  // Work unit: (batch*head, key block), heaviest key blocks first under a causal mask.
-  const int BH = p.B * p.H;
-  const int kv_tile = blockIdx.x / BH;
-  const int bh = blockIdx.x % BH;
-  const int b = bh / p.H, h = bh % p.H;
-  const int j0 = kv_tile * kRowsKV;
+  // Work unit: (batch*head or sequence*head, key block), heaviest key blocks
+  // first under a causal mask. A key block past the end of its sequence has no
+  // work: the whole CTA leaves before any setup.
+  Unit u;
+  if (!unit_decode(p, blockIdx.x, kRowsKV, 0, u)) return;
+  const int bh = u.bh, b = u.b, h = u.h;
+  const int Nl = u.n;                    // rows of this (batch, head) or sequence
+  const int j0 = u.tile * kRowsKV;
   const int i_first = p.causal ? j0 : 0;
-  int i_last = p.N - 1;
+  int i_last = Nl - 1;
   if (p.window > 0) i_last = min(i_last, j0 + kRowsKV - 2 + p.window);
   const int nsteps = (i_last >= i_first) ? (i_last - i_first) / kStepQ + 1 : 0;
 
@@ -161,8 +163,8 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar(C::bKV), 2 * C::kKVTile);
       for (int pn = 0; pn < C::kPanels; ++pn) {
-        tma_load_4d(sb + C::oK + pn * C::kKVPanel, &tmK, bar(C::bKV), 64 * pn, j0, h, b);
-        tma_load_4d(sb + C::oV + pn * C::kKVPanel, &tmV, bar(C::bKV), 64 * pn, j0, h, b);
+        tma_load_4d(sb + C::oK + pn * C::kKVPanel, &tmK, bar(C::bKV), 64 * pn, u.row0 + j0, h, b);
+        tma_load_4d(sb + C::oV + pn * C::kKVPanel, &tmV, bar(C::bKV), 64 * pn, u.row0 + j0, h, b);
       }
       int issued = 0;
       for (int it = 0; it < nsteps; ++it) {
@@ -171,12 +173,12 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const int i0 = i_first + it * kStepQ;
         mbar_arrive_expect_tx(bar(C::bQFull + s), C::kStageBytes);
         for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn, i0,
-                      h, b);
+          tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn,
+                      u.row0 + i0, h, b);
           tma_load_4d(sb + C::oDO + s * C::kQTile + pn * C::kQPanel, &tmDO, bar(C::bQFull + s), 64 * pn,
-                      i0, h, b);
+                      u.row0 + i0, h, b);
         }
-        const long long ws = (long long)bh * p.n_pad + i0;
+        const long long ws = u.ws + i0;
         bulk_load(sb + C::oL + s * kStepQ * 4, p.ws_nL2 + ws, kStepQ * 4, bar(C::bQFull + s));
         bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_nD + ws, kStepQ * 4, bar(C::bQFull + s));
         issued = it + 1;
@@ -349,16 +351,16 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       const int base = i0 + 32 * c;
       // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep bits
       uint32_t allow = 0u;
-      if (j < p.N) {
+      if (j < Nl) {
         const int lo = p.causal ? j - base : 0;
-        int hi = p.N - base;
+        int hi = Nl - base;
         if (p.window > 0) hi = min(hi, j + p.window - base);
         allow = bit_range(lo, hi);
       }
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) {
         __syncwarp();  // warp-collective (shuffles)
-        keep = keep_bits_for_key(p.drop, bh, p.N, base, j);
+        keep = keep_bits_for_key(p.drop, bh, Nl, base, j);
       }
       float P[32];          // P (before dropout) of this thread's 32 pairs, for the dS phase
       bool split_h[2];
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty + bb));
         if (jl < D) {
-          float* dst = p.ws_dq + ((long long)bh * p.n_pad + base) * D + jl;
+          float* dst = p.ws_dq + (u.acc + base) * D + jl;
 #pragma unroll
           for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
         }
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     if (ok) {
       tc_fence_after();
       const bool isK = rg >= 2;
-      const long long off = (long long)b * p.sb + (long long)j * p.sn + (long long)h * p.sh;
+      const long long off = (long long)b * p.sb + (long long)(u.row0 + j) * p.sn + (long long)h * p.sh;
       uint16_t* dst = static_cast<uint16_t*>(isK ? p.dk : p.dv) + off;
       const uint32_t col0 = (isK ? tdK : tdV) + lane_off;
       const float mul = isK ? p.scale : 1.f;
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
 #pragma unroll
         for (int x = 0; x < 16; ++x)
           w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * mul, __uint_as_float(r[2 * x + 1]) * mul);
-        if (j < p.N) {
+        if (j < Nl) {
           uint4* g = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int t = 0; t < 4; ++t) g[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
@@ -553,8 +555,9 @@ static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, c
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int tiles = (p.N + kRowsKV - 1) / kRowsKV;
-  const unsigned grid = (unsigned)(tiles * p.B * p.H);
+  const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
+  const int tiles = (rows + kRowsKV - 1) / kRowsKV;
+  const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
   kern<<<grid, kKVThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }

@@ -119,14 +119,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
   auto bar = [&](int idx) -> uint32_t { return sb + C::oBar + 8u * idx; };
 
-  // Work unit: (batch*head, query block), heaviest query blocks first under a causal mask.
-  const int BH = p.B * p.H;
-  const int ntiles = (p.N + kRowsQ - 1) / kRowsQ;
-  const int q_tile = ntiles - 1 - (int)(blockIdx.x / BH);
-  const int bh = blockIdx.x % BH;
-  const int b = bh / p.H, h = bh % p.H;
-  const int i0 = q_tile * kRowsQ;
-  const int j_last = p.causal ? min(p.N - 1, i0 + kRowsQ - 1) : p.N - 1;
+  // Work unit: (batch*head or sequence*head, query block), heaviest query
+  // blocks first under a causal mask. A query block past the end of its
+  // sequence has no work: the whole CTA leaves before any setup.
+  Unit u;
+  const int ntiles = ((p.cu_seqlens ? p.max_seqlen : p.N) + kRowsQ - 1) / kRowsQ;
+  if (!unit_decode(p, blockIdx.x, kRowsQ, ntiles, u)) return;
+  const int bh = u.bh, b = u.b, h = u.h;
+  const int Nl = u.n;                    // rows of this (batch, head) or sequence
+  const int i0 = u.tile * kRowsQ;
+  const int j_last = p.causal ? min(Nl - 1, i0 + kRowsQ - 1) : Nl - 1;
   const int j_first = p.window > 0 ? (max(0, i0 - p.window + 1) / kStepKV) * kStepKV : 0;
   const int nkv = (j_last >= j_first) ? (j_last - j_first) / kStepKV + 1 : 0;
   // One pass over the key blocks in both modes.
@@ -183,8 +185,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const CUtensorMap* mL = kDq ? &tmK : &tmV;
       mbar_arrive_expect_tx(bar(C::bRes), C::kResident);
       for (int pn = 0; pn < C::kPanels; ++pn) {
-        tma_load_4d(sb + C::oQ + pn * C::kPanel, &tmQ, bar(C::bRes), 64 * pn, i0, h, b);
-        if (kDq) tma_load_4d(sb + C::oDO + pn * C::kPanel, &tmDO, bar(C::bRes), 64 * pn, i0, h, b);
+        tma_load_4d(sb + C::oQ + pn * C::kPanel, &tmQ, bar(C::bRes), 64 * pn, u.row0 + i0, h, b);
+        if (kDq) tma_load_4d(sb + C::oDO + pn * C::kPanel, &tmDO, bar(C::bRes), 64 * pn, u.row0 + i0, h, b);
       }
       int issuedE = 0, issuedL = 0;
       bool ok = true;
@@ -195,7 +197,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (!mbar_wait(bar(C::bEEmpty + se), ((it / C::kNE) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(bar(C::bEFull + se), C::kTile);
         for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_4d(sb + C::oE + se * C::kTile + pn * C::kPanel, mE, bar(C::bEFull + se), 64 * pn, jj, h, b);
+          tma_load_4d(sb + C::oE + se * C::kTile + pn * C::kPanel, mE, bar(C::bEFull + se), 64 * pn, u.row0 + jj,
+                      h, b);
         issuedE = it + 1;
         if (it >= first_out) {
           const int li = it - first_out, sl = li % C::kNL;
@@ -205,7 +208,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
           mbar_arrive_expect_tx(bar(C::bLFull + sl), C::kTile);
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn, jj, h, b);
+            tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn,
+                        u.row0 + jj, h, b);
           issuedL = li + 1;
         }
       }
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int i = i0 + il;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tdPc = tdP + lane_off + 32 * c;
-    const long long ws = (long long)bh * p.n_pad + i;  // i < n_pad always
+    const long long ws = u.ws + i;  // i < the padded row count always
     // dQ: -L*log2(e) (-inf for a row with no allowed key) and -D, read; the
     // negated forms are addends of one FMA / add (packed two-wide below).
     // Forward: mref, the running reference maximum of S*scale*log2e over the
@@ -364,9 +368,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       tc_fence_after();
       // allowed keys of this warpgroup's 32 columns (bit x <-> key base + x)
       const uint32_t allow =
-          bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(p.N - base, p.causal ? i + 1 - base : 32));
+          bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(Nl - base, p.causal ? i + 1 - base : 32));
       uint32_t keep = 0xFFFFFFFFu;
-      if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, p.N, i, base);
+      if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, Nl, i, base);
       // dQ: both halves of this warpgroup's dP columns come in with S, so the dP
       // buffer is released (and the next dP MMAs may run) before any arithmetic.
       // Forward: all of S comes in, for the row maximum.
@@ -563,7 +567,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (ok && have_acc) ok = warp_wait<kRowMathPoll>(bar(C::bAcc), 0, abort_flag, p.status);
     if (ok) {
       tc_fence_after();
-      const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+      const long long off = (long long)b * p.sb + (long long)(u.row0 + i) * p.sn + (long long)h * p.sh;
       uint16_t* dst = static_cast<uint16_t*>(p.out) + off;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -580,13 +584,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
         for (int x = 0; x < 8; ++x)
           w[x] = pack2<kBf16>(__uint_as_float(r[2 * x]) * scale_out, __uint_as_float(r[2 * x + 1]) * scale_out);
-        if (i < p.N) {
+        if (i < Nl) {
           uint4* g = reinterpret_cast<uint4*>(dst + col);
           g[0] = make_uint4(w[0], w[1], w[2], w[3]);
           g[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      if (!kDq && c == 0 && i < p.N) p.lse_out[(long long)bh * p.N + i] = lse_row;
+      if (!kDq && c == 0 && i < Nl) p.lse_out[u.lse + i] = lse_row;
     }
   }
 
@@ -606,8 +610,9 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int tiles = (p.N + kRowsQ - 1) / kRowsQ;
-  const unsigned grid = (unsigned)(tiles * p.B * p.H);
+  const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
+  const int tiles = (rows + kRowsQ - 1) / kRowsQ;
+  const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
   kern<<<grid, kQThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
   return cudaGetLastError();
 }

@@ -87,3 +87,27 @@ def make_inputs(w: Workload, device: str = "cpu"):
 def head_subset(w: Workload, heads):
     """Slice a workload's inputs to some heads (the oracle checks large ones per head)."""
     return w.with_(H=len(heads))
+
+
+def make_varlen_inputs(lengths, H: int, d: int, dtype: str, seed: int = 0, dout_std: float = 1.0):
+    """Packed variable-length inputs: (q, k, v, do) as [total, H, d] tensors of
+    ``dtype`` plus cu_seqlens (int32, nseq + 1 offsets), drawn like
+    :func:`make_inputs` with the packed shape."""
+    lengths = [int(n) for n in lengths]
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (int(cu[-1]), H, d)
+    q, k, v, do = (torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(4))
+    if dout_std != 1.0:
+        do = do * torch.tensor(dout_std, dtype=torch.float32)
+    dt = _DTYPES[dtype]
+    return q.to(dt), k.to(dt), v.to(dt), do.to(dt), cu
+
+
+def varlen_lengths(nseq: int, max_seqlen: int, seed: int = 0, min_seqlen: int = 1):
+    """A seeded length mix: nseq lengths uniform on [min_seqlen, max_seqlen]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randint(min_seqlen, max_seqlen + 1, (nseq,), generator=g).tolist()

@@ -139,6 +139,38 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
                    uint64_t seed, uint64_t offset, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Packed variable-length sequences ("Lecture 7 — Backward Pass and
+ * Validation", §Use it in the real stack, lists varlen among the cases a
+ * complete harness covers; the math per sequence is that of fa_fwd / fa_bwd).
+ *
+ * nseq sequences of different lengths share one packed [total, H, d] tensor
+ * per operand: sequence s occupies rows [cu_seqlens[s], cu_seqlens[s+1]), and
+ * attention (with the causal / window mask, positions local to the sequence)
+ * never crosses a sequence boundary. cu_seqlens is a DEVICE int32 array of
+ * nseq + 1 nondecreasing offsets with cu_seqlens[0] = 0, cu_seqlens[nseq] =
+ * total and every length <= max_seqlen; the library cannot check device
+ * contents, so it clamps offsets into [0, total] and lengths to max_seqlen (a
+ * malformed array gives wrong gradients, never an out-of-bounds access).
+ * stride_n / stride_h are element strides of the packed tensors (d stride 1,
+ * multiples of 8). lse is contiguous fp32 [H, total]. 16-bit dtypes, d in
+ * {64, 128}, nseq * H <= 65535, no dropout (dropout_p is not an argument).
+ * Errors as fa_fwd / fa_bwd; the caller owns every buffer.
+ * ------------------------------------------------------------------------- */
+size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, int d, fa_dtype dtype,
+                                    int deterministic);
+/* Forward: O [total, H, d] and lse [H, total] per sequence. */
+int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens, int nseq,
+                  int max_seqlen, int total, int H, int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype,
+                  float scale, int causal, int window, void* stream);
+/* Backward: dQ, dK, dV [total, H, d] per sequence; deterministic and atomic dQ
+ * as fa_bwd; workspace of fa_varlen_bwd_workspace_size(...) bytes, 256-byte
+ * aligned. */
+int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H,
+                  int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window,
+                  int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Reads (and with clear != 0 resets) the status word of the current device.
  * Call after synchronising the streams the kernels ran on. *status receives
  * the raw bits (1 = a bounded wait timed out). Returns FA_OK, FA_ERR_TIMEOUT

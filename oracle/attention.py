@@ -235,3 +235,47 @@ def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, s
 
 __all__ = ["allowed", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows", "backward_rows",
            "backward_cols"]
+
+
+def _segments(cu_seqlens):
+    cu = [int(x) for x in np.asarray(cu_seqlens).reshape(-1)]
+    return list(zip(cu[:-1], cu[1:]))
+
+
+def varlen_forward(q, k, v, cu_seqlens, scale, causal=False, window=0):
+    """Packed variable-length forward; returns (O [total,H,d], L [H,total]) float64.
+
+    q, k, v are [total, H, d]; sequence s is rows cu_seqlens[s]:cu_seqlens[s+1]
+    and attends only within itself, with mask positions local to it. This is
+    :func:`forward` applied to each sequence as a batch of one ("Lecture 7 —
+    Backward Pass and Validation" §Use it in the real stack names packed
+    variable-length batches among the cases to cover; the attention of each
+    sequence is unchanged by its neighbours).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, H, d = q.shape
+    O = np.zeros((total, H, d))
+    L = np.full((H, total), -np.inf)
+    for s0, s1 in _segments(cu_seqlens):
+        if s1 <= s0:
+            continue
+        o, lse = forward(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], scale, causal, window)
+        O[s0:s1] = o[0]
+        L[:, s0:s1] = lse[0]
+    return O, L
+
+
+def varlen_backward(q, k, v, o, do, lse, cu_seqlens, scale, causal=False, window=0):
+    """Packed variable-length backward from (O, L [H,total]); returns (dQ, dK, dV) [total,H,d] float64.
+
+    :func:`backward` applied to each sequence of the pack on its own.
+    """
+    q, k, v, o, do, lse = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do), _f64(lse)
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s0, s1 in _segments(cu_seqlens):
+        if s1 <= s0:
+            continue
+        g = backward(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], o[None, s0:s1], do[None, s0:s1],
+                     lse[None, :, s0:s1], scale, causal, window)
+        dQ[s0:s1], dK[s0:s1], dV[s0:s1] = g[0][0], g[1][0], g[2][0]
+    return dQ, dK, dV

@@ -111,6 +111,50 @@ def test_bwd_rejects_bad_arguments(lib):
     assert _bwd(lib, stage=1, d=80) == EUNSUP
 
 
+def _vfwd(lib, *, q=P, cu=P, nseq=3, msl=300, total=700, H=2, d=128, sn=256, sh=128, dt=BF16, window=0):
+    return lib.fa_varlen_fwd(q, P, P, P, P, cu, nseq, msl, total, H, d, sn, sh, dt, 0.1, 1, window, None)
+
+
+def _vbwd(lib, *, ptrs=None, cu=P, nseq=3, msl=300, total=700, H=2, d=128, dt=BF16, det=1, ws=0x100000,
+          ws_bytes=1 << 30):
+    ptrs = ptrs or [P] * 9
+    return lib.fa_varlen_bwd(*ptrs, cu, nseq, msl, total, H, d, H * d, d, dt, 0.1, 1, 0, det, ws, ws_bytes, None)
+
+
+def test_varlen_rejects_bad_arguments(lib):
+    assert _vfwd(lib, dt=F32) == EUNSUP          # 16-bit only
+    assert _vfwd(lib, d=96) == EUNSUP
+    assert _vfwd(lib, cu=0) == EINVAL
+    assert _vfwd(lib, cu=P + 2) == EINVAL        # int32 offsets must be 4-byte aligned
+    assert _vfwd(lib, nseq=0) == EINVAL
+    assert _vfwd(lib, msl=0) == EINVAL
+    assert _vfwd(lib, total=0) == EINVAL
+    assert _vfwd(lib, nseq=40000, H=2) == EUNSUP  # nseq * H bounded by the grid's y extent
+    assert _vfwd(lib, sn=260) == EALIGN
+    assert _vfwd(lib, window=-1) == EINVAL
+    assert _vfwd(lib, q=0) == EINVAL
+    assert _vfwd(lib, q=P + 8) == EALIGN
+    assert _vbwd(lib, ptrs=[P] * 8 + [0]) == EINVAL
+    assert _vbwd(lib, ws=0) == EWS
+    need = fa.fa_varlen_bwd_workspace_size(3, 300, 700, 2, 128, BF16, True)
+    assert _vbwd(lib, ws_bytes=need - 1) == EWS
+    need_atomic = fa.fa_varlen_bwd_workspace_size(3, 300, 700, 2, 128, BF16, False)
+    assert _vbwd(lib, det=0, ws_bytes=need) == EWS and need_atomic > need
+
+
+def test_varlen_workspace_size(lib):
+    # L and D rows per (head, sequence), each padded to roundup(max_seqlen, 128);
+    # atomic mode adds an fp32 dQ accumulator of roundup(total, 128) + 128 rows per head.
+    nseq, msl, total, H, d = 3, 300, 700, 4, 128
+    vec = H * nseq * 384 * 4
+    vec = (vec + 255) // 256 * 256
+    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, BF16, True) == 2 * vec
+    acc = H * (768 + 128) * d * 4
+    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, F16, False) == 2 * vec + acc
+    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, F32, True) == 0
+    assert fa.fa_varlen_bwd_workspace_size(0, msl, total, H, d, BF16, True) == 0
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)

@@ -251,3 +251,34 @@ def test_sampled_rows_and_columns_match_whole_head(causal, window, p):
             dk_c, dv_c = oracle.backward_cols(q, k, v, O, do, L, b, h, rows, 0.3, causal, window, p, 9, 2)
             np.testing.assert_allclose(dk_c, dK[b, rows, h], rtol=1e-12, atol=1e-13)
             np.testing.assert_allclose(dv_c, dV[b, rows, h], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 5), (False, 4)])
+def test_varlen_matches_block_diagonal_dense(causal, window):
+    """Packed sequences against one dense attention over the whole pack whose
+    mask keeps only pairs inside one sequence (positions counted from each
+    sequence's start), differentiated by torch float64 autograd. An off-by-one
+    in the segment bounds or a mask taken on packed instead of local
+    positions fails this."""
+    cu = np.array([0, 7, 8, 8, 29, 40])  # lengths 7, 1, 0 (empty), 21, 11
+    total, H, d = int(cu[-1]), 2, 8
+    q, k, v, do = (_rand((total, H, d), 1200 + t) for t in range(4))
+    scale = float(np.float32(0.3))  # the oracle takes the float32 value the kernels receive
+    O, L = oracle.varlen_forward(q, k, v, cu, scale, causal, window)
+    dQ, dK, dV = oracle.varlen_backward(q, k, v, O, do, L, cu, scale, causal, window)
+    seg = np.searchsorted(cu, np.arange(total), side="right") - 1
+    pos = np.arange(total) - cu[seg]
+    ok = seg[:, None] == seg[None, :]
+    if causal:
+        ok &= pos[None, :] <= pos[:, None]
+    if window > 0:
+        ok &= pos[None, :] > pos[:, None] - window
+    tq, tk, tv = (torch.tensor(x[None], requires_grad=True) for x in (q, k, v))
+    out = _torch_attention(tq, tk, tv, scale, torch.tensor(ok)[None, None], None)
+    out.backward(torch.tensor(do[None]))
+    for a, t in ((O, out.detach()[0]), (dQ, tq.grad[0]), (dK, tk.grad[0]), (dV, tv.grad[0])):
+        t = t.numpy()
+        assert np.linalg.norm(a - t) <= 1e-12 * np.linalg.norm(t)
+    s = torch.einsum("nhd,mhd->hnm", torch.tensor(q), torch.tensor(k)) * scale
+    np.testing.assert_allclose(L, torch.logsumexp(s.masked_fill(~torch.tensor(ok), float("-inf")), -1).numpy(),
+                               rtol=1e-13, atol=1e-13)
