@@ -63,17 +63,29 @@ struct Unit {
   long long ws, acc, lse;
 };
 
-// Decodes block `idx`: tiles outermost, units in (batch, head) or (sequence,
-// head) order within a tile. reverse_tiles = n > 0 numbers the tiles n-1, n-2,
-// ... in launch order (heaviest first for the query-major kernels). Returns
-// false for tiles past the end of a short sequence (the CTA has no work).
-__device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int tile_rows, int reverse_tiles,
+// Units (one (batch, head) or (sequence, head) each) are launched in groups
+// of kUnitGroup: within a group tiles are outermost (heaviest first), so the
+// CTAs resident at one time cover about 152 / kUnitGroup tiles of each of a
+// few units and share those units' streamed operands through L2, while the
+// heavy tiles of every group still start early.
+constexpr int kUnitGroup = 8;
+
+// Decodes block `idx` of a grid of ntiles * units CTAs. reverse_tiles != 0
+// numbers the tiles from the last one down in launch order (heaviest first for
+// the query-major kernels under a causal mask). Returns false for tiles past
+// the end of a short sequence (the CTA has no work).
+__device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int tile_rows, bool reverse_tiles,
                                             Unit& u) {
-  if (p.cu_seqlens == nullptr) {
-    const int BH = p.B * p.H;
-    u.tile = idx / BH;
-    if (reverse_tiles > 0) u.tile = reverse_tiles - 1 - u.tile;
-    u.bh = idx % BH;
+  const bool packed = p.cu_seqlens != nullptr;
+  const int units = packed ? p.nseq * p.H : p.B * p.H;
+  const int ntiles = ((packed ? p.max_seqlen : p.N) + tile_rows - 1) / tile_rows;
+  const int g = idx / (kUnitGroup * ntiles), r = idx - g * (kUnitGroup * ntiles);
+  const int gsize = min(kUnitGroup, units - g * kUnitGroup);  // the last group may be short
+  u.tile = r / gsize;
+  if (reverse_tiles) u.tile = ntiles - 1 - u.tile;
+  const int unit = g * kUnitGroup + r % gsize;
+  if (!packed) {
+    u.bh = unit;
     u.b = u.bh / p.H;
     u.h = u.bh % p.H;
     u.row0 = 0;
@@ -83,11 +95,8 @@ __device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int ti
     u.lse = (long long)u.bh * p.N;
     return true;
   }
-  const int SH = p.nseq * p.H;
-  u.tile = idx / SH;
-  if (reverse_tiles > 0) u.tile = reverse_tiles - 1 - u.tile;
-  const int sh = idx % SH, sq = sh / p.H;
-  u.h = sh % p.H;
+  const int sq = unit / p.H;
+  u.h = unit % p.H;
   u.b = 0;
   u.bh = u.h;
   // Clamp the offsets into [0, N] and the length to max_seqlen, so that a

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   // first under a causal mask. A key block past the end of its sequence has no
   // work: the whole CTA leaves before any setup.
   Unit u;
-  if (!unit_decode(p, blockIdx.x, kRowsKV, 0, u)) return;
+  if (!unit_decode(p, blockIdx.x, kRowsKV, false, u)) return;
   const int bh = u.bh, b = u.b, h = u.h;
   const int Nl = u.n;                    // rows of this (batch, head) or sequence
   const int j0 = u.tile * kRowsKV;

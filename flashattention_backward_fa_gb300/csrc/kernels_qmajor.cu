@@ -123,8 +123,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // blocks first under a causal mask. A query block past the end of its
   // sequence has no work: the whole CTA leaves before any setup.
   Unit u;
-  const int ntiles = ((p.cu_seqlens ? p.max_seqlen : p.N) + kRowsQ - 1) / kRowsQ;
-  if (!unit_decode(p, blockIdx.x, kRowsQ, ntiles, u)) return;
+  if (!unit_decode(p, blockIdx.x, kRowsQ, true, u)) return;
   const int bh = u.bh, b = u.b, h = u.h;
   const int Nl = u.n;                    // rows of this (batch, head) or sequence
   const int i0 = u.tile * kRowsQ;
