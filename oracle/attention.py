@@ -25,6 +25,11 @@ kernels avoid):
   dS = P o (dP - D); dQ = scale * dS K; dK = scale * dS^T Q.
 * Masks, "Lecture 7" §Mask behaviour: causal keeps j <= i (top-left aligned,
   square), a window W > 0 keeps j > i - W; both may be on at once.
+* ALiBi ("Lecture 7" §Use it in the real stack names it among the cases a
+  complete harness covers; the pages give no formula): the usual linear
+  position bias, S_ij = scale * q_i.k_j - m * |i - j| with one slope m per
+  head (or per batch and head), added after the scale and before the mask. The
+  slopes are constants, so the gradient formulas above are unchanged.
   A row with no allowed key has L = -inf, P = 0, O = 0 and zero gradients.
 
 Parity pins (tests that fix this oracle to something other than itself) live
@@ -55,6 +60,20 @@ def allowed(rows, N: int, causal: bool, window: int):
     return ok
 
 
+def alibi_bias(alibi, b: int, h: int, rows, cols):
+    """-m * |i - j| for the given query rows and key columns (0 without ALiBi).
+
+    ``alibi`` holds the slopes m, shaped [H] (shared over the batch) or [B, H].
+    """
+    if alibi is None:
+        return 0.0
+    sl = np.asarray(alibi, dtype=np.float64)
+    m = sl[h] if sl.ndim == 1 else sl[b, h]
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.asarray(cols, dtype=np.int64)[None, :]
+    return -m * np.abs(i - j).astype(np.float64)
+
+
 def _panels(N: int):
     rows = max(1, min(N, _PANEL_BYTES // (8 * max(N, 1))))
     for r0 in range(0, N, rows):
@@ -73,7 +92,7 @@ def _dropout_scale(b, h, H, N, rows, seed, offset, p):
     return z.astype(np.float64) / (1.0 - p)
 
 
-def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None):
     """Attention forward; returns (O [B,N,H,d] float64, L [B,H,N] float64).
 
     q, k, v are [B, N, H, d] arrays of any float dtype (widened exactly).
@@ -90,7 +109,7 @@ def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offse
             for r0, r1 in _panels(N):
                 rows = np.arange(r0, r1)
                 ok = allowed(rows, N, causal, window)
-                S = np.where(ok, scale * (Q[r0:r1] @ K.T), -np.inf)
+                S = np.where(ok, scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N)), -np.inf)
                 m = S.max(axis=1)
                 live = np.isfinite(m)
                 ms = np.where(live, m, 0.0)
@@ -115,7 +134,7 @@ def preprocess_D(o, do):
 
 
 def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
-             seed=0, offset=0):
+             seed=0, offset=0, alibi=None):
     """Attention backward from the saved state (O, L); returns (dQ, dK, dV, D).
 
     Gradients are [B, N, H, d] float64, D is [B, H, N] float64. ``o`` and
@@ -139,7 +158,7 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
                 ok = allowed(rows, N, causal, window)
                 Lr = lse[b, h, r0:r1]
                 live = np.isfinite(Lr)
-                S = scale * (Q[r0:r1] @ K.T)
+                S = scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N))
                 # P_ij = exp(S_ij - L_i) on allowed pairs of rows that have any.
                 P = np.where(ok & live[:, None],
                              np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
@@ -155,7 +174,8 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
     return dQ, dK, dV, D
 
 
-def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
+                 alibi=None):
     """O[b, rows, h, :] and L[b, h, rows] of one head: the same definitions as
     :func:`forward`, evaluated for the listed query rows only (rows are independent)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -163,7 +183,8 @@ def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0
     scale = float(np.float32(scale))
     rows = np.asarray(rows, dtype=np.int64)
     ok = allowed(rows, N, causal, window)
-    S = np.where(ok, scale * (q[b, rows, h, :] @ k[b, :, h, :].T), -np.inf)
+    S = np.where(ok, scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N)),
+                 -np.inf)
     m = S.max(axis=1)
     live = np.isfinite(m)
     ms = np.where(live, m, 0.0)
@@ -176,7 +197,7 @@ def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0
 
 
 def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0,
-                  offset=0):
+                  offset=0, alibi=None):
     """dQ[b, rows, h, :] of one head from the given O and L (function mode), by the
     definitions of :func:`backward` restricted to the listed query rows."""
     q, k, v, o, do = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do)
@@ -187,7 +208,7 @@ def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0
     ok = allowed(rows, N, causal, window)
     Lr = lse[b, h, rows]
     live = np.isfinite(Lr)
-    S = scale * (q[b, rows, h, :] @ k[b, :, h, :].T)
+    S = scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N))
     P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
     D = np.einsum("rd,rd->r", do[b, rows, h, :], o[b, rows, h, :])
     dP = do[b, rows, h, :] @ v[b, :, h, :].T
@@ -199,7 +220,7 @@ def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0
 
 
 def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0, dropout_p=0.0, seed=0,
-                  offset=0):
+                  offset=0, alibi=None):
     """(dK, dV)[b, cols, h, :] of one head from the given O and L (function mode):
     the definitions of :func:`backward` restricted to the listed key rows, which
     need the column slice P[:, cols] over all query rows."""
@@ -212,7 +233,7 @@ def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0
     ok = allowed(rows, N, causal, window)[:, cols]
     Lr = lse[b, h, :]
     live = np.isfinite(Lr)
-    S = scale * (q[b, :, h, :] @ k[b, cols, h, :].T)
+    S = scale * (q[b, :, h, :] @ k[b, cols, h, :].T) + alibi_bias(alibi, b, h, rows, cols)
     P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
     D = np.einsum("nd,nd->n", do[b, :, h, :], o[b, :, h, :])
     zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
@@ -226,15 +247,23 @@ def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0
     return scale * (dS.T @ q[b, :, h, :]), Pt.T @ do[b, :, h, :]
 
 
-def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None):
     """Exact mode: forward in float64, then backward from that O and L."""
-    O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset)
-    dQ, dK, dV, D = backward(q, k, v, O, do, L, scale, causal, window, dropout_p, seed, offset)
+    O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi)
+    dQ, dK, dV, D = backward(q, k, v, O, do, L, scale, causal, window, dropout_p, seed, offset, alibi)
     return O, L, dQ, dK, dV, D
 
 
-__all__ = ["allowed", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows", "backward_rows",
-           "backward_cols"]
+__all__ = ["allowed", "alibi_bias", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows",
+           "backward_rows", "backward_cols", "varlen_forward", "varlen_backward"]
+
+
+def _seq_slopes(alibi, sq: int):
+    """Slopes of sequence sq: [H] shared by every sequence, or row sq of [nseq, H]."""
+    if alibi is None:
+        return None
+    sl = np.asarray(alibi, dtype=np.float64)
+    return sl if sl.ndim == 1 else sl[sq]
 
 
 def _segments(cu_seqlens):
@@ -242,7 +271,7 @@ def _segments(cu_seqlens):
     return list(zip(cu[:-1], cu[1:]))
 
 
-def varlen_forward(q, k, v, cu_seqlens, scale, causal=False, window=0):
+def varlen_forward(q, k, v, cu_seqlens, scale, causal=False, window=0, alibi=None):
     """Packed variable-length forward; returns (O [total,H,d], L [H,total]) float64.
 
     q, k, v are [total, H, d]; sequence s is rows cu_seqlens[s]:cu_seqlens[s+1]
@@ -256,26 +285,27 @@ def varlen_forward(q, k, v, cu_seqlens, scale, causal=False, window=0):
     total, H, d = q.shape
     O = np.zeros((total, H, d))
     L = np.full((H, total), -np.inf)
-    for s0, s1 in _segments(cu_seqlens):
+    for sq, (s0, s1) in enumerate(_segments(cu_seqlens)):
         if s1 <= s0:
             continue
-        o, lse = forward(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], scale, causal, window)
+        o, lse = forward(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], scale, causal, window,
+                         alibi=_seq_slopes(alibi, sq))
         O[s0:s1] = o[0]
         L[:, s0:s1] = lse[0]
     return O, L
 
 
-def varlen_backward(q, k, v, o, do, lse, cu_seqlens, scale, causal=False, window=0):
+def varlen_backward(q, k, v, o, do, lse, cu_seqlens, scale, causal=False, window=0, alibi=None):
     """Packed variable-length backward from (O, L [H,total]); returns (dQ, dK, dV) [total,H,d] float64.
 
     :func:`backward` applied to each sequence of the pack on its own.
     """
     q, k, v, o, do, lse = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do), _f64(lse)
     dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    for s0, s1 in _segments(cu_seqlens):
+    for sq, (s0, s1) in enumerate(_segments(cu_seqlens)):
         if s1 <= s0:
             continue
         g = backward(q[None, s0:s1], k[None, s0:s1], v[None, s0:s1], o[None, s0:s1], do[None, s0:s1],
-                     lse[None, :, s0:s1], scale, causal, window)
+                     lse[None, :, s0:s1], scale, causal, window, alibi=_seq_slopes(alibi, sq))
         dQ[s0:s1], dK[s0:s1], dV[s0:s1] = g[0][0], g[1][0], g[2][0]
     return dQ, dK, dV

@@ -282,3 +282,83 @@ def test_varlen_matches_block_diagonal_dense(causal, window):
     s = torch.einsum("nhd,mhd->hnm", torch.tensor(q), torch.tensor(k)) * scale
     np.testing.assert_allclose(L, torch.logsumexp(s.masked_fill(~torch.tensor(ok), float("-inf")), -1).numpy(),
                                rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------- ALiBi ---------------------------------------
+@pytest.mark.parametrize("N,d,causal,window,p", [(6, 3, True, 0, 0.0), (7, 2, False, 0, 0.0), (8, 2, True, 3, 0.25)])
+def test_alibi_central_finite_differences(N, d, causal, window, p):
+    """Gradients with the position bias on, against central differences of the biased forward."""
+    B, H = 2, 2
+    q, k, v, R = (_rand((B, N, H, d), 300 + t) for t in range(4))
+    slopes = np.array([[0.5, 0.125], [0.25, 1.0]])  # [B, H]
+    kw = dict(causal=causal, window=window, dropout_p=p, seed=5, offset=1, alibi=slopes)
+    _, _, dQ, dK, dV, _ = oracle.reference_grads(q, k, v, R, 0.6, **kw)
+
+    def loss(qq, kk, vv):
+        return float((R * oracle.forward(qq, kk, vv, 0.6, **kw)[0]).sum())
+
+    h = 1e-5
+    for which, grad in ((0, dQ), (1, dK), (2, dV)):
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            fd[idx] = (up - loss(*args)) / (2 * h)
+        assert np.abs(fd - grad).max() <= 1e-6 * max(1.0, np.abs(grad).max()), which
+
+
+@pytest.mark.parametrize("causal,window,per_batch", [(True, 0, False), (False, 0, True), (True, 9, True)])
+def test_alibi_torch_float64_autograd(causal, window, per_batch):
+    """Against torch autograd of softmax(scale QK^T + B) V with the bias matrix
+    B_ij = -m |i - j| built by torch from broadcast position vectors."""
+    B, N, H, d = 2, 37, 3, 8
+    q, k, v, do = (_rand((B, N, H, d), 400 + t) for t in range(4))
+    slopes = np.array([0.5, 0.0625, 2.0 ** -0.5]) if not per_batch else np.array([[0.5, 0.25, 0.1], [1.0, 0.0, 0.3]])
+    scale = float(np.float32(0.35))
+    O, L, dQ, dK, dV, _ = oracle.reference_grads(q, k, v, do, scale, causal, window, alibi=slopes)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    pos = torch.arange(N, dtype=torch.float64)
+    dist = (pos[:, None] - pos[None, :]).abs()                      # [N, N]
+    m = torch.tensor(slopes if per_batch else np.broadcast_to(slopes, (B, H)).copy())  # [B, H]
+    bias = -m[:, :, None, None] * dist[None, None]                  # [B, H, N, N]
+    s = torch.einsum("bnhd,bmhd->bhnm", tq, tk) * scale + bias
+    ok = torch.tensor(allowed(np.arange(N), N, causal, window))[None, None]
+    s = s.masked_fill(~ok, float("-inf"))
+    out = torch.einsum("bhnm,bmhd->bnhd", torch.softmax(s, dim=-1), tv)
+    out.backward(torch.tensor(do))
+    for a, t in ((O, out.detach()), (dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        t = t.numpy()
+        assert np.linalg.norm(a - t) <= 1e-12 * np.linalg.norm(t)
+    np.testing.assert_allclose(L, torch.logsumexp(s.detach(), dim=-1).numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_alibi_closed_form_zero_queries_causal():
+    """Q = 0 under a causal mask leaves only the bias: P_ij = r^(i-j) (1 - r) / (1 - r^(i+1))
+    with r = exp(-m), and L_i = log((1 - r^(i+1)) / (1 - r))."""
+    N, d, m = 12, 3, 0.7
+    q = np.zeros((1, N, 1, d))
+    k, v = _rand((1, N, 1, d), 500), _rand((1, N, 1, d), 501)
+    O, L = oracle.forward(q, k, v, 1.0, causal=True, alibi=np.array([m]))
+    r = np.exp(-m)
+    for i in range(N):
+        j = np.arange(i + 1)
+        P = r ** (i - j) * (1 - r) / (1 - r ** (i + 1))
+        np.testing.assert_allclose(O[0, i, 0], P @ v[0, : i + 1, 0], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(L[0, 0, i], np.log((1 - r ** (i + 1)) / (1 - r)), rtol=1e-12)
+
+
+def test_alibi_zero_slope_is_plain_attention_and_sign_matters():
+    B, N, H, d = 1, 20, 2, 4
+    q, k, v, do = (_rand((B, N, H, d), 600 + t) for t in range(4))
+    a = oracle.reference_grads(q, k, v, do, 0.5, True)
+    b = oracle.reference_grads(q, k, v, do, 0.5, True, alibi=np.zeros(H))
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    # a positive slope pulls probability toward the diagonal: row i's weight on
+    # key i grows against the unbiased softmax
+    O1, L1 = oracle.forward(q, k, v, 0.5, True)
+    O2, L2 = oracle.forward(q, k, v, 0.5, True, alibi=np.full(H, 0.8))
+    s = 0.5 * np.einsum("bnhd,bnhd->bhn", q, k)  # diagonal scores (bias 0 there)
+    assert np.all(s[:, :, 1:] - L2[:, :, 1:] > s[:, :, 1:] - L1[:, :, 1:])
