@@ -68,10 +68,15 @@ def load_library(path: str = LIB_PATH):
     i64 = ctypes.c_int64
     lib.fa_varlen_bwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.fa_varlen_bwd_workspace_size.restype = sz
-    lib.fa_varlen_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, i64, i64, i, f, i, i, vp]
+    lib.fa_varlen_fwd.argtypes = [vp] * 6 + [i, i, i, i, i, i64, i64, i, f, i, i, vp, i64, vp]
     lib.fa_varlen_fwd.restype = i
-    lib.fa_varlen_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i64, i64, i, f, i, i, i, vp, sz, vp]
+    lib.fa_varlen_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i64, i64, i, f, i, i, vp, i64, i, vp, sz, vp]
     lib.fa_varlen_bwd.restype = i
+    lib.fa_fwd_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, vp]
+    lib.fa_fwd_alibi.restype = i
+    lib.fa_bwd_alibi.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, i, vp, sz,
+                                            vp]
+    lib.fa_bwd_alibi.restype = i
     _lib = lib
     return lib
 
@@ -120,6 +125,19 @@ def _stream(stream):
     return ctypes.c_void_p(int(stream))
 
 
+def _alibi(slopes, lead: int, H: int, device):
+    """(pointer, lead stride) of ALiBi slopes shaped [H] or [lead, H] (fp32 CUDA), or (None, 0)."""
+    if slopes is None:
+        return None, 0
+    if slopes.dtype != torch.float32 or not slopes.is_cuda or slopes.device != device:
+        raise ValueError("alibi_slopes must be a float32 tensor on the tensors' device")
+    if slopes.dim() == 1 and slopes.shape[0] == H and slopes.stride(0) == 1:
+        return slopes.data_ptr(), 0
+    if slopes.dim() == 2 and tuple(slopes.shape) == (lead, H) and slopes.stride(1) == 1:
+        return slopes.data_ptr(), slopes.stride(0)
+    raise ValueError(f"alibi_slopes must be [H] or [{lead}, H] with a contiguous head dimension")
+
+
 def default_scale(d: int) -> float:
     return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
 
@@ -129,15 +147,23 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype, deterministic: 
     return int(load_library().fa_bwd_workspace_size(B, H, N, d, code, int(bool(deterministic))))
 
 
-def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, stream=None):
-    """Forward through the C ABI: fills o ([B,N,H,d]) and lse ([B,H,N] fp32)."""
+def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, stream=None,
+           alibi_slopes=None):
+    """Forward through the C ABI: fills o ([B,N,H,d]) and lse ([B,H,N] fp32).
+
+    ``alibi_slopes`` (fp32 [H] or [B, H]) adds -m|i - j| to the scaled scores (fa_fwd_alibi).
+    """
     (B, N, H, d), st = _same_layout(q, k, v, o)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     lib = load_library()
-    _check(lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, st,
-                      _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal),
-                      int(window), float(dropout_p), int(seed), int(offset), _stream(stream)))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, st,
+            _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
+            float(dropout_p), int(seed), int(offset))
+    if alibi_slopes is None:
+        _check(lib.fa_fwd(*args, _stream(stream)))
+    else:
+        _check(lib.fa_fwd_alibi(*args, *_alibi(alibi_slopes, B, H, q.device), _stream(stream)))
 
 
 def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p, seed, offset, deterministic,
@@ -153,10 +179,18 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
 
 
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, window=0, dropout_p=0.0,
-           seed=0, offset=0, deterministic=True, stream=None):
-    """Backward through the C ABI: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor."""
-    _check(load_library().fa_bwd(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
-                                            seed, offset, deterministic, workspace, stream)))
+           seed=0, offset=0, deterministic=True, stream=None, alibi_slopes=None):
+    """Backward through the C ABI: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor.
+
+    ``alibi_slopes`` as for :func:`fa_fwd` (fa_bwd_alibi)."""
+    a = _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p, seed, offset, deterministic,
+                  workspace, stream)
+    if alibi_slopes is None:
+        _check(load_library().fa_bwd(*a))
+    else:
+        # fa_bwd_alibi takes the slopes before `deterministic`
+        _check(load_library().fa_bwd_alibi(*a[:21], *_alibi(alibi_slopes, q.shape[0], q.shape[2], q.device),
+                                           *a[21:]))
 
 
 def fa_bwd_stage(stage, q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, window=0,
@@ -199,23 +233,24 @@ def alloc_workspace(q: torch.Tensor, deterministic: bool = True) -> torch.Tensor
     return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
 
 
-def attention_forward(q, k, v, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0):
+def attention_forward(q, k, v, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
+                      alibi_slopes=None):
     """Allocate O and L and run the forward; returns (o, lse)."""
     B, N, H, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, scale, causal, window, dropout_p, seed, offset)
+    fa_fwd(q, k, v, o, lse, scale, causal, window, dropout_p, seed, offset, alibi_slopes=alibi_slopes)
     return o, lse
 
 
 def attention_backward(q, k, v, o, do, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
-                       deterministic=True, workspace=None):
+                       deterministic=True, workspace=None, alibi_slopes=None):
     """Allocate dQ, dK, dV (and the workspace unless given) and run the backward."""
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = alloc_workspace(q, deterministic)
     fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, window, dropout_p, seed, offset,
-           deterministic)
+           deterministic, alibi_slopes=alibi_slopes)
     return dq, dk, dv
 
 
@@ -246,18 +281,21 @@ def fa_varlen_bwd_workspace_size(nseq: int, max_seqlen: int, total: int, H: int,
                                                            int(bool(deterministic))))
 
 
-def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0, stream=None):
-    """Forward over packed sequences: fills o ([total, H, d]) and lse ([H, total] fp32)."""
+def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0, stream=None,
+                  alibi_slopes=None):
+    """Forward over packed sequences: fills o ([total, H, d]) and lse ([H, total] fp32).
+
+    ``alibi_slopes``: fp32 [H] or [nseq, H], or None."""
     total, H, d, sn, sh, nseq = _varlen_layout(q, cu_seqlens, k, v, o)
     _varlen_lse_check(lse, H, total)
     _check(load_library().fa_varlen_fwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), cu_seqlens.data_ptr(), nseq,
         int(max_seqlen), total, H, d, sn, sh, _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else
-        float(scale), int(causal), int(window), _stream(stream)))
+        float(scale), int(causal), int(window), *_alibi(alibi_slopes, nseq, H, q.device), _stream(stream)))
 
 
 def fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, workspace, scale=None, causal=False,
-                  window=0, deterministic=True, stream=None):
+                  window=0, deterministic=True, stream=None, alibi_slopes=None):
     """Backward over packed sequences: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor."""
     total, H, d, sn, sh, nseq = _varlen_layout(q, cu_seqlens, k, v, o, do, dq, dk, dv)
     _varlen_lse_check(lse, H, total)
@@ -265,48 +303,49 @@ def fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, works
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(), nseq, int(max_seqlen), total, H, d, sn, sh,
         _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
-        int(bool(deterministic)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        *_alibi(alibi_slopes, nseq, H, q.device), int(bool(deterministic)), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def varlen_attention_forward(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, window=0):
+def varlen_attention_forward(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, window=0,
+                             alibi_slopes=None):
     """Allocate O and L and run the packed forward; returns (o, lse)."""
     total, H, _ = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
-    fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale, causal, window)
+    fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale, causal, window, alibi_slopes=alibi_slopes)
     return o, lse
 
 
 def varlen_attention_backward(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0,
-                              deterministic=True):
+                              deterministic=True, alibi_slopes=None):
     """Allocate dQ, dK, dV and the workspace and run the packed backward."""
     total, H, d = q.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     nbytes = fa_varlen_bwd_workspace_size(cu_seqlens.numel() - 1, max_seqlen, total, H, d, q.dtype, deterministic)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, ws, scale, causal, window,
-                  deterministic)
+                  deterministic, alibi_slopes=alibi_slopes)
     return dq, dk, dv
 
 
 class _FlashAttnFunc(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal, window, dropout_p, seed, offset, deterministic):
-        o, lse = attention_forward(q, k, v, scale, causal, window, dropout_p, seed, offset)
+    def forward(ctx, q, k, v, scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes):
+        o, lse = attention_forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi_slopes)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.cfg = (scale, causal, window, dropout_p, seed, offset, deterministic)
+        ctx.cfg = (scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        scale, causal, window, dropout_p, seed, offset, deterministic = ctx.cfg
+        scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes = ctx.cfg
         if do.stride() != q.stride():
             do = _match_layout(do, q)
         dq, dk, dv = attention_backward(q, k, v, o, do, lse, scale, causal, window, dropout_p, seed, offset,
-                                        deterministic)
-        return dq, dk, dv, None, None, None, None, None, None, None
+                                        deterministic, alibi_slopes=alibi_slopes)
+        return dq, dk, dv, None, None, None, None, None, None, None, None
 
 
 def _match_layout(t: torch.Tensor, ref: torch.Tensor) -> torch.Tensor:
@@ -316,8 +355,11 @@ def _match_layout(t: torch.Tensor, ref: torch.Tensor) -> torch.Tensor:
 
 
 def flash_attn_func(q, k, v, causal=False, window=0, dropout_p=0.0, softmax_scale=None, seed=0, offset=0,
-                    deterministic=True):
-    """Attention on [B, S, H, D] tensors with autograd (forward fa_fwd, backward fa_bwd)."""
+                    deterministic=True, alibi_slopes=None):
+    """Attention on [B, S, H, D] tensors with autograd (forward fa_fwd, backward fa_bwd).
+
+    ``alibi_slopes`` (fp32 [H] or [B, H], not differentiated) adds -m|i - j| to the scaled scores."""
     k = k if k.stride() == q.stride() else _match_layout(k, q)
     v = v if v.stride() == q.stride() else _match_layout(v, q)
-    return _FlashAttnFunc.apply(q, k, v, softmax_scale, causal, window, dropout_p, seed, offset, deterministic)
+    return _FlashAttnFunc.apply(q, k, v, softmax_scale, causal, window, dropout_p, seed, offset, deterministic,
+                                alibi_slopes)

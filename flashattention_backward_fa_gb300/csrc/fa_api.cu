@@ -140,6 +140,17 @@ void fill_params(AttnParams& p, int B, int H, int N, int d, fa_strides s, float 
   p.drop.off_hi = (uint32_t)(offset >> 32);
 }
 
+// ALiBi slopes: fp32, 4-byte aligned, a non-negative batch (or sequence)
+// stride; the kernels fold the bias into the raw scores as m / scale, so the
+// scale must be positive.
+int check_alibi(const float* alibi, int64_t alibi_sb, float scale) {
+  if (!alibi) return FA_OK;
+  if (reinterpret_cast<uintptr_t>(alibi) & 3u) return FA_ERR_ALIGNMENT;
+  if (alibi_sb < 0) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 // Launches one backward stage for fully validated and filled parameters.
@@ -220,12 +231,22 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int det
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
            uint64_t seed, uint64_t offset, void* stream) {
+  return fa_fwd_alibi(q, k, v, o, lse, B, H, N, d, strides, dtype, scale, causal, window, dropout_p, seed, offset,
+                      nullptr, 0, stream);
+}
+
+int fa_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                 uint64_t seed, uint64_t offset, const float* alibi_slopes, int64_t alibi_stride_b, void* stream) {
   int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
+  if ((rc = check_alibi(alibi_slopes, alibi_stride_b, scale))) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  p.alibi = alibi_slopes;
+  p.alibi_sb = alibi_stride_b;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -248,8 +269,41 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
                  fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
                  uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
                  void* stream) {
+  return fa::bwd_stage_run(stage, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal,
+                           window, dropout_p, seed, offset, nullptr, 0, deterministic, workspace, workspace_bytes,
+                           stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+           float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+           int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                     dropout_p, seed, offset, nullptr, 0, deterministic, workspace, workspace_bytes, stream, true);
+}
+
+int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+                 float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+                 const float* alibi_slopes, int64_t alibi_stride_b, int deterministic, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                     dropout_p, seed, offset, alibi_slopes, alibi_stride_b, deterministic, workspace,
+                     workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+namespace fa {
+
+int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, int deterministic,
+                  void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
+  if ((rc = check_alibi(alibi, alibi_sb, scale))) return rc;
   if (stage != FA_BWD_PREPROCESS && stage != FA_BWD_DKDV && stage != FA_BWD_DQ) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
@@ -260,6 +314,8 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
     return FA_ERR_WORKSPACE;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  p.alibi = alibi;
+  p.alibi_sb = alibi_sb;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -277,13 +333,9 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
   return launch_stage(stage, p, dtype, deterministic, stream);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-           void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
-           float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-           int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
-  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, deterministic, workspace, workspace_bytes, stream, true);
-}
+}  // namespace fa
+
+extern "C" {
 
 int fa_get_device_status(unsigned int* status, int clear) {
   if (!status) return FA_ERR_INVALID_ARG;
@@ -333,10 +385,11 @@ namespace fa {
 int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
             float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream) {
+            const float* alibi, int64_t alibi_sb, int deterministic, void* workspace, size_t workspace_bytes,
+            void* stream, bool allow_side_stream) {
   auto stage = [&](fa_bwd_stage_id s, void* st) {
-    return fa_bwd_stage(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                        dropout_p, seed, offset, deterministic, workspace, workspace_bytes, st);
+    return bwd_stage_run(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                         dropout_p, seed, offset, alibi, alibi_sb, deterministic, workspace, workspace_bytes, st);
   };
   return run_backward(stage, deterministic, dtype, allow_side_stream, stream);
 }
@@ -365,7 +418,8 @@ VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int
 
 // Validation and parameters common to the varlen forward and backward.
 int varlen_params(AttnParams& p, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H, int d,
-                  int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window) {
+                  int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window,
+                  const float* alibi, int64_t alibi_ss) {
   if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
   if (nseq < 1 || max_seqlen < 1 || total < 1 || H < 1) return FA_ERR_INVALID_ARG;
@@ -375,7 +429,10 @@ int varlen_params(AttnParams& p, const int* cu_seqlens, int nseq, int max_seqlen
   const fa_strides s = {stride_n, stride_n, stride_h};  // B = 1: the batch stride is never used
   int rc = check_common(1, H, total, d, s, dtype, scale, window, 0.f);
   if (rc) return rc;
+  if ((rc = check_alibi(alibi, alibi_ss, scale))) return rc;
   fill_params(p, 1, H, total, d, s, scale, causal, window, 0.f, 0, 0);
+  p.alibi = alibi;
+  p.alibi_sb = alibi_ss;
   p.cu_seqlens = cu_seqlens;
   p.nseq = nseq;
   p.max_seqlen = max_seqlen;
@@ -396,10 +453,11 @@ size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, 
 
 int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens, int nseq,
                   int max_seqlen, int total, int H, int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype,
-                  float scale, int causal, int window, void* stream) {
+                  float scale, int causal, int window, const float* alibi_slopes, int64_t alibi_stride_seq,
+                  void* stream) {
   AttnParams p;
   int rc = varlen_params(p, cu_seqlens, nseq, max_seqlen, total, H, d, stride_n, stride_h, dtype, scale, causal,
-                         window);
+                         window, alibi_slopes, alibi_stride_seq);
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
@@ -421,10 +479,11 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
 int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H,
                   int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window,
-                  int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+                  const float* alibi_slopes, int64_t alibi_stride_seq, int deterministic, void* workspace,
+                  size_t workspace_bytes, void* stream) {
   AttnParams p;
   int rc = varlen_params(p, cu_seqlens, nseq, max_seqlen, total, H, d, stride_n, stride_h, dtype, scale, causal,
-                         window);
+                         window, alibi_slopes, alibi_stride_seq);
   if (rc) return rc;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};

@@ -12,6 +12,14 @@ namespace fa {
 int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
             float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            int deterministic, void* workspace, size_t workspace_bytes, void* stream, bool allow_side_stream);
+            const float* alibi, int64_t alibi_sb, int deterministic, void* workspace, size_t workspace_bytes,
+            void* stream, bool allow_side_stream);
+
+// One backward stage (fa_bwd_stage with optional ALiBi slopes).
+int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
+                  const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, int deterministic,
+                  void* workspace, size_t workspace_bytes, void* stream);
 
 }  // namespace fa

@@ -51,6 +51,12 @@ struct AttnParams {
   int nseq;
   int max_seqlen;
   int seq_pad;
+  // ALiBi slopes (null: no position bias): the score of (i, j) gains
+  // -m * |i - j| after the scale, m = alibi[seq * alibi_sb + h] with seq the
+  // batch index (or the sequence index of packed input); alibi_sb = 0 shares
+  // one slope per head across the batch.
+  const float* alibi;
+  int64_t alibi_sb;
 };
 
 // One CTA's unit: a tile of rows of one (batch, head), or of one (sequence,
@@ -59,7 +65,7 @@ struct AttnParams {
 // ws its L / D workspace row base, acc its dQ-accumulator row base, lse its
 // base index in L.
 struct Unit {
-  int tile, b, h, bh, row0, n;
+  int tile, b, h, bh, seq, row0, n;
   long long ws, acc, lse;
 };
 
@@ -88,6 +94,7 @@ __device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int ti
     u.bh = unit;
     u.b = u.bh / p.H;
     u.h = u.bh % p.H;
+    u.seq = u.b;
     u.row0 = 0;
     u.n = p.N;
     u.ws = (long long)u.bh * p.n_pad;
@@ -97,6 +104,7 @@ __device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int ti
   }
   const int sq = unit / p.H;
   u.h = unit % p.H;
+  u.seq = sq;
   u.b = 0;
   u.bh = u.h;
   // Clamp the offsets into [0, N] and the length to max_seqlen, so that a
@@ -108,6 +116,23 @@ __device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int ti
   u.acc = (long long)u.h * p.n_pad + s0;
   u.lse = (long long)u.h * p.N + s0;
   return u.tile * tile_rows < u.n;
+}
+
+// ALiBi slope of a unit in score units: m / scale, so that the bias folds into
+// the raw scores S = Q.K before the kernels' scale * log2(e) (the host requires
+// scale > 0 with ALiBi).
+__device__ __forceinline__ float alibi_slope_raw(const AttnParams& p, const Unit& u) {
+  return __ldg(p.alibi + (long long)u.seq * p.alibi_sb + u.h) / p.scale;
+}
+
+// ALiBi on 16 raw scores of one TMEM row: s_e -= slope_raw * |d0 + kSign * e|,
+// where d0 + kSign * e is i - j of column e (query-major rows: d0 = i - j_first,
+// kSign = -1; key-major rows: d0 = i_first - j, kSign = +1).
+template <int kSign>
+__device__ __forceinline__ void alibi_fold16(uint32_t (&sr)[16], float d0, float slope_raw) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    sr[e] = __float_as_uint(fmaf(-slope_raw, fabsf(d0 + (float)(kSign * e)), __uint_as_float(sr[e])));
 }
 
 // Allowed (query i, key j) pair under the causal / sliding-window mask.

@@ -245,6 +245,12 @@ __device__ __forceinline__ float dot_row(const float* __restrict__ a_smem, const
   return acc;
 }
 
+// ALiBi slope of (batch b, head h) in the log2 domain (0 without ALiBi): the
+// score of (i, j) gains -m * |i - j| after the scale.
+__device__ __forceinline__ float alibi_slope_log2(const AttnParams& p, int b, int h) {
+  return p.alibi ? __ldg(p.alibi + (long long)b * p.alibi_sb + h) * kLog2e : 0.f;
+}
+
 // Forward, one warp per query row: pass 1 row max and sum of exp2 (lanes take
 // keys lane, lane+32, ...), pass 2 O = sum_j P~_ij V_j with lanes owning head
 // dimensions and P broadcast by shuffles.
@@ -259,9 +265,10 @@ __global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_co
   __syncwarp();
   const int jlo = p.window > 0 ? max(0, i - p.window + 1) : 0;
   const int jhi = p.causal ? i : p.N - 1;
+  const float am = alibi_slope_log2(p, b, h);
   float m = -INFINITY, l = 0.f;
   for (int j = jlo + lane; j <= jhi; j += 32) {
-    const float x = dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2;
+    const float x = fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2);
     const float mn = fmaxf(m, x);
     l = l * ex2_approx(m - mn) + ex2_approx(x - mn);
     m = mn;
@@ -283,7 +290,8 @@ __global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_co
     const int j = jb + lane;
     float pj = 0.f;
     if (j <= jhi) {
-      pj = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 - L2);
+      pj = ex2_approx(fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) -
+                      L2);
       if (p.drop.threshold) pj = dropout_keep(p.drop, bh, p.N, i, j) ? pj * p.drop.rp : 0.f;
     }
     const int cnt = min(32, jhi - jb + 1);
@@ -326,12 +334,14 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __gr
   const int ihi = p.window > 0 ? min(p.N - 1, j + p.window - 1) : p.N - 1;
   const float* nL2 = p.ws_nL2 + (long long)bh * p.n_pad;
   const float* nD = p.ws_nD + (long long)bh * p.n_pad;
+  const float am = alibi_slope_log2(p, b, h);
   float dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
   for (int ib = ilo; ib <= ihi; ib += 32) {
     const int i = ib + lane;
     float pt = 0.f, ds = 0.f;
     if (i <= ihi) {
-      const float pv = ex2_approx(dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2 + nL2[i]);
+      const float pv = ex2_approx(
+          fmaf(-am, fabsf((float)(i - j)), dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2) + nL2[i]);
       float dp = dot_row(vrow[w], row_ptr(p, p.dout, b, i, h), p.d);
       pt = pv;
       if (p.drop.threshold) {
@@ -386,12 +396,14 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid
   const int jhi = p.causal ? i : p.N - 1;
   const float nL2 = p.ws_nL2[(long long)bh * p.n_pad + i];
   const float nD = p.ws_nD[(long long)bh * p.n_pad + i];
+  const float am = alibi_slope_log2(p, b, h);
   float dq[4] = {0.f, 0.f, 0.f, 0.f};
   for (int jb = jlo; jb <= jhi; jb += 32) {
     const int j = jb + lane;
     float ds = 0.f;
     if (j <= jhi) {
-      const float pv = ex2_approx(dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2 + nL2);
+      const float pv = ex2_approx(
+          fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) + nL2);
       float dp = dot_row(grow[w], row_ptr(p, p.v, b, j, h), p.d);
       if (p.drop.threshold) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
       ds = pv * (dp + nD);

@@ -94,7 +94,7 @@ __device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row,
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop>
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi>
 __global__ void __launch_bounds__(kKVThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tSc = tS + lane_off + 64 * bb + 32 * c, tdPc = tdP + lane_off + 64 * bb + 32 * c;
     const uint32_t imgRow = sb + C::oImg + 2 * bb * C::kPTile + jl * 128;
+    const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
     bool ok = true;
     for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         __syncwarp();  // per-lane branches above: converge for the TMEM load
         tmem_ld16(tSc + 16 * hh, sr);
         tmem_ld_wait16(sr);
+        if constexpr (kAlibi) alibi_fold16<1>(sr, (float)(base + 16 * hh - j), slope_raw);
         float cmax = 0.f;
         float pt[16];
         // P = exp2(S * scale*log2e + (-L*log2e)) on pairs of columns; the unmasked
@@ -548,10 +550,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop>
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi>
 static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   using C = KVCfg<D, kAtomic>;
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop>;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop, kAlibi>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -562,12 +564,19 @@ static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, c
   return cudaGetLastError();
 }
 
+template <int D, bool kBf16, bool kAtomic>
+static cudaError_t launch_dkdv_a(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+  const bool drop = p.drop.threshold != 0;
+  if (p.alibi)
+    return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true>(p, maps, st)
+                : launch_dkdv_t<D, kBf16, kAtomic, false, true>(p, maps, st);
+  return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, false>(p, maps, st)
+              : launch_dkdv_t<D, kBf16, kAtomic, false, false>(p, maps, st);
+}
+
 template <int D, bool kBf16>
 static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, const CUtensorMap* maps, cudaStream_t st) {
-  const bool drop = p.drop.threshold != 0;
-  if (atomic)
-    return drop ? launch_dkdv_t<D, kBf16, true, true>(p, maps, st) : launch_dkdv_t<D, kBf16, true, false>(p, maps, st);
-  return drop ? launch_dkdv_t<D, kBf16, false, true>(p, maps, st) : launch_dkdv_t<D, kBf16, false, false>(p, maps, st);
+  return atomic ? launch_dkdv_a<D, kBf16, true>(p, maps, st) : launch_dkdv_a<D, kBf16, false>(p, maps, st);
 }
 
 // maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows).

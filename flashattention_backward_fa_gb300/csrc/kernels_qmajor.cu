@@ -104,7 +104,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
-template <int D, bool kBf16, int kMode, bool kDrop>
+template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi>
 __global__ void __launch_bounds__(kQThreads, 1)
     qmajor_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       nL2 = p.ws_nL2[ws];
       nD = p.ws_nD[ws];
     }
+    const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
     float mref = -INFINITY, lsum = 0.f;
     float* xchg = reinterpret_cast<float*>(smem + C::oStats);
     bool ok = true;
@@ -384,9 +385,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld_wait16x3(sr2[0], dr2[0], dr2[1]);
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty));
+        if constexpr (kAlibi) alibi_fold16<-1>(sr2[0], (float)(i - base), slope_raw);
       } else {
         tmem_ld16(tSc + 16, sr2[1]);
         tmem_ld_wait16x2(sr2[0], sr2[1]);
+        if constexpr (kAlibi) {
+          alibi_fold16<-1>(sr2[0], (float)(i - base), slope_raw);
+          alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
+        }
       }
       bool resc = false;
       float alpha = 1.f;
@@ -437,6 +443,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           __syncwarp();
           tmem_ld16(tSc + 16, sr2[1]);
           tmem_ld_wait16(sr2[1]);
+          if constexpr (kAlibi) alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
         }
         const uint32_t (&sr)[16] = sr2[hh];
         const uint32_t (&dr)[16] = dr2[hh];
@@ -602,10 +609,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode, bool kDrop>
+template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi>
 static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   using C = QCfg<D, kMode>;
-  auto kern = qmajor_kernel<D, kBf16, kMode, kDrop>;
+  auto kern = qmajor_kernel<D, kBf16, kMode, kDrop, kAlibi>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -616,12 +623,19 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
   return cudaGetLastError();
 }
 
+template <int D, bool kBf16, int kMode>
+static cudaError_t launch_q_m(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+  const bool drop = p.drop.threshold != 0;
+  if (p.alibi)
+    return drop ? launch_q_t<D, kBf16, kMode, true, true>(p, maps, st)
+                : launch_q_t<D, kBf16, kMode, false, true>(p, maps, st);
+  return drop ? launch_q_t<D, kBf16, kMode, true, false>(p, maps, st)
+              : launch_q_t<D, kBf16, kMode, false, false>(p, maps, st);
+}
+
 template <int D, bool kBf16>
 static cudaError_t launch_q_d(const AttnParams& p, bool dq_mode, const CUtensorMap* maps, cudaStream_t st) {
-  const bool drop = p.drop.threshold != 0;
-  if (dq_mode)
-    return drop ? launch_q_t<D, kBf16, kModeDq, true>(p, maps, st) : launch_q_t<D, kBf16, kModeDq, false>(p, maps, st);
-  return drop ? launch_q_t<D, kBf16, kModeFwd, true>(p, maps, st) : launch_q_t<D, kBf16, kModeFwd, false>(p, maps, st);
+  return dq_mode ? launch_q_m<D, kBf16, kModeDq>(p, maps, st) : launch_q_m<D, kBf16, kModeFwd>(p, maps, st);
 }
 
 // maps: Q, K, V, dO (Q/dO boxes of kRowsQ rows, K/V boxes of kStepKV rows).

@@ -140,6 +140,27 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    uint64_t seed, uint64_t offset, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ALiBi position bias ("Lecture 7 — Backward Pass and Validation", §Use it in
+ * the real stack, names ALiBi among the cases a complete harness covers; the
+ * pages give no formula, so the usual linear bias is taken): the score of
+ * query i and key j becomes scale * q_i.k_j - m * |i - j| before the mask and
+ * the softmax, with m = alibi_slopes[b * alibi_stride_b + h] (fp32, device
+ * memory, 4-byte aligned; alibi_stride_b = 0 shares one slope per head across
+ * the batch, H otherwise for a [B, H] array). The slopes are constants: the
+ * gradients keep their form with the biased P. Requires scale > 0
+ * (FA_ERR_UNSUPPORTED otherwise); a null alibi_slopes is plain attention.
+ * Every other argument, layout and error as fa_fwd / fa_bwd.
+ * ------------------------------------------------------------------------- */
+int fa_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                 uint64_t seed, uint64_t offset, const float* alibi_slopes, int64_t alibi_stride_b, void* stream);
+int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+                 float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+                 const float* alibi_slopes, int64_t alibi_stride_b, int deterministic, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Packed variable-length sequences ("Lecture 7 — Backward Pass and
  * Validation", §Use it in the real stack, lists varlen among the cases a
  * complete harness covers; the math per sequence is that of fa_fwd / fa_bwd).
@@ -155,6 +176,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  * stride_n / stride_h are element strides of the packed tensors (d stride 1,
  * multiples of 8). lse is contiguous fp32 [H, total]. 16-bit dtypes, d in
  * {64, 128}, nseq * H <= 65535, no dropout (dropout_p is not an argument).
+ * Optional ALiBi slopes as for fa_fwd_alibi, indexed by sequence:
+ * m = alibi_slopes[s * alibi_stride_seq + h] (null: no bias).
  * Errors as fa_fwd / fa_bwd; the caller owns every buffer.
  * ------------------------------------------------------------------------- */
 size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, int d, fa_dtype dtype,
@@ -162,14 +185,16 @@ size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, 
 /* Forward: O [total, H, d] and lse [H, total] per sequence. */
 int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens, int nseq,
                   int max_seqlen, int total, int H, int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype,
-                  float scale, int causal, int window, void* stream);
+                  float scale, int causal, int window, const float* alibi_slopes, int64_t alibi_stride_seq,
+                  void* stream);
 /* Backward: dQ, dK, dV [total, H, d] per sequence; deterministic and atomic dQ
  * as fa_bwd; workspace of fa_varlen_bwd_workspace_size(...) bytes, 256-byte
  * aligned. */
 int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, const int* cu_seqlens, int nseq, int max_seqlen, int total, int H,
                   int d, int64_t stride_n, int64_t stride_h, fa_dtype dtype, float scale, int causal, int window,
-                  int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+                  const float* alibi_slopes, int64_t alibi_stride_seq, int deterministic, void* workspace,
+                  size_t workspace_bytes, void* stream);
 
 /* Reads (and with clear != 0 resets) the status word of the current device.
  * Call after synchronising the streams the kernels ran on. *status receives

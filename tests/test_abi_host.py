@@ -111,14 +111,17 @@ def test_bwd_rejects_bad_arguments(lib):
     assert _bwd(lib, stage=1, d=80) == EUNSUP
 
 
-def _vfwd(lib, *, q=P, cu=P, nseq=3, msl=300, total=700, H=2, d=128, sn=256, sh=128, dt=BF16, window=0):
-    return lib.fa_varlen_fwd(q, P, P, P, P, cu, nseq, msl, total, H, d, sn, sh, dt, 0.1, 1, window, None)
+def _vfwd(lib, *, q=P, cu=P, nseq=3, msl=300, total=700, H=2, d=128, sn=256, sh=128, dt=BF16, window=0,
+          alibi=None, alibi_ss=0, scale=0.1):
+    return lib.fa_varlen_fwd(q, P, P, P, P, cu, nseq, msl, total, H, d, sn, sh, dt, scale, 1, window, alibi,
+                             alibi_ss, None)
 
 
 def _vbwd(lib, *, ptrs=None, cu=P, nseq=3, msl=300, total=700, H=2, d=128, dt=BF16, det=1, ws=0x100000,
           ws_bytes=1 << 30):
     ptrs = ptrs or [P] * 9
-    return lib.fa_varlen_bwd(*ptrs, cu, nseq, msl, total, H, d, H * d, d, dt, 0.1, 1, 0, det, ws, ws_bytes, None)
+    return lib.fa_varlen_bwd(*ptrs, cu, nseq, msl, total, H, d, H * d, d, dt, 0.1, 1, 0, None, 0, det, ws,
+                             ws_bytes, None)
 
 
 def test_varlen_rejects_bad_arguments(lib):
@@ -140,6 +143,29 @@ def test_varlen_rejects_bad_arguments(lib):
     assert _vbwd(lib, ws_bytes=need - 1) == EWS
     need_atomic = fa.fa_varlen_bwd_workspace_size(3, 300, 700, 2, 128, BF16, False)
     assert _vbwd(lib, det=0, ws_bytes=need) == EWS and need_atomic > need
+
+
+def test_alibi_rejects_bad_arguments(lib):
+    st = _strides(64, 2, 128)
+
+    def fwd(alibi=P, sb=0, scale=0.1, B=1, d=128):
+        a = [P] * 5 + [B, 2, 64, d, st, BF16]
+        return lib.fa_fwd_alibi(*a, scale, 1, 0, 0.0, 0, 0, alibi, sb, None)
+    assert fwd(alibi=P + 2) == EALIGN          # fp32 slopes, 4-byte aligned
+    assert fwd(sb=-1) == EINVAL
+    assert fwd(scale=0.0) == EUNSUP            # the bias folds in as m / scale
+    assert fwd(scale=-0.5) == EUNSUP
+    assert fwd(d=96) == EUNSUP                 # the common checks still apply
+    assert fwd(B=0) == EINVAL
+    assert _vfwd(lib, alibi=P + 1) == EALIGN
+    assert _vfwd(lib, alibi=P, scale=0.0) == EUNSUP
+
+    def bwd(alibi=P, sb=0, scale=0.1, ws=0x100000, ws_bytes=1 << 30):
+        return lib.fa_bwd_alibi(*([P] * 9), 1, 2, 64, 128, st, BF16, scale, 1, 0, 0.0, 0, 0, alibi, sb, 1, ws,
+                                ws_bytes, None)
+    assert bwd(alibi=P + 2) == EALIGN
+    assert bwd(scale=0.0) == EUNSUP
+    assert bwd(ws=0) == EWS
 
 
 def test_varlen_workspace_size(lib):
