@@ -135,6 +135,14 @@ __device__ __forceinline__ void alibi_fold16(uint32_t (&sr)[16], float d0, float
     sr[e] = __float_as_uint(fmaf(-slope_raw, fabsf(d0 + (float)(kSign * e)), __uint_as_float(sr[e])));
 }
 
+// ALiBi ramp on 16 raw scores: s_e += slope * (kX0 + e), kX0 the chunk column
+// of e = 0 (one FMA with an immediate a score).
+template <int kX0>
+__device__ __forceinline__ void alibi_ramp16(uint32_t (&sr)[16], float slope) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) sr[e] = __float_as_uint(fmaf(slope, (float)(kX0 + e), __uint_as_float(sr[e])));
+}
+
 // Allowed (query i, key j) pair under the causal / sliding-window mask.
 __device__ __forceinline__ bool pair_allowed(const AttnParams& p, int i, int j) {
   return j < p.N && i < p.N && (!p.causal || j <= i) && (p.window <= 0 || j > i - p.window);

@@ -133,6 +133,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // One pass over the key blocks in both modes.
   const int nsteps = nkv;
   const int first_out = 0;
+  // Key block of step it. Ascending, except in the ALiBi forward: there the
+  // blocks go outward from the one holding this tile's diagonal (nearest first,
+  // alternating below and above), so that every row meets its largest biased
+  // scores early and the online softmax's reference rarely has to move.
+  auto key_block = [&](int it) -> int {
+    if constexpr (kAlibi && !kDq) {
+      const int g = min(max((i0 - j_first) / kStepKV, 0), nkv - 1);
+      const int below = g, above = nkv - 1 - g, m = min(below, above);
+      int t;
+      if (it == 0) t = g;
+      else if (it <= 2 * m) t = (it & 1) ? g - (it + 1) / 2 : g + it / 2;
+      else t = below > above ? g - (it - m) : g + (it - m);
+      return j_first + t * kStepKV;
+    } else {
+      return j_first + it * kStepKV;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bRes), 1);
@@ -190,8 +207,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int issuedE = 0, issuedL = 0;
       bool ok = true;
       for (int it = 0; ok && it < nsteps; ++it) {
-        const int jt = it >= nkv ? it - nkv : it;
-        const int jj = j_first + jt * kStepKV;
+        const int jj = key_block(it);
         const int se = it % C::kNE;
         if (!mbar_wait(bar(C::bEEmpty + se), ((it / C::kNE) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(bar(C::bEFull + se), C::kTile);
@@ -359,7 +375,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     bool ok = true;
     for (int it = 0; it < nsteps; ++it) {
       const int bb = it % C::kSBuf, xb = it & 1;
-      const int base = j_first + it * kStepKV + 32 * c;
+      const int base = key_block(it) + 32 * c;
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
       if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it / C::kSBuf) & 1, abort_flag, p.status)) {
         ok = false;
@@ -385,14 +401,37 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld_wait16x3(sr2[0], dr2[0], dr2[1]);
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty));
-        if constexpr (kAlibi) alibi_fold16<-1>(sr2[0], (float)(i - base), slope_raw);
       } else {
         tmem_ld16(tSc + 16, sr2[1]);
         tmem_ld_wait16x2(sr2[0], sr2[1]);
-        if constexpr (kAlibi) {
-          alibi_fold16<-1>(sr2[0], (float)(i - base), slope_raw);
-          alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
+      }
+      // ALiBi: where every allowed key of this chunk lies on one side of the
+      // diagonal (always under a causal mask), the bias -m|i - j| is a row
+      // constant plus a ramp over the chunk's columns: the ramp goes into the
+      // raw scores (one FMA a score) and the constant, rc2 (log2 domain), into
+      // the exp2 addend. A chunk that straddles the diagonal folds |i - j| in.
+      float rc2 = 0.f, ramp = 0.f;
+      bool straddle = false;
+      if constexpr (kAlibi) {
+        const int dd = i - base;  // i - j of the chunk's column 0
+        if (p.causal || dd >= 31) {
+          ramp = slope_raw;
+          rc2 = -slope_raw * (float)dd * p.scale_log2;
+        } else if (dd <= 0) {
+          ramp = -slope_raw;
+          rc2 = slope_raw * (float)dd * p.scale_log2;
+        } else {
+          straddle = true;
         }
+        auto fold = [&](auto half) {
+          constexpr int hx = decltype(half)::value;
+          if (straddle)
+            alibi_fold16<-1>(sr2[hx], (float)(dd - 16 * hx), slope_raw);
+          else
+            alibi_ramp16<16 * hx>(sr2[hx], ramp);
+        };
+        fold(std::integral_constant<int, 0>{});
+        if constexpr (!kDq) fold(std::integral_constant<int, 1>{});
       }
       bool resc = false;
       float alpha = 1.f;
@@ -416,6 +455,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             for (int e = 0; e < 16; ++e)
               cm = ((allow >> (16 * hh + e)) & 1u) ? fmaxf(cm, __uint_as_float(sr2[hh][e]) * p.scale_log2) : cm;
         }
+        if constexpr (kAlibi) cm += rc2;  // -inf stays -inf
         xchg[(xb * 4 + c) * kRowsQ + il] = cm;
         warp_arrive(bar(C::bXchg + xb));
         if (!warp_wait<kRowMathPoll>(bar(C::bXchg + xb), (it >> 1) & 1, abort_flag, p.status)) {
@@ -436,6 +476,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         nL2 = -mref;  // P = exp2(S*scale*log2e + (-mref)); +inf only where every key so far is masked
       }
+      const float nL2c = kAlibi ? nL2 + rc2 : nL2;  // the exp2 addend of this chunk
       bool lo_any = false;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -443,7 +484,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
           __syncwarp();
           tmem_ld16(tSc + 16, sr2[1]);
           tmem_ld_wait16(sr2[1]);
-          if constexpr (kAlibi) alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
+          if constexpr (kAlibi) {
+            if (straddle)
+              alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
+            else
+              alibi_ramp16<16>(sr2[1], ramp);
+          }
         }
         const uint32_t (&sr)[16] = sr2[hh];
         const uint32_t (&dr)[16] = dr2[hh];
@@ -453,7 +499,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         auto elementwise = [&](auto masked) {
           if constexpr (!kDrop) {
             // pairs of columns through the packed FMA / add / multiply
-            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), l2 = f2_pack(nL2, nL2);
+            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2), l2 = f2_pack(nL2c, nL2c);
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
               float p0, p1;
@@ -478,7 +524,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const int bit = 16 * hh + e;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, nL2));
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[e]), p.scale_log2, nL2c));
               if constexpr (decltype(masked)::value) pv = ((allow >> bit) & 1u) ? pv : 0.f;
               cmax = fmaxf(cmax, pv);
               const bool kept = (keep >> bit) & 1u;

@@ -98,7 +98,10 @@ def test_alibi_long_sequence_steep_slopes(dtype, d):
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 64)])
 def test_alibi_zero_slopes_bit_identical_to_plain(dtype, d):
-    """fma(-0, |i - j|, s) = s exactly: zero slopes must reproduce the plain kernels bit for bit."""
+    """Zero slopes add exact zeros to every score, so the backward kernels (and the
+    fp32 forward) reproduce the plain ones bit for bit. The 16-bit ALiBi forward
+    visits key blocks outward from the diagonal instead of in ascending order, so
+    its O and L agree with the plain forward up to summation order."""
     w = Workload("alibi0", 2, 2, 321, d, dtype, causal=True, input_seed=3)
     q, k, v, do = (t.cuda() for t in make_inputs(w))
     z = torch.zeros(2, dtype=torch.float32, device="cuda")
@@ -107,7 +110,11 @@ def test_alibi_zero_slopes_bit_identical_to_plain(dtype, d):
     g1 = fa.attention_backward(q, k, v, o1, do, l1, causal=True)
     g2 = fa.attention_backward(q, k, v, o1, do, l1, causal=True, alibi_slopes=z)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    if dtype == "f32":
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    else:
+        assert torch.allclose(o1.float(), o2.float(), rtol=8e-3, atol=1e-3)
+        assert torch.allclose(l1, l2, rtol=0, atol=1e-5)
     for a, b in zip(g1, g2):
         assert torch.equal(a, b)
 
