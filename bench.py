@@ -61,7 +61,8 @@ def dkdv_traffic(w, deterministic: bool):
     with open(path) as f:
         rec = json.load(f)
     csrc = os.path.join(ROOT, "flashattention_backward_fa_gb300", "csrc")
-    src = b"".join(open(os.path.join(csrc, n), "rb").read() for n in ("kernels_bwd_kv.cu", "device_common.cuh"))
+    src = b"".join(open(os.path.join(csrc, n), "rb").read()
+                   for n in ("kernels_bwd_kv.cu", "device_common.cuh", "fa_internal.h"))
     if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
         return None
     return rec["dram_bytes_per_launch_capture"] * (w.B * w.H) / rec["heads_in_capture"]
