@@ -72,6 +72,10 @@ def load_library(path: str = LIB_PATH):
     lib.fa_varlen_fwd.restype = i
     lib.fa_varlen_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, i64, i64, i, f, i, i, vp, i64, i, vp, sz, vp]
     lib.fa_varlen_bwd.restype = i
+    lib.fa_bwd_host_buffer_size.argtypes = [i, i, i, i, i, i]
+    lib.fa_bwd_host_buffer_size.restype = sz
+    lib.fa_bwd_host.argtypes = bwd_args
+    lib.fa_bwd_host.restype = i
     lib.fa_fwd_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, vp]
     lib.fa_fwd_alibi.restype = i
     lib.fa_bwd_alibi.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, i, vp, sz,
@@ -216,6 +220,40 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale=None, causal=False, wi
         dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
         default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p), int(seed),
         int(offset), _stream(stream)))
+
+
+def _host_layout(ref: torch.Tensor, *others: torch.Tensor):
+    if ref.dim() != 4 or ref.is_cuda or ref.stride(3) != 1:
+        raise ValueError("host tensors are CPU [B, N, H, d] with a contiguous head dimension")
+    for o in others:
+        if o.is_cuda or tuple(o.shape) != tuple(ref.shape) or o.stride() != ref.stride() or o.dtype != ref.dtype:
+            raise ValueError("all host [B, N, H, d] tensors must share shape, strides and dtype")
+    B, N, H, d = ref.shape
+    return (B, N, H, d), FaStrides(ref.stride(0), ref.stride(1), ref.stride(2))
+
+
+def fa_bwd_host_buffer_size(B: int, H: int, N: int, d: int, dtype, deterministic: bool = True) -> int:
+    code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().fa_bwd_host_buffer_size(B, H, N, d, code, int(bool(deterministic))))
+
+
+def fa_bwd_host(q, k, v, o, do, lse, dq, dk, dv, dev_buf, scale=None, causal=False, window=0, dropout_p=0.0,
+                seed=0, offset=0, deterministic=True, stream=None):
+    """Backward from host (CPU) tensors through fa_bwd_host: uploads, computes and downloads
+    on ``stream`` with the copies overlapped; pin the host tensors for that overlap.
+    ``dev_buf`` is a uint8 CUDA tensor of fa_bwd_host_buffer_size(...) bytes. The outputs
+    are ready once the stream has completed the work."""
+    (B, N, H, d), st = _host_layout(q, k, v, o, do, dq, dk, dv)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() or lse.is_cuda:
+        raise ValueError("lse must be a contiguous float32 CPU [B, H, N] tensor")
+    if not dev_buf.is_cuda:
+        raise ValueError("dev_buf must be device memory")
+    _check(load_library().fa_bwd_host(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+        dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
+        default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p), int(seed),
+        int(offset), int(bool(deterministic)), dev_buf.data_ptr(), dev_buf.numel() * dev_buf.element_size(),
+        _stream(stream)))
 
 
 def fa_get_device_status(clear: bool = True) -> int:

@@ -541,13 +541,15 @@ struct DropoutParams {
   uint32_t threshold;  // keep iff word >= threshold; 0 disables dropout
   float rp;            // 1 / (1 - p)
   uint32_t seed_lo, seed_hi, off_lo, off_hi;
+  uint32_t bh_off;     // added to the launch's (batch * H + head) index: a launch over a
+                       // slice of the heads or batches draws the full problem's masks
 };
 
 // Keep decision for element (bh, i, j) of an N x N head: word (j mod 4) of
 // Philox at counter (g, offset), g = (bh * N + i) * ceil(N/4) + j/4.
 __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t bh, int N, int i, int j) {
   const uint64_t n4 = (uint64_t)((N + 3) >> 2);
-  const uint64_t g = ((uint64_t)bh * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j >> 2);
+  const uint64_t g = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j >> 2);
   const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi),
                                 dp.seed_lo, dp.seed_hi);
   const uint32_t sel = (j & 3) == 0 ? w.x : (j & 3) == 1 ? w.y : (j & 3) == 2 ? w.z : w.w;
@@ -563,7 +565,7 @@ __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t b
 static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
   const int lane = threadIdx.x & 31, r = lane & 3;
   const uint64_t n4 = (uint64_t)((N + 3) >> 2);
-  const uint64_t row0 = (uint64_t)bh * (uint64_t)N;
+  const uint64_t row0 = (uint64_t)(bh + dp.bh_off) * (uint64_t)N;
   uint32_t mine = 0;  // nibble t: keep bits of the group's four keys for query i0 + 4t + r
 #pragma unroll 1
   for (int t = 0; t < 8; ++t) {
@@ -588,7 +590,7 @@ static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp
 // so each Philox call yields the words of four keys.
 static __device__ __noinline__ uint32_t keep_bits_for_query(const DropoutParams dp, uint32_t bh, int N, int i, int j0) {
   const uint64_t n4 = (uint64_t)((N + 3) >> 2);
-  const uint64_t g0 = ((uint64_t)bh * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j0 >> 2);
+  const uint64_t g0 = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j0 >> 2);
   uint32_t bits = 0;
 #pragma unroll 1
   for (int x = 0; x < 32; x += 4) {

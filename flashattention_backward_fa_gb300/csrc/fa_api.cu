@@ -270,8 +270,8 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
                  uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
                  void* stream) {
   return fa::bwd_stage_run(stage, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal,
-                           window, dropout_p, seed, offset, nullptr, 0, deterministic, workspace, workspace_bytes,
-                           stream);
+                           window, dropout_p, seed, offset, nullptr, 0, 0, deterministic, workspace,
+                           workspace_bytes, stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -279,7 +279,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
            int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, nullptr, 0, deterministic, workspace, workspace_bytes, stream, true);
+                     dropout_p, seed, offset, nullptr, 0, 0, deterministic, workspace, workspace_bytes, stream, true);
 }
 
 int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -288,7 +288,7 @@ int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, con
                  const float* alibi_slopes, int64_t alibi_stride_b, int deterministic, void* workspace,
                  size_t workspace_bytes, void* stream) {
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, alibi_slopes, alibi_stride_b, deterministic, workspace,
+                     dropout_p, seed, offset, alibi_slopes, alibi_stride_b, 0, deterministic, workspace,
                      workspace_bytes, stream, true);
 }
 
@@ -299,8 +299,8 @@ namespace fa {
 int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
-                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, int deterministic,
-                  void* workspace, size_t workspace_bytes, void* stream) {
+                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off,
+                  int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
   if ((rc = check_alibi(alibi, alibi_sb, scale))) return rc;
@@ -314,6 +314,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
     return FA_ERR_WORKSPACE;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  p.drop.bh_off = philox_bh_off;
   p.alibi = alibi;
   p.alibi_sb = alibi_sb;
   p.q = q;
@@ -331,6 +332,11 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
   if ((rc = status_ptr(&p.status))) return rc;
   return launch_stage(stage, p, dtype, deterministic, stream);
+}
+
+int check_bwd_args(int B, int H, int N, int d, fa_strides strides, fa_dtype dtype, float scale, int window,
+                   float dropout_p) {
+  return check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
 }
 
 }  // namespace fa
@@ -385,11 +391,12 @@ namespace fa {
 int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
             float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            const float* alibi, int64_t alibi_sb, int deterministic, void* workspace, size_t workspace_bytes,
-            void* stream, bool allow_side_stream) {
+            const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off, int deterministic, void* workspace,
+            size_t workspace_bytes, void* stream, bool allow_side_stream) {
   auto stage = [&](fa_bwd_stage_id s, void* st) {
     return bwd_stage_run(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                         dropout_p, seed, offset, alibi, alibi_sb, deterministic, workspace, workspace_bytes, st);
+                         dropout_p, seed, offset, alibi, alibi_sb, philox_bh_off, deterministic, workspace,
+                         workspace_bytes, st);
   };
   return run_backward(stage, deterministic, dtype, allow_side_stream, stream);
 }

@@ -12,14 +12,20 @@ namespace fa {
 int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
             float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            const float* alibi, int64_t alibi_sb, int deterministic, void* workspace, size_t workspace_bytes,
-            void* stream, bool allow_side_stream);
+            const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off, int deterministic, void* workspace,
+            size_t workspace_bytes, void* stream, bool allow_side_stream);
 
-// One backward stage (fa_bwd_stage with optional ALiBi slopes).
+// One backward stage (fa_bwd_stage with optional ALiBi slopes). philox_bh_off is
+// added to every (batch * H + head) index that keys a dropout mask, so a call on
+// a slice of the heads (B = 1) or of the batch draws the whole problem's masks.
 int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
-                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, int deterministic,
-                  void* workspace, size_t workspace_bytes, void* stream);
+                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off,
+                  int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+// The shape, dtype, stride and scalar checks every entry point applies.
+int check_bwd_args(int B, int H, int N, int d, fa_strides strides, fa_dtype dtype, float scale, int window,
+                   float dropout_p);
 
 }  // namespace fa

@@ -140,6 +140,30 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    uint64_t seed, uint64_t offset, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Backward from host buffers: fa_bwd with Q, K, V, O, dO, L and dQ, dK, dV in
+ * HOST memory (same shapes, strides, dtypes and scalars as fa_bwd; L
+ * contiguous fp32 [B, H, N]). The call uploads the inputs into a caller-owned
+ * device staging buffer, runs the backward there and downloads the gradients,
+ * all enqueued on `stream` and asynchronous to the host: the host buffers must
+ * stay valid, and the outputs are ready, once `stream` has completed the work.
+ * The problem is cut into up to four groups (of heads when B = 1, of batch
+ * entries otherwise) so that the upload of one group, the backward of the
+ * previous one and the download of the one before run at the same time on
+ * two library-owned copy streams and `stream`. Page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister) is needed for that overlap; pageable
+ * memory is accepted, with copies that then synchronise with the host.
+ * dev_buf: device memory of fa_bwd_host_buffer_size(...) bytes, 256-byte
+ * aligned, owned by the caller; its contents after the call are unspecified.
+ * Results equal fa_bwd's bit for bit in deterministic mode (dropout masks
+ * included). Errors as fa_bwd (FA_ERR_WORKSPACE for dev_buf).
+ * ------------------------------------------------------------------------- */
+size_t fa_bwd_host_buffer_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic);
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+                float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+                int deterministic, void* dev_buf, size_t dev_buf_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * ALiBi position bias ("Lecture 7 — Backward Pass and Validation", §Use it in
  * the real stack, names ALiBi among the cases a complete harness covers; the
  * pages give no formula, so the usual linear bias is taken): the score of

@@ -168,6 +168,26 @@ def test_alibi_rejects_bad_arguments(lib):
     assert bwd(ws=0) == EWS
 
 
+def test_host_backward_rejects_bad_arguments(lib):
+    st = _strides(64, 2, 128)
+
+    def call(ptrs=None, B=1, d=128, dt=BF16, buf=0x100000, nbytes=1 << 30, p=0.0):
+        ptrs = ptrs or [P] * 9
+        return lib.fa_bwd_host(*ptrs, B, 2, 64, d, st, dt, 0.1, 1, 0, p, 0, 0, 1, buf, nbytes, None)
+    assert call(B=0) == EINVAL
+    assert call(d=96) == EUNSUP
+    assert call(p=1.0) == EINVAL
+    assert call(ptrs=[P] * 8 + [0]) == EINVAL
+    assert call(buf=0) == EWS
+    assert call(buf=0x100000 + 64) == EWS              # 256-byte alignment
+    need = fa.fa_bwd_host_buffer_size(1, 2, 64, 128, BF16, True)
+    assert call(nbytes=need - 1) == EWS
+    # staging: 8 dense tensors, L in one 256-byte slot per group, one group's workspace
+    # (B = 1: two groups of one head)
+    t = 64 * 2 * 128 * 2
+    assert need == 8 * t + 2 * 256 + fa.fa_bwd_workspace_size(1, 1, 64, 128, BF16, True)
+
+
 def test_varlen_workspace_size(lib):
     # L and D rows per (head, sequence), each padded to roundup(max_seqlen, 128);
     # atomic mode adds an fp32 dQ accumulator of roundup(total, 128) + 128 rows per head.
