@@ -30,6 +30,10 @@ kernels avoid):
   position bias, S_ij = scale * q_i.k_j - m * |i - j| with one slope m per
   head (or per batch and head), added after the scale and before the mask. The
   slopes are constants, so the gradient formulas above are unchanged.
+* attn_bias ("Lecture 7" §Mask behaviour: custom masks enter as an additive
+  bias and need their own test path): a given [B or 1, H or 1, N, N] tensor
+  added to the scaled scores, S_ij = scale * q_i.k_j + bias_ij, before the
+  mask; -inf entries mask pairs out. A constant: no gradient is taken for it.
   A row with no allowed key has L = -inf, P = 0, O = 0 and zero gradients.
 
 Parity pins (tests that fix this oracle to something other than itself) live
@@ -74,6 +78,17 @@ def alibi_bias(alibi, b: int, h: int, rows, cols):
     return -m * np.abs(i - j).astype(np.float64)
 
 
+def tensor_bias(bias, b: int, h: int, rows, cols):
+    """bias[b, h, rows, cols] of a [B or 1, H or 1, N, N] array (size-1 dims
+    broadcast); 0 without one."""
+    if bias is None:
+        return 0.0
+    t = np.asarray(bias)
+    bb = b if t.shape[0] > 1 else 0
+    hh = h if t.shape[1] > 1 else 0
+    return t[bb, hh][np.ix_(np.asarray(rows, dtype=np.int64), np.asarray(cols, dtype=np.int64))].astype(np.float64)
+
+
 def _panels(N: int):
     rows = max(1, min(N, _PANEL_BYTES // (8 * max(N, 1))))
     for r0 in range(0, N, rows):
@@ -92,7 +107,7 @@ def _dropout_scale(b, h, H, N, rows, seed, offset, p):
     return z.astype(np.float64) / (1.0 - p)
 
 
-def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None):
+def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None, bias=None):
     """Attention forward; returns (O [B,N,H,d] float64, L [B,H,N] float64).
 
     q, k, v are [B, N, H, d] arrays of any float dtype (widened exactly).
@@ -109,7 +124,8 @@ def forward(q, k, v, scale, causal=False, window=0, dropout_p=0.0, seed=0, offse
             for r0, r1 in _panels(N):
                 rows = np.arange(r0, r1)
                 ok = allowed(rows, N, causal, window)
-                S = np.where(ok, scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N)), -np.inf)
+                S = np.where(ok, scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+                             + tensor_bias(bias, b, h, rows, np.arange(N)), -np.inf)
                 m = S.max(axis=1)
                 live = np.isfinite(m)
                 ms = np.where(live, m, 0.0)
@@ -134,7 +150,7 @@ def preprocess_D(o, do):
 
 
 def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
-             seed=0, offset=0, alibi=None):
+             seed=0, offset=0, alibi=None, bias=None):
     """Attention backward from the saved state (O, L); returns (dQ, dK, dV, D).
 
     Gradients are [B, N, H, d] float64, D is [B, H, N] float64. ``o`` and
@@ -158,7 +174,8 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
                 ok = allowed(rows, N, causal, window)
                 Lr = lse[b, h, r0:r1]
                 live = np.isfinite(Lr)
-                S = scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+                S = (scale * (Q[r0:r1] @ K.T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+                     + tensor_bias(bias, b, h, rows, np.arange(N)))
                 # P_ij = exp(S_ij - L_i) on allowed pairs of rows that have any.
                 P = np.where(ok & live[:, None],
                              np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
@@ -175,7 +192,7 @@ def backward(q, k, v, o, do, lse, scale, causal=False, window=0, dropout_p=0.0,
 
 
 def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
-                 alibi=None):
+                 alibi=None, bias=None):
     """O[b, rows, h, :] and L[b, h, rows] of one head: the same definitions as
     :func:`forward`, evaluated for the listed query rows only (rows are independent)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -183,8 +200,8 @@ def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0
     scale = float(np.float32(scale))
     rows = np.asarray(rows, dtype=np.int64)
     ok = allowed(rows, N, causal, window)
-    S = np.where(ok, scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N)),
-                 -np.inf)
+    S = np.where(ok, scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+                 + tensor_bias(bias, b, h, rows, np.arange(N)), -np.inf)
     m = S.max(axis=1)
     live = np.isfinite(m)
     ms = np.where(live, m, 0.0)
@@ -197,7 +214,7 @@ def forward_rows(q, k, v, b, h, rows, scale, causal=False, window=0, dropout_p=0
 
 
 def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0, dropout_p=0.0, seed=0,
-                  offset=0, alibi=None):
+                  offset=0, alibi=None, bias=None):
     """dQ[b, rows, h, :] of one head from the given O and L (function mode), by the
     definitions of :func:`backward` restricted to the listed query rows."""
     q, k, v, o, do = _f64(q), _f64(k), _f64(v), _f64(o), _f64(do)
@@ -208,7 +225,8 @@ def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0
     ok = allowed(rows, N, causal, window)
     Lr = lse[b, h, rows]
     live = np.isfinite(Lr)
-    S = scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+    S = (scale * (q[b, rows, h, :] @ k[b, :, h, :].T) + alibi_bias(alibi, b, h, rows, np.arange(N))
+         + tensor_bias(bias, b, h, rows, np.arange(N)))
     P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
     D = np.einsum("rd,rd->r", do[b, rows, h, :], o[b, rows, h, :])
     dP = do[b, rows, h, :] @ v[b, :, h, :].T
@@ -220,7 +238,7 @@ def backward_rows(q, k, v, o, do, lse, b, h, rows, scale, causal=False, window=0
 
 
 def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0, dropout_p=0.0, seed=0,
-                  offset=0, alibi=None):
+                  offset=0, alibi=None, bias=None):
     """(dK, dV)[b, cols, h, :] of one head from the given O and L (function mode):
     the definitions of :func:`backward` restricted to the listed key rows, which
     need the column slice P[:, cols] over all query rows."""
@@ -233,7 +251,8 @@ def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0
     ok = allowed(rows, N, causal, window)[:, cols]
     Lr = lse[b, h, :]
     live = np.isfinite(Lr)
-    S = scale * (q[b, :, h, :] @ k[b, cols, h, :].T) + alibi_bias(alibi, b, h, rows, cols)
+    S = (scale * (q[b, :, h, :] @ k[b, cols, h, :].T) + alibi_bias(alibi, b, h, rows, cols)
+         + tensor_bias(bias, b, h, rows, cols))
     P = np.where(ok & live[:, None], np.exp(np.where(ok, S, 0.0) - np.where(live, Lr, 0.0)[:, None]), 0.0)
     D = np.einsum("nd,nd->n", do[b, :, h, :], o[b, :, h, :])
     zs = _dropout_scale(b, h, H, N, rows, seed, offset, dropout_p)
@@ -247,14 +266,15 @@ def backward_cols(q, k, v, o, do, lse, b, h, cols, scale, causal=False, window=0
     return scale * (dS.T @ q[b, :, h, :]), Pt.T @ do[b, :, h, :]
 
 
-def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None):
+def reference_grads(q, k, v, do, scale, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, alibi=None,
+                    bias=None):
     """Exact mode: forward in float64, then backward from that O and L."""
-    O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi)
-    dQ, dK, dV, D = backward(q, k, v, O, do, L, scale, causal, window, dropout_p, seed, offset, alibi)
+    O, L = forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi, bias)
+    dQ, dK, dV, D = backward(q, k, v, O, do, L, scale, causal, window, dropout_p, seed, offset, alibi, bias)
     return O, L, dQ, dK, dV, D
 
 
-__all__ = ["allowed", "alibi_bias", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows",
+__all__ = ["allowed", "alibi_bias", "tensor_bias", "forward", "backward", "preprocess_D", "reference_grads", "forward_rows",
            "backward_rows", "backward_cols", "varlen_forward", "varlen_backward"]
 
 

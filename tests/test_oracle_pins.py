@@ -362,3 +362,83 @@ def test_alibi_zero_slope_is_plain_attention_and_sign_matters():
     O2, L2 = oracle.forward(q, k, v, 0.5, True, alibi=np.full(H, 0.8))
     s = 0.5 * np.einsum("bnhd,bnhd->bhn", q, k)  # diagonal scores (bias 0 there)
     assert np.all(s[:, :, 1:] - L2[:, :, 1:] > s[:, :, 1:] - L1[:, :, 1:])
+
+
+# ------------------------------ attn_bias -------------------------------------
+def _bias(shape, seed, neg_inf_frac=0.0, keep_diag=True):
+    r = np.random.default_rng(seed)
+    b = r.standard_normal(shape) * 2.0
+    if neg_inf_frac:
+        mask = r.random(shape) < neg_inf_frac
+        if keep_diag:
+            n = shape[-1]
+            mask[..., np.arange(n), np.arange(n)] = False
+        b[mask] = -np.inf
+    return b
+
+
+@pytest.mark.parametrize("bshape,causal,window", [((1, 3, 29, 29), True, 0), ((2, 1, 29, 29), False, 0),
+                                                   ((2, 3, 29, 29), True, 7), ((1, 1, 29, 29), False, 5)])
+def test_bias_torch_float64_autograd(bshape, causal, window):
+    """Against torch autograd of softmax(scale QK^T + bias) V, broadcast bias shapes,
+    with a fifth of the entries -inf (masked) off the diagonal."""
+    B, N, H, d = 2, 29, 3, 8
+    q, k, v, do = (_rand((B, N, H, d), 700 + t) for t in range(4))
+    bias = _bias(bshape, 710, neg_inf_frac=0.2)
+    scale = float(np.float32(0.3))
+    O, L, dQ, dK, dV, _ = oracle.reference_grads(q, k, v, do, scale, causal, window, bias=bias)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    s = torch.einsum("bnhd,bmhd->bhnm", tq, tk) * scale + torch.tensor(bias)
+    ok = torch.tensor(allowed(np.arange(N), N, causal, window))[None, None]
+    s = s.masked_fill(~ok, float("-inf"))
+    out = torch.einsum("bhnm,bmhd->bnhd", torch.softmax(s, dim=-1), tv)
+    out.backward(torch.tensor(do))
+    for a, t in ((O, out.detach()), (dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        t = t.numpy()
+        assert np.linalg.norm(a - t) <= 1e-12 * np.linalg.norm(t)
+    np.testing.assert_allclose(L, torch.logsumexp(s.detach(), dim=-1).numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_bias_central_finite_differences():
+    B, N, H, d = 1, 7, 2, 3
+    q, k, v, R = (_rand((B, N, H, d), 720 + t) for t in range(4))
+    bias = _bias((1, H, N, N), 730, neg_inf_frac=0.25)
+    kw = dict(causal=True, window=0, dropout_p=0.2, seed=4, offset=2, bias=bias)
+    _, _, dQ, dK, dV, _ = oracle.reference_grads(q, k, v, R, 0.5, **kw)
+
+    def loss(qq, kk, vv):
+        return float((R * oracle.forward(qq, kk, vv, 0.5, **kw)[0]).sum())
+
+    h = 1e-5
+    for which, grad in ((0, dQ), (1, dK), (2, dV)):
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            up = loss(*args)
+            args[which][idx] -= 2 * h
+            fd[idx] = (up - loss(*args)) / (2 * h)
+        assert np.abs(fd - grad).max() <= 1e-6 * max(1.0, np.abs(grad).max()), which
+
+
+def test_bias_special_cases():
+    """A -inf upper triangle is the causal mask; a row of -inf is a dead row
+    (O = 0, L = -inf, no gradient through it); the ALiBi matrix as a bias is ALiBi."""
+    B, N, H, d = 1, 16, 2, 4
+    q, k, v, do = (_rand((B, N, H, d), 740 + t) for t in range(4))
+    tri = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, 0.0)[None, None]
+    a = oracle.reference_grads(q, k, v, do, 0.5, bias=tri)
+    b = oracle.reference_grads(q, k, v, do, 0.5, causal=True)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, rtol=1e-13, atol=1e-15)
+    dead = np.zeros((1, 1, N, N))
+    dead[0, 0, 5, :] = -np.inf
+    O, L, dQ, dK, dV, _ = oracle.reference_grads(q, k, v, do, 0.5, bias=dead)
+    assert np.all(O[0, 5] == 0) and np.all(np.isneginf(L[0, :, 5])) and np.all(dQ[0, 5] == 0)
+    slopes = np.array([0.3, 0.05])
+    pos = np.arange(N)
+    ab = (-slopes[:, None, None] * np.abs(pos[:, None] - pos[None, :]))[None]
+    a = oracle.reference_grads(q, k, v, do, 0.5, True, bias=ab)
+    b = oracle.reference_grads(q, k, v, do, 0.5, True, alibi=slopes)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-14)
