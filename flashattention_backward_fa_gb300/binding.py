@@ -76,6 +76,12 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd_host_buffer_size.restype = sz
     lib.fa_bwd_host.argtypes = bwd_args
     lib.fa_bwd_host.restype = i
+    lib.fa_fwd_bias.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, FaStrides,
+                                vp]
+    lib.fa_fwd_bias.restype = i
+    lib.fa_bwd_bias.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, FaStrides, i, vp,
+                                           sz, vp]
+    lib.fa_bwd_bias.restype = i
     lib.fa_fwd_alibi.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, vp]
     lib.fa_fwd_alibi.restype = i
     lib.fa_bwd_alibi.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp, i64, i, vp, sz,
@@ -142,6 +148,19 @@ def _alibi(slopes, lead: int, H: int, device):
     raise ValueError(f"alibi_slopes must be [H] or [{lead}, H] with a contiguous head dimension")
 
 
+def _bias(bias, q):
+    """(pointer, FaStrides(b, n, h)) of an attention bias shaped [B or 1, H or 1, N, N]."""
+    B, N, H, _ = q.shape
+    if bias.dtype != q.dtype or not bias.is_cuda or bias.device != q.device:
+        raise ValueError("attn_bias must be a CUDA tensor of the tensors' dtype on their device")
+    if bias.dim() != 4 or bias.shape[0] not in (1, B) or bias.shape[1] not in (1, H) or \
+            tuple(bias.shape[2:]) != (N, N) or bias.stride(3) != 1:
+        raise ValueError(f"attn_bias must be [B or 1, H or 1, {N}, {N}] with contiguous keys")
+    sb = bias.stride(0) if bias.shape[0] > 1 else 0
+    sh = bias.stride(1) if bias.shape[1] > 1 else 0
+    return bias.data_ptr(), FaStrides(sb, bias.stride(2), sh)
+
+
 def default_scale(d: int) -> float:
     return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
 
@@ -152,7 +171,7 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype, deterministic: 
 
 
 def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, stream=None,
-           alibi_slopes=None):
+           alibi_slopes=None, attn_bias=None):
     """Forward through the C ABI: fills o ([B,N,H,d]) and lse ([B,H,N] fp32).
 
     ``alibi_slopes`` (fp32 [H] or [B, H]) adds -m|i - j| to the scaled scores (fa_fwd_alibi).
@@ -164,7 +183,11 @@ def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, s
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, st,
             _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
             float(dropout_p), int(seed), int(offset))
-    if alibi_slopes is None:
+    if alibi_slopes is not None and attn_bias is not None:
+        raise ValueError("pass either alibi_slopes or attn_bias (fold ALiBi into the bias to combine them)")
+    if attn_bias is not None:
+        _check(lib.fa_fwd_bias(*args, *_bias(attn_bias, q), _stream(stream)))
+    elif alibi_slopes is None:
         _check(lib.fa_fwd(*args, _stream(stream)))
     else:
         _check(lib.fa_fwd_alibi(*args, *_alibi(alibi_slopes, B, H, q.device), _stream(stream)))
@@ -183,13 +206,17 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
 
 
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale=None, causal=False, window=0, dropout_p=0.0,
-           seed=0, offset=0, deterministic=True, stream=None, alibi_slopes=None):
+           seed=0, offset=0, deterministic=True, stream=None, alibi_slopes=None, attn_bias=None):
     """Backward through the C ABI: fills dq, dk, dv. ``workspace`` is a uint8 CUDA tensor.
 
     ``alibi_slopes`` as for :func:`fa_fwd` (fa_bwd_alibi)."""
     a = _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p, seed, offset, deterministic,
                   workspace, stream)
-    if alibi_slopes is None:
+    if alibi_slopes is not None and attn_bias is not None:
+        raise ValueError("pass either alibi_slopes or attn_bias (fold ALiBi into the bias to combine them)")
+    if attn_bias is not None:
+        _check(load_library().fa_bwd_bias(*a[:21], *_bias(attn_bias, q), *a[21:]))
+    elif alibi_slopes is None:
         _check(load_library().fa_bwd(*a))
     else:
         # fa_bwd_alibi takes the slopes before `deterministic`
@@ -272,23 +299,24 @@ def alloc_workspace(q: torch.Tensor, deterministic: bool = True) -> torch.Tensor
 
 
 def attention_forward(q, k, v, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
-                      alibi_slopes=None):
+                      alibi_slopes=None, attn_bias=None):
     """Allocate O and L and run the forward; returns (o, lse)."""
     B, N, H, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, scale, causal, window, dropout_p, seed, offset, alibi_slopes=alibi_slopes)
+    fa_fwd(q, k, v, o, lse, scale, causal, window, dropout_p, seed, offset, alibi_slopes=alibi_slopes,
+           attn_bias=attn_bias)
     return o, lse
 
 
 def attention_backward(q, k, v, o, do, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0,
-                       deterministic=True, workspace=None, alibi_slopes=None):
+                       deterministic=True, workspace=None, alibi_slopes=None, attn_bias=None):
     """Allocate dQ, dK, dV (and the workspace unless given) and run the backward."""
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
         workspace = alloc_workspace(q, deterministic)
     fa_bwd(q, k, v, o, do, lse, dq, dk, dv, workspace, scale, causal, window, dropout_p, seed, offset,
-           deterministic, alibi_slopes=alibi_slopes)
+           deterministic, alibi_slopes=alibi_slopes, attn_bias=attn_bias)
     return dq, dk, dv
 
 
@@ -369,21 +397,21 @@ def varlen_attention_backward(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale
 
 class _FlashAttnFunc(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes):
-        o, lse = attention_forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi_slopes)
+    def forward(ctx, q, k, v, scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes, attn_bias):
+        o, lse = attention_forward(q, k, v, scale, causal, window, dropout_p, seed, offset, alibi_slopes, attn_bias)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.cfg = (scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes)
+        ctx.cfg = (scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes, attn_bias)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes = ctx.cfg
+        scale, causal, window, dropout_p, seed, offset, deterministic, alibi_slopes, attn_bias = ctx.cfg
         if do.stride() != q.stride():
             do = _match_layout(do, q)
         dq, dk, dv = attention_backward(q, k, v, o, do, lse, scale, causal, window, dropout_p, seed, offset,
-                                        deterministic, alibi_slopes=alibi_slopes)
-        return dq, dk, dv, None, None, None, None, None, None, None, None
+                                        deterministic, alibi_slopes=alibi_slopes, attn_bias=attn_bias)
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None
 
 
 def _match_layout(t: torch.Tensor, ref: torch.Tensor) -> torch.Tensor:
@@ -393,11 +421,12 @@ def _match_layout(t: torch.Tensor, ref: torch.Tensor) -> torch.Tensor:
 
 
 def flash_attn_func(q, k, v, causal=False, window=0, dropout_p=0.0, softmax_scale=None, seed=0, offset=0,
-                    deterministic=True, alibi_slopes=None):
+                    deterministic=True, alibi_slopes=None, attn_bias=None):
     """Attention on [B, S, H, D] tensors with autograd (forward fa_fwd, backward fa_bwd).
 
-    ``alibi_slopes`` (fp32 [H] or [B, H], not differentiated) adds -m|i - j| to the scaled scores."""
+    ``alibi_slopes`` (fp32 [H] or [B, H]) adds -m|i - j| to the scaled scores; ``attn_bias``
+    ([B or 1, H or 1, S, S], the tensors' dtype, -inf masks) adds itself. Neither is differentiated."""
     k = k if k.stride() == q.stride() else _match_layout(k, q)
     v = v if v.stride() == q.stride() else _match_layout(v, q)
     return _FlashAttnFunc.apply(q, k, v, softmax_scale, causal, window, dropout_p, seed, offset, deterministic,
-                                alibi_slopes)
+                                alibi_slopes, attn_bias)

@@ -80,6 +80,25 @@ bool make_map(CUtensorMap* m, const void* base, const AttnParams& p, bool bf16, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The attention bias as a 4-D map (keys, query rows, heads, batches); a
+// broadcast dimension (stride 0) becomes a dimension of size 1. Boxes of
+// kStepQ rows x kRowsKV keys, unswizzled; rows and keys past N read as 0.
+bool make_bias_map(CUtensorMap* m, const AttnParams& p, bool bf16) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t nh = p.bias_sh ? (cuuint64_t)p.H : 1, nb = p.bias_sb ? (cuuint64_t)p.B : 1;
+  const cuuint64_t plane = (cuuint64_t)p.bias_sn * p.N * 2;  // bytes of one [N, N] plane (stride of size-1 dims)
+  const cuuint64_t dims[4] = {(cuuint64_t)p.N, (cuuint64_t)p.N, nh, nb};
+  const cuuint64_t strides[3] = {(cuuint64_t)p.bias_sn * 2, p.bias_sh ? (cuuint64_t)p.bias_sh * 2 : plane,
+                                 p.bias_sb ? (cuuint64_t)p.bias_sb * 2 : plane};
+  const cuuint32_t box[4] = {(cuuint32_t)fa::kRowsKV, (cuuint32_t)fa::kStepQ, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+             const_cast<void*>(p.bias), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int pad_rows(int N) { return (N + fa::kPadRows - 1) / fa::kPadRows * fa::kPadRows; }
 
@@ -151,6 +170,29 @@ int check_alibi(const float* alibi, int64_t alibi_sb, float scale) {
   return FA_OK;
 }
 
+// Attention bias: strides non-negative with rows at least N keys apart; the
+// 16-bit kernels read it with 16-byte loads and TMA, so there the base is
+// 16-byte aligned and every stride a multiple of 8 elements; folded in score
+// units as bias / scale, so the scale must be positive.
+int check_bias(const void* bias, fa_strides st, int N, int dtype, float scale) {
+  if (!bias) return FA_OK;
+  if (st.b < 0 || st.h < 0 || st.n < N) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_F32) return (reinterpret_cast<uintptr_t>(bias) & 3u) ? FA_ERR_ALIGNMENT : FA_OK;
+  if ((reinterpret_cast<uintptr_t>(bias) & 15u) || ((st.b | st.h | st.n) & 7)) return FA_ERR_ALIGNMENT;
+  return FA_OK;
+}
+
+void apply_extras(AttnParams& p, const fa::Extras& ex) {
+  p.drop.bh_off = ex.philox_bh_off;
+  p.alibi = ex.alibi;
+  p.alibi_sb = ex.alibi_sb;
+  p.bias = ex.bias;
+  p.bias_sb = ex.bias_st.b;
+  p.bias_sh = ex.bias_st.h;
+  p.bias_sn = ex.bias_st.n;
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 // Launches one backward stage for fully validated and filled parameters.
@@ -161,10 +203,12 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
     return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
   const bool bf16 = dtype == FA_BF16;
   if (stage == FA_BWD_DKDV) {
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
         !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
       return FA_ERR_CUDA;
+    if (p.bias ? !make_bias_map(&maps[4], p, bf16) : false) return FA_ERR_CUDA;
+    if (!p.bias) maps[4] = maps[0];  // unused
     return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
   }
   if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
@@ -231,37 +275,29 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int det
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
            uint64_t seed, uint64_t offset, void* stream) {
-  return fa_fwd_alibi(q, k, v, o, lse, B, H, N, d, strides, dtype, scale, causal, window, dropout_p, seed, offset,
-                      nullptr, 0, stream);
+  return fa::fwd_run(q, k, v, o, lse, B, H, N, d, strides, dtype, scale, causal, window, dropout_p, seed, offset,
+                     fa::Extras{}, stream);
 }
 
 int fa_fwd_alibi(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                  fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
                  uint64_t seed, uint64_t offset, const float* alibi_slopes, int64_t alibi_stride_b, void* stream) {
-  int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
-  if (rc) return rc;
-  if ((rc = check_alibi(alibi_slopes, alibi_stride_b, scale))) return rc;
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
-  AttnParams p;
-  fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
-  p.alibi = alibi_slopes;
-  p.alibi_sb = alibi_stride_b;
-  p.q = q;
-  p.k = k;
-  p.v = v;
-  p.out = o;
-  p.lse_out = lse;
-  if ((rc = status_ptr(&p.status))) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == FA_F32) return cuda_rc(fa::launch_fwd_f32(p, st));
-  const bool bf16 = dtype == FA_BF16;
-  CUtensorMap maps[4];
-  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
-      !make_map(&maps[2], v, p, bf16, fa::kStepKV))
-    return FA_ERR_CUDA;
-  maps[3] = maps[0];
-  return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, st));
+  fa::Extras ex;
+  ex.alibi = alibi_slopes;
+  ex.alibi_sb = alibi_stride_b;
+  return fa::fwd_run(q, k, v, o, lse, B, H, N, d, strides, dtype, scale, causal, window, dropout_p, seed, offset,
+                     ex, stream);
+}
+
+int fa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                uint64_t seed, uint64_t offset, const void* bias, fa_strides bias_strides, void* stream) {
+  if (!bias) return FA_ERR_INVALID_ARG;
+  fa::Extras ex;
+  ex.bias = bias;
+  ex.bias_st = bias_strides;
+  return fa::fwd_run(q, k, v, o, lse, B, H, N, d, strides, dtype, scale, causal, window, dropout_p, seed, offset,
+                     ex, stream);
 }
 
 int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
@@ -270,8 +306,8 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
                  uint64_t seed, uint64_t offset, int deterministic, void* workspace, size_t workspace_bytes,
                  void* stream) {
   return fa::bwd_stage_run(stage, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal,
-                           window, dropout_p, seed, offset, nullptr, 0, 0, deterministic, workspace,
-                           workspace_bytes, stream);
+                           window, dropout_p, seed, offset, fa::Extras{}, deterministic, workspace, workspace_bytes,
+                           stream);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -279,7 +315,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
            int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, nullptr, 0, 0, deterministic, workspace, workspace_bytes, stream, true);
+                     dropout_p, seed, offset, fa::Extras{}, deterministic, workspace, workspace_bytes, stream, true);
 }
 
 int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -287,9 +323,24 @@ int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
                  const float* alibi_slopes, int64_t alibi_stride_b, int deterministic, void* workspace,
                  size_t workspace_bytes, void* stream) {
+  fa::Extras ex;
+  ex.alibi = alibi_slopes;
+  ex.alibi_sb = alibi_stride_b;
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, alibi_slopes, alibi_stride_b, 0, deterministic, workspace,
-                     workspace_bytes, stream, true);
+                     dropout_p, seed, offset, ex, deterministic, workspace, workspace_bytes, stream, true);
+}
+
+int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+                float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+                const void* bias, fa_strides bias_strides, int deterministic, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (!bias) return FA_ERR_INVALID_ARG;
+  fa::Extras ex;
+  ex.bias = bias;
+  ex.bias_st = bias_strides;
+  return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
+                     dropout_p, seed, offset, ex, deterministic, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"
@@ -299,11 +350,12 @@ namespace fa {
 int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
-                  uint64_t seed, uint64_t offset, const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off,
-                  int deterministic, void* workspace, size_t workspace_bytes, void* stream) {
+                  uint64_t seed, uint64_t offset, const Extras& ex, int deterministic, void* workspace,
+                  size_t workspace_bytes, void* stream) {
   int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
-  if ((rc = check_alibi(alibi, alibi_sb, scale))) return rc;
+  if ((rc = check_alibi(ex.alibi, ex.alibi_sb, scale))) return rc;
+  if ((rc = check_bias(ex.bias, ex.bias_st, N, dtype, scale))) return rc;
   if (stage != FA_BWD_PREPROCESS && stage != FA_BWD_DKDV && stage != FA_BWD_DQ) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
@@ -314,9 +366,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
     return FA_ERR_WORKSPACE;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
-  p.drop.bh_off = philox_bh_off;
-  p.alibi = alibi;
-  p.alibi_sb = alibi_sb;
+  apply_extras(p, ex);
   p.q = q;
   p.k = k;
   p.v = v;
@@ -332,6 +382,35 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
   if ((rc = status_ptr(&p.status))) return rc;
   return launch_stage(stage, p, dtype, deterministic, stream);
+}
+
+int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p, uint64_t seed,
+            uint64_t offset, const Extras& ex, void* stream) {
+  int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
+  if (rc) return rc;
+  if ((rc = check_alibi(ex.alibi, ex.alibi_sb, scale))) return rc;
+  if ((rc = check_bias(ex.bias, ex.bias_st, N, dtype, scale))) return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  AttnParams p;
+  fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
+  apply_extras(p, ex);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = o;
+  p.lse_out = lse;
+  if ((rc = status_ptr(&p.status))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_F32) return cuda_rc(fa::launch_fwd_f32(p, st));
+  const bool bf16 = dtype == FA_BF16;
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
+      !make_map(&maps[2], v, p, bf16, fa::kStepKV))
+    return FA_ERR_CUDA;
+  maps[3] = maps[0];
+  return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, st));
 }
 
 int check_bwd_args(int B, int H, int N, int d, fa_strides strides, fa_dtype dtype, float scale, int window,
@@ -391,12 +470,11 @@ namespace fa {
 int bwd_run(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
             void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
             float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
-            const float* alibi, int64_t alibi_sb, uint32_t philox_bh_off, int deterministic, void* workspace,
-            size_t workspace_bytes, void* stream, bool allow_side_stream) {
+            const Extras& ex, int deterministic, void* workspace, size_t workspace_bytes, void* stream,
+            bool allow_side_stream) {
   auto stage = [&](fa_bwd_stage_id s, void* st) {
     return bwd_stage_run(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                         dropout_p, seed, offset, alibi, alibi_sb, philox_bh_off, deterministic, workspace,
-                         workspace_bytes, st);
+                         dropout_p, seed, offset, ex, deterministic, workspace, workspace_bytes, st);
   };
   return run_backward(stage, deterministic, dtype, allow_side_stream, stream);
 }

@@ -210,10 +210,11 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
     // backward of the group on the caller's stream (groups share the workspace, in stream order)
     const size_t elem0 = ((size_t)b0 * N * H + h0) * d * es;
     auto at = [&](int t) { return static_cast<void*>(base + L.off[t] + elem0); };
-    const uint32_t bh_off = (uint32_t)(b0 * H + h0);
+    fa::Extras ex;
+    ex.philox_bh_off = (uint32_t)(b0 * H + h0);
     rc = fa::bwd_run(at(0), at(1), at(2), at(3), at(4), lse_dev,
                      at(5), at(6), at(7), nb, nh, N, d, dense, dtype, scale, causal, window, dropout_p, seed, offset,
-                     nullptr, 0, bh_off, deterministic, base + L.off_ws, L.ws, stream, true);
+                     ex, deterministic, base + L.off_ws, L.ws, stream, true);
     if (rc) return rc;
     // download: the group's dQ, dK, dV
     if (cudaEventRecord(hp->done[g], st) != cudaSuccess || cudaStreamWaitEvent(hp->down, hp->done[g], 0) != cudaSuccess)

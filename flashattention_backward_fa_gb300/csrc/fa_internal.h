@@ -57,6 +57,12 @@ struct AttnParams {
   // one slope per head across the batch.
   const float* alibi;
   int64_t alibi_sb;
+  // Additive attention bias (null: none): the score of (i, j) gains
+  // bias[b, h, i, j] after the scale, in the tensors' dtype, element strides
+  // bias_sb / bias_sh (0 broadcasts over batches / heads) and bias_sn per
+  // query row; keys are contiguous. -inf entries mask pairs out.
+  const void* bias;
+  int64_t bias_sb, bias_sh, bias_sn;
 };
 
 // One CTA's unit: a tile of rows of one (batch, head), or of one (sequence,
@@ -141,6 +147,50 @@ template <int kX0>
 __device__ __forceinline__ void alibi_ramp16(uint32_t (&sr)[16], float slope) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) sr[e] = __float_as_uint(fmaf(slope, (float)(kX0 + e), __uint_as_float(sr[e])));
+}
+
+// Start of the bias row of local query row i in unit u (elements of T).
+template <typename T>
+__device__ __forceinline__ const T* bias_row(const AttnParams& p, const Unit& u, int i) {
+  return static_cast<const T*>(p.bias) + (long long)u.b * p.bias_sb + (long long)u.h * p.bias_sh +
+         (long long)(u.row0 + i) * p.bias_sn;
+}
+
+// 16-bit value (bf16 or fp16 bits in the low half) to fp32.
+template <bool kBf16>
+__device__ __forceinline__ float h16_bits_to_f32(uint32_t bits) {
+  if constexpr (kBf16) {
+    return __uint_as_float(bits << 16);
+  } else {
+    float f;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "r"(bits));
+    return f;
+  }
+}
+
+// Attention bias on 16 raw scores of one TMEM row, read from a bias tile in
+// shared memory: value e at addr + e * row_bytes, folded in score units
+// (s += bias / scale, so that the kernels' scale * log2(e) restores it).
+template <bool kBf16>
+__device__ __forceinline__ void bias_fold16_smem(uint32_t (&sr)[16], uint32_t addr, uint32_t row_bytes,
+                                                 float inv_scale) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr + (uint32_t)e * row_bytes));
+    sr[e] = __float_as_uint(fmaf(h16_bits_to_f32<kBf16>(v), inv_scale, __uint_as_float(sr[e])));
+  }
+}
+
+// The same from 16 consecutive 16-bit values held in registers (8 words).
+template <bool kBf16>
+__device__ __forceinline__ void bias_fold16_regs(uint32_t (&sr)[16], const uint32_t* w, float inv_scale) {
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const float lo = h16_bits_to_f32<kBf16>(w[x] & 0xFFFFu), hi = h16_bits_to_f32<kBf16>(w[x] >> 16);
+    sr[2 * x] = __float_as_uint(fmaf(lo, inv_scale, __uint_as_float(sr[2 * x])));
+    sr[2 * x + 1] = __float_as_uint(fmaf(hi, inv_scale, __uint_as_float(sr[2 * x + 1])));
+  }
 }
 
 // Allowed (query i, key j) pair under the causal / sliding-window mask.

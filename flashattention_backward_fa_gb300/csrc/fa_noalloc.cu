@@ -67,5 +67,5 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   if (rc) return rc;
   // Single stream: this entry point creates nothing, not even the side stream.
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, nullptr, 0, 0, 1, scratch, kNoAllocScratchBytes, stream, false);
+                     dropout_p, seed, offset, fa::Extras{}, 1, scratch, kNoAllocScratchBytes, stream, false);
 }

@@ -20,6 +20,12 @@
 namespace fa {
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// -L * log2(e) for the backward's exp2 addend. A row with no finite score
+// (L = -inf, possible only when an attention bias masks every key) gets -inf,
+// not +inf, so that its probabilities come out 0 even where a biased score is
+// -inf (-inf + inf would be NaN).
+__device__ __forceinline__ float neg_l2(float L) { return L == -INFINITY ? L : -(L * kLog2e); }
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <typename T>
@@ -83,7 +89,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
   }
   if (lane == 0) {
     p.ws_nD[ws] = -acc;
-    p.ws_nL2[ws] = (i < p.N) ? -(p.lse[(long long)bh * p.N + i] * kLog2e) : __int_as_float(0xff800000);
+    p.ws_nL2[ws] = (i < p.N) ? neg_l2(p.lse[(long long)bh * p.N + i]) : __int_as_float(0xff800000);
   }
   if (p.ws_dq != nullptr) {
     float* dq = p.ws_dq + ws * p.d;
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_consta
     if (i >= pad) continue;
     if (e0 == 0) {
       p.ws_nD[ws0 + i] = -acc;
-      p.ws_nL2[ws0 + i] = (i < n) ? -(p.lse[lse0 + i] * kLog2e) : __int_as_float(0xff800000);
+      p.ws_nL2[ws0 + i] = (i < n) ? neg_l2(p.lse[lse0 + i]) : __int_as_float(0xff800000);
     }
     // (packed input: the dQ accumulator is zeroed separately)
     if (p.ws_dq != nullptr && p.cu_seqlens == nullptr) {
@@ -251,6 +257,14 @@ __device__ __forceinline__ float alibi_slope_log2(const AttnParams& p, int b, in
   return p.alibi ? __ldg(p.alibi + (long long)b * p.alibi_sb + h) * kLog2e : 0.f;
 }
 
+// Attention bias of (query i, key j) in the log2 domain (0 without a bias).
+__device__ __forceinline__ float bias_log2_f32(const AttnParams& p, int b, int h, int i, int j) {
+  if (!p.bias) return 0.f;
+  const float* row = static_cast<const float*>(p.bias) + (long long)b * p.bias_sb + (long long)h * p.bias_sh +
+                     (long long)i * p.bias_sn;
+  return __ldg(row + j) * kLog2e;
+}
+
 // Forward, one warp per query row: pass 1 row max and sum of exp2 (lanes take
 // keys lane, lane+32, ...), pass 2 O = sum_j P~_ij V_j with lanes owning head
 // dimensions and P broadcast by shuffles.
@@ -268,7 +282,9 @@ __global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_co
   const float am = alibi_slope_log2(p, b, h);
   float m = -INFINITY, l = 0.f;
   for (int j = jlo + lane; j <= jhi; j += 32) {
-    const float x = fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2);
+    const float x = fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) +
+                    bias_log2_f32(p, b, h, i, j);
+    if (x == -INFINITY) continue;  // a pair the bias masks out
     const float mn = fmaxf(m, x);
     l = l * ex2_approx(m - mn) + ex2_approx(x - mn);
     m = mn;
@@ -290,8 +306,8 @@ __global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_co
     const int j = jb + lane;
     float pj = 0.f;
     if (j <= jhi) {
-      pj = ex2_approx(fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) -
-                      L2);
+      pj = ex2_approx(fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) +
+                      bias_log2_f32(p, b, h, i, j) - L2);
       if (p.drop.threshold) pj = dropout_keep(p.drop, bh, p.N, i, j) ? pj * p.drop.rp : 0.f;
     }
     const int cnt = min(32, jhi - jb + 1);
@@ -341,7 +357,8 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __gr
     float pt = 0.f, ds = 0.f;
     if (i <= ihi) {
       const float pv = ex2_approx(
-          fmaf(-am, fabsf((float)(i - j)), dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2) + nL2[i]);
+          fmaf(-am, fabsf((float)(i - j)), dot_row(krow[w], row_ptr(p, p.q, b, i, h), p.d) * p.scale_log2) +
+          bias_log2_f32(p, b, h, i, j) + nL2[i]);
       float dp = dot_row(vrow[w], row_ptr(p, p.dout, b, i, h), p.d);
       pt = pv;
       if (p.drop.threshold) {
@@ -403,7 +420,8 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid
     float ds = 0.f;
     if (j <= jhi) {
       const float pv = ex2_approx(
-          fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) + nL2);
+          fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) +
+          bias_log2_f32(p, b, h, i, j) + nL2);
       float dp = dot_row(grow[w], row_ptr(p, p.v, b, j, h), p.d);
       if (p.drop.threshold) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
       ds = pv * (dp + nD);

@@ -41,7 +41,7 @@ namespace fa {
 
 constexpr int kKVThreads = 640;  // 4 role warps + 4 row-math warpgroups
 
-template <int D, bool kAtomic>
+template <int D, bool kAtomic, bool kBias = false>
 struct KVCfg {
   static constexpr int kPanels = D / 64;
   static constexpr uint32_t kKVPanel = kRowsKV * 128;          // 16 KB: 128 rows x 64 elements
@@ -50,8 +50,10 @@ struct KVCfg {
   static constexpr uint32_t kQTile = kPanels * kQPanel;
   static constexpr uint32_t kPTile = kRowsKV * kStepQ * 2;     // 16 KB: 128 keys x 64 queries
   static constexpr uint32_t kImgBytes = kAtomic ? 4 * kPTile : 0;  // dS^T [buffer][rounded, residual]
-  static constexpr uint32_t kStageBytes = 2 * kQTile + 2 * kStepQ * 4;
-  static constexpr uint32_t kFixed = 2 * kKVTile + kImgBytes + 512 + 1024;
+  // attention bias tile of a step: 64 query rows x 128 keys, 16-bit, unswizzled
+  static constexpr uint32_t kBiasTile = kBias ? kStepQ * kRowsKV * 2 : 0;
+  static constexpr uint32_t kStageBytes = 2 * kQTile + 2 * kStepQ * 4 + kBiasTile;
+  static constexpr uint32_t kFixed = 2 * kKVTile + kImgBytes + 512 + 1024 + 128;
   static constexpr int kNSraw = (int)((227u * 1024u - kFixed) / kStageBytes);
   static constexpr int kNS = kNSraw > 4 ? 4 : kNSraw;          // Q/dO pipeline stages
   static constexpr uint32_t oK = 0;
@@ -61,7 +63,8 @@ struct KVCfg {
   static constexpr uint32_t oImg = oDO + kNS * kQTile;
   static constexpr uint32_t oL = oImg + kImgBytes;
   static constexpr uint32_t oD = oL + kNS * kStepQ * 4;
-  static constexpr uint32_t oBar = oD + kNS * kStepQ * 4;
+  static constexpr uint32_t oB = (oD + kNS * kStepQ * 4 + 127) & ~127u;
+  static constexpr uint32_t oBar = oB + kNS * kBiasTile;
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kNS;
@@ -94,12 +97,12 @@ __device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row,
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi>
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias>
 __global__ void __launch_bounds__(kKVThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmDO) {
-  using C = KVCfg<D, kAtomic>;
+                    const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmBias) {
+  using C = KVCfg<D, kAtomic, kBias>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -178,6 +181,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
           tma_load_4d(sb + C::oDO + s * C::kQTile + pn * C::kQPanel, &tmDO, bar(C::bQFull + s), 64 * pn,
                       u.row0 + i0, h, b);
         }
+        if constexpr (kBias)  // 64 query rows x 128 keys of the bias (rows / keys past N read as 0)
+          tma_load_4d(sb + C::oB + s * C::kBiasTile, &tmBias, bar(C::bQFull + s), u.row0 + j0, u.row0 + i0,
+                      p.bias_sh ? h : 0, p.bias_sb ? b : 0);
         const long long ws = u.ws + i0;
         bulk_load(sb + C::oL + s * kStepQ * 4, p.ws_nL2 + ws, kStepQ * 4, bar(C::bQFull + s));
         bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_nD + ws, kStepQ * 4, bar(C::bQFull + s));
@@ -336,6 +342,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     const uint32_t tSc = tS + lane_off + 64 * bb + 32 * c, tdPc = tdP + lane_off + 64 * bb + 32 * c;
     const uint32_t imgRow = sb + C::oImg + 2 * bb * C::kPTile + jl * 128;
     const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
+    const float inv_scale = kBias ? 1.f / p.scale : 0.f;
     bool ok = true;
     for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
@@ -373,6 +380,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tmem_ld16(tSc + 16 * hh, sr);
         tmem_ld_wait16(sr);
         if constexpr (kAlibi) alibi_fold16<1>(sr, (float)(base + 16 * hh - j), slope_raw);
+        if constexpr (kBias)  // bias tile row = query (32c + 16hh + e) of the step, column = this key
+          bias_fold16_smem<kBf16>(sr, sb + C::oB + s * C::kBiasTile + (uint32_t)(32 * c + 16 * hh) * (kRowsKV * 2) +
+                                          (uint32_t)jl * 2,
+                                  kRowsKV * 2, inv_scale);
         float cmax = 0.f;
         float pt[16];
         // P = exp2(S * scale*log2e + (-L*log2e)) on pairs of columns; the unmasked
@@ -550,28 +561,34 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi>
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias>
 static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  using C = KVCfg<D, kAtomic>;
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop, kAlibi>;
+  using C = KVCfg<D, kAtomic, kBias>;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop, kAlibi, kBias>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
   const int tiles = (rows + kRowsKV - 1) / kRowsKV;
   const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
-  kern<<<grid, kKVThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, kKVThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4]);
   return cudaGetLastError();
+}
+
+template <int D, bool kBf16, bool kAtomic, bool kBias>
+static cudaError_t launch_dkdv_b(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+  const bool drop = p.drop.threshold != 0;
+  if (p.alibi)
+    return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true, kBias>(p, maps, st)
+                : launch_dkdv_t<D, kBf16, kAtomic, false, true, kBias>(p, maps, st);
+  return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, false, kBias>(p, maps, st)
+              : launch_dkdv_t<D, kBf16, kAtomic, false, false, kBias>(p, maps, st);
 }
 
 template <int D, bool kBf16, bool kAtomic>
 static cudaError_t launch_dkdv_a(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  const bool drop = p.drop.threshold != 0;
-  if (p.alibi)
-    return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true>(p, maps, st)
-                : launch_dkdv_t<D, kBf16, kAtomic, false, true>(p, maps, st);
-  return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, false>(p, maps, st)
-              : launch_dkdv_t<D, kBf16, kAtomic, false, false>(p, maps, st);
+  return p.bias ? launch_dkdv_b<D, kBf16, kAtomic, true>(p, maps, st)
+                : launch_dkdv_b<D, kBf16, kAtomic, false>(p, maps, st);
 }
 
 template <int D, bool kBf16>
@@ -579,7 +596,9 @@ static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, const CUtenso
   return atomic ? launch_dkdv_a<D, kBf16, true>(p, maps, st) : launch_dkdv_a<D, kBf16, false>(p, maps, st);
 }
 
-// maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows).
+// maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows), and
+// the attention bias (boxes of kStepQ rows x kRowsKV keys; any valid map when
+// p.bias is null).
 cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
                                cudaStream_t st) {
   if (p.d == 128)

@@ -104,7 +104,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
-template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi>
+template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi, bool kBias>
 __global__ void __launch_bounds__(kQThreads, 1)
     qmajor_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -370,6 +370,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       nD = p.ws_nD[ws];
     }
     const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
+    const float inv_scale = kBias ? 1.f / p.scale : 0.f;
+    // this row's attention bias (null past the sequence: those rows store nothing)
+    const uint16_t* brow = nullptr;
+    if constexpr (kBias) brow = i < Nl ? bias_row<uint16_t>(p, u, i) : nullptr;
     float mref = -INFINITY, lsum = 0.f;
     float* xchg = reinterpret_cast<float*>(smem + C::oStats);
     bool ok = true;
@@ -377,6 +381,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int bb = it % C::kSBuf, xb = it & 1;
       const int base = key_block(it) + 32 * c;
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
+      // The bias of this chunk's 32 keys, loaded before the wait for S so that
+      // its latency overlaps it: four 16-byte loads, or per-key loads where the
+      // chunk runs past the last key.
+      uint32_t bw[16];
+      if constexpr (kBias) {
+        if (brow != nullptr && base + 32 <= p.N) {
+          const uint4* src = reinterpret_cast<const uint4*>(brow + base);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint4 v4 = __ldg(src + t);
+            bw[4 * t] = v4.x;
+            bw[4 * t + 1] = v4.y;
+            bw[4 * t + 2] = v4.z;
+            bw[4 * t + 3] = v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int j = base + 2 * x;
+            const uint32_t lo = (brow != nullptr && j < p.N) ? __ldg(brow + j) : 0u;
+            const uint32_t hi = (brow != nullptr && j + 1 < p.N) ? __ldg(brow + j + 1) : 0u;
+            bw[x] = lo | (hi << 16);
+          }
+        }
+      }
       if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it / C::kSBuf) & 1, abort_flag, p.status)) {
         ok = false;
         break;
@@ -410,6 +439,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // constant plus a ramp over the chunk's columns: the ramp goes into the
       // raw scores (one FMA a score) and the constant, rc2 (log2 domain), into
       // the exp2 addend. A chunk that straddles the diagonal folds |i - j| in.
+      if constexpr (kBias) {
+        bias_fold16_regs<kBf16>(sr2[0], bw, inv_scale);
+        if constexpr (!kDq) bias_fold16_regs<kBf16>(sr2[1], bw + 8, inv_scale);
+      }
       float rc2 = 0.f, ramp = 0.f;
       bool straddle = false;
       if constexpr (kAlibi) {
@@ -475,6 +508,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
           mref = mstep;
         }
         nL2 = -mref;  // P = exp2(S*scale*log2e + (-mref)); +inf only where every key so far is masked
+        // With a bias, an allowed score may be -inf: while a row has no finite
+        // score its addend must stay finite (-inf + inf is NaN).
+        if constexpr (kBias) nL2 = mref == -INFINITY ? 0.f : nL2;
       }
       const float nL2c = kAlibi ? nL2 + rc2 : nL2;  // the exp2 addend of this chunk
       bool lo_any = false;
@@ -484,6 +520,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           __syncwarp();
           tmem_ld16(tSc + 16, sr2[1]);
           tmem_ld_wait16(sr2[1]);
+          if constexpr (kBias) bias_fold16_regs<kBf16>(sr2[1], bw + 8, inv_scale);
           if constexpr (kAlibi) {
             if (straddle)
               alibi_fold16<-1>(sr2[1], (float)(i - base - 16), slope_raw);
@@ -655,10 +692,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 }
 
-template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi>
+template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi, bool kBias>
 static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   using C = QCfg<D, kMode>;
-  auto kern = qmajor_kernel<D, kBf16, kMode, kDrop, kAlibi>;
+  auto kern = qmajor_kernel<D, kBf16, kMode, kDrop, kAlibi, kBias>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -669,14 +706,19 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
   return cudaGetLastError();
 }
 
-template <int D, bool kBf16, int kMode>
-static cudaError_t launch_q_m(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+template <int D, bool kBf16, int kMode, bool kBias>
+static cudaError_t launch_q_b(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   const bool drop = p.drop.threshold != 0;
   if (p.alibi)
-    return drop ? launch_q_t<D, kBf16, kMode, true, true>(p, maps, st)
-                : launch_q_t<D, kBf16, kMode, false, true>(p, maps, st);
-  return drop ? launch_q_t<D, kBf16, kMode, true, false>(p, maps, st)
-              : launch_q_t<D, kBf16, kMode, false, false>(p, maps, st);
+    return drop ? launch_q_t<D, kBf16, kMode, true, true, kBias>(p, maps, st)
+                : launch_q_t<D, kBf16, kMode, false, true, kBias>(p, maps, st);
+  return drop ? launch_q_t<D, kBf16, kMode, true, false, kBias>(p, maps, st)
+              : launch_q_t<D, kBf16, kMode, false, false, kBias>(p, maps, st);
+}
+
+template <int D, bool kBf16, int kMode>
+static cudaError_t launch_q_m(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+  return p.bias ? launch_q_b<D, kBf16, kMode, true>(p, maps, st) : launch_q_b<D, kBf16, kMode, false>(p, maps, st);
 }
 
 template <int D, bool kBf16>

@@ -185,6 +185,31 @@ int fa_bwd_alibi(const void* q, const void* k, const void* v, const void* o, con
                  size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Additive attention bias ("Lecture 7 — Backward Pass and Validation", §Mask
+ * behaviour: custom masks enter as an attn_bias and need their own test path):
+ * the score of query i and key j becomes scale * q_i.k_j + bias[b, h, i, j]
+ * before the mask and the softmax; -inf entries mask pairs out (a row with
+ * every key masked gets O = 0, L = -inf and no gradient). The bias is a
+ * constant: no gradient is computed for it.
+ * bias: device memory in the tensors' dtype, logically [B, H, N, N] with keys
+ * contiguous and element strides bias_strides = {b, n (per query row), h}; a
+ * stride of 0 for b or h broadcasts one plane over the batch or the heads.
+ * Requires scale > 0 and bias_strides.n >= N; for 16-bit dtypes a 16-byte
+ * aligned base and strides that are multiples of 8 elements (a [N, N] plane
+ * with N not a multiple of 8 is passed as a view of rows padded to one;
+ * FA_ERR_ALIGNMENT otherwise); fp32: a 4-byte aligned base, any strides.
+ * Errors as fa_fwd / fa_bwd (FA_ERR_INVALID_ARG for a null bias).
+ * ------------------------------------------------------------------------- */
+int fa_fwd_bias(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
+                uint64_t seed, uint64_t offset, const void* bias, fa_strides bias_strides, void* stream);
+int fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
+                float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
+                const void* bias, fa_strides bias_strides, int deterministic, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Packed variable-length sequences ("Lecture 7 — Backward Pass and
  * Validation", §Use it in the real stack, lists varlen among the cases a
  * complete harness covers; the math per sequence is that of fa_fwd / fa_bwd).

@@ -188,6 +188,30 @@ def test_host_backward_rejects_bad_arguments(lib):
     assert need == 8 * t + 2 * 256 + fa.fa_bwd_workspace_size(1, 1, 64, 128, BF16, True)
 
 
+def test_bias_rejects_bad_arguments(lib):
+    N = 64
+    st = _strides(N, 2, 128)
+
+    def fwd(bias=P, bst=(0, N, 0), scale=0.1, dt=BF16, d=128):
+        return lib.fa_fwd_bias(*([P] * 5), 1, 2, N, d, st, dt, scale, 1, 0, 0.0, 0, 0, bias, fa.FaStrides(*bst), None)
+    assert fwd(bias=0) == EINVAL
+    assert fwd(bst=(0, N - 8, 0)) == EINVAL      # rows must not overlap
+    assert fwd(bst=(-8, N, 0)) == EINVAL
+    assert fwd(scale=0.0) == EUNSUP               # folded in score units as bias / scale
+    assert fwd(bias=P + 8) == EALIGN              # 16-bit: 16-byte aligned base
+    assert fwd(bst=(0, N + 4, 0)) == EALIGN       # 16-bit: strides in multiples of 8 elements
+    assert fwd(bst=(12, N, 0)) == EALIGN
+    assert fwd(d=96) == EUNSUP
+    assert fwd(dt=F32, bias=P + 2) == EALIGN      # fp32: 4-byte aligned
+
+    def bwd(bias=P, bst=(0, N, 0), ws=0x100000):
+        return lib.fa_bwd_bias(*([P] * 9), 1, 2, N, 128, st, BF16, 0.1, 1, 0, 0.0, 0, 0, bias, fa.FaStrides(*bst), 1,
+                               ws, 1 << 30, None)
+    assert bwd(bias=0) == EINVAL
+    assert bwd(bias=P + 2) == EALIGN
+    assert bwd(ws=0) == EWS
+
+
 def test_varlen_workspace_size(lib):
     # L and D rows per (head, sequence), each padded to roundup(max_seqlen, 128);
     # atomic mode adds an fp32 dQ accumulator of roundup(total, 128) + 128 rows per head.
