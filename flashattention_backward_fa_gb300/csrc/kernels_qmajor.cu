@@ -386,6 +386,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // chunk runs past the last key.
       uint32_t bw[16];
       if constexpr (kBias) {
+        // pull the segment of two steps ahead into L2 (64 bytes, within one line)
+        if (brow != nullptr && it + 2 < nsteps) {
+          const int ahead = key_block(it + 2) + 32 * c;
+          if (ahead < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(brow + ahead));
+        }
         if (brow != nullptr && base + 32 <= p.N) {
           const uint4* src = reinterpret_cast<const uint4*>(brow + base);
 #pragma unroll
