@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int nkv = (j_last >= j_first) ? (j_last - j_first) / kStepKV + 1 : 0;
   // One pass over the key blocks in both modes.
   const int nsteps = nkv;
-  const int first_out = 0;
   // Key block of step it. Ascending, except in the ALiBi forward: there the
   // blocks go outward from the one holding this tile's diagonal (nearest first,
   // alternating below and above), so that every row meets its largest biased
@@ -215,18 +214,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tma_load_4d(sb + C::oE + se * C::kTile + pn * C::kPanel, mE, bar(C::bEFull + se), 64 * pn, u.row0 + jj,
                       h, b);
         issuedE = it + 1;
-        if (it >= first_out) {
-          const int li = it - first_out, sl = li % C::kNL;
-          if (!mbar_wait(bar(C::bLEmpty + sl), ((li / C::kNL) & 1) ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(C::bLFull + sl), C::kTile);
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn,
-                        u.row0 + jj, h, b);
-          issuedL = li + 1;
+        const int sl = it % C::kNL;
+        if (!mbar_wait(bar(C::bLEmpty + sl), ((it / C::kNL) & 1) ^ 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx(bar(C::bLFull + sl), C::kTile);
+        for (int pn = 0; pn < C::kPanels; ++pn)
+          tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn, u.row0 + jj,
+                      h, b);
+        issuedL = it + 1;
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
@@ -297,8 +294,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------ accumulating MMA issuer (O or dQ) ---------------------
-    // After the row math of step t: acc += (P~ or dS) . (V_j or K_j) on output
-    // steps, then release the S buffer and the ring-L tile.
+    // After the row math of step t: acc += (P~ or dS) . (V_j or K_j), then
+    // release the S buffer and the ring-L tile.
     {
       constexpr uint32_t idO = make_idesc(128, D, kBf16, false, true);
       const uint64_t b0 = make_sdesc(sb + C::oL, C::kPanel, 1024);
@@ -310,37 +307,33 @@ __global__ void __launch_bounds__(kQThreads, 1)
           break;
         }
         tc_fence_after();
-        if (t >= first_out) {
-          const int li = t - first_out, sl = li % C::kNL;
-          // Forward: V (ring L) must have landed before the MMA reads it. In the dQ
-          // kernel ring L holds K, whose arrival the S issuer waited for before S.
-          if (!kDq && !warp_wait<kIssuerPoll>(bar(C::bLFull + sl), (li / C::kNL) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t first = t > first_out ? 1u : 0u;
-          const int4* f4 = reinterpret_cast<const int4*>(const_cast<const int*>(flags) + 16 * bt);
-          int any = 0;
+        const int sl = t % C::kNL;
+        // Forward: V (ring L) must have landed before the MMA reads it. In the dQ
+        // kernel ring L holds K, whose arrival the S issuer waited for before S.
+        if (!kDq && !warp_wait<kIssuerPoll>(bar(C::bLFull + sl), (t / C::kNL) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t first = t > 0 ? 1u : 0u;  // the first step overwrites the accumulator
+        const int4* f4 = reinterpret_cast<const int4*>(const_cast<const int*>(flags) + 16 * bt);
+        int any = 0;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int4 v = f4[x];
-            any |= v.x | v.y | v.z | v.w;
-          }
-          const uint64_t bop = desc_add(b0, sl * C::kTile);
+        for (int x = 0; x < 4; ++x) {
+          const int4 v = f4[x];
+          any |= v.x | v.y | v.z | v.w;
+        }
+        const uint64_t bop = desc_add(b0, sl * C::kTile);
+#pragma unroll
+        for (int k = 0; k < kStepKV / 16; ++k)
+          tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k, desc_add(bop, 2048 * k), idO, k > 0 ? 1u : first);
+        if (any) {
 #pragma unroll
           for (int k = 0; k < kStepKV / 16; ++k)
-            tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k, desc_add(bop, 2048 * k), idO, k > 0 ? 1u : first);
-          if (any) {
-#pragma unroll
-            for (int k = 0; k < kStepKV / 16; ++k)
-              tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
-          }
-          tc_commit_w(bar(C::bSEmpty + bt));
-          tc_commit_w(bar(C::bLEmpty + sl));
-          if (!kDq) tc_commit_w(bar(C::bODone));
-        } else {
-          tc_commit_w(bar(C::bSEmpty + bt));
+            tc_mma_ts_w(tAcc, tS + 128 * bt + 16 * k + 8, desc_add(bop, 2048 * k), idO, 1u);
         }
+        tc_commit_w(bar(C::bSEmpty + bt));
+        tc_commit_w(bar(C::bLEmpty + sl));
+        if (!kDq) tc_commit_w(bar(C::bODone));
       }
       tc_commit_w(bar(C::bAcc));
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
