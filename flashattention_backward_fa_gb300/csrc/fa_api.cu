@@ -81,9 +81,11 @@ bool make_map(CUtensorMap* m, const void* base, const AttnParams& p, bool bf16, 
 }
 
 // The attention bias as a 4-D map (keys, query rows, heads, batches); a
-// broadcast dimension (stride 0) becomes a dimension of size 1. Boxes of
-// kStepQ rows x kRowsKV keys, unswizzled; rows and keys past N read as 0.
-bool make_bias_map(CUtensorMap* m, const AttnParams& p, bool bf16) {
+// broadcast dimension (stride 0) becomes a dimension of size 1; rows and keys
+// past N read as 0. Key-major kernel: boxes of kStepQ rows x kRowsKV keys,
+// unswizzled. Query-major kernels: boxes of kRowsQ rows x 64 keys, 128-byte
+// swizzle.
+bool make_bias_map(CUtensorMap* m, const AttnParams& p, bool bf16, bool query_major) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t nh = p.bias_sh ? (cuuint64_t)p.H : 1, nb = p.bias_sb ? (cuuint64_t)p.B : 1;
@@ -91,12 +93,13 @@ bool make_bias_map(CUtensorMap* m, const AttnParams& p, bool bf16) {
   const cuuint64_t dims[4] = {(cuuint64_t)p.N, (cuuint64_t)p.N, nh, nb};
   const cuuint64_t strides[3] = {(cuuint64_t)p.bias_sn * 2, p.bias_sh ? (cuuint64_t)p.bias_sh * 2 : plane,
                                  p.bias_sb ? (cuuint64_t)p.bias_sb * 2 : plane};
-  const cuuint32_t box[4] = {(cuuint32_t)fa::kRowsKV, (cuuint32_t)fa::kStepQ, 1, 1};
+  const cuuint32_t box[4] = {query_major ? 64u : (cuuint32_t)fa::kRowsKV,
+                             query_major ? (cuuint32_t)fa::kRowsQ : (cuuint32_t)fa::kStepQ, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
              const_cast<void*>(p.bias), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             query_major ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -207,15 +210,17 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
     if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
         !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
       return FA_ERR_CUDA;
-    if (p.bias ? !make_bias_map(&maps[4], p, bf16) : false) return FA_ERR_CUDA;
+    if (p.bias ? !make_bias_map(&maps[4], p, bf16, false) : false) return FA_ERR_CUDA;
     if (!p.bias) maps[4] = maps[0];  // unused
     return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
   }
   if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   if (!make_map(&maps[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], p.k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], p.v, p, bf16, fa::kStepKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kRowsQ))
     return FA_ERR_CUDA;
+  if (p.bias ? !make_bias_map(&maps[4], p, bf16, true) : false) return FA_ERR_CUDA;
+  if (!p.bias) maps[4] = maps[0];  // unused
   return cuda_rc(fa::launch_qmajor_tc(p, bf16, true, maps, st));
 }
 
@@ -405,11 +410,13 @@ int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == FA_F32) return cuda_rc(fa::launch_fwd_f32(p, st));
   const bool bf16 = dtype == FA_BF16;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], v, p, bf16, fa::kStepKV))
     return FA_ERR_CUDA;
   maps[3] = maps[0];
+  if (p.bias ? !make_bias_map(&maps[4], p, bf16, true) : false) return FA_ERR_CUDA;
+  if (!p.bias) maps[4] = maps[0];  // unused
   return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, st));
 }
 
@@ -553,11 +560,12 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
   p.lse_out = lse;
   if ((rc = status_ptr(&p.status))) return rc;
   const bool bf16 = dtype == FA_BF16;
-  CUtensorMap maps[4];
+  CUtensorMap maps[5];
   if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], v, p, bf16, fa::kStepKV))
     return FA_ERR_CUDA;
   maps[3] = maps[0];
+  maps[4] = maps[0];  // no attention bias on packed input
   return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, static_cast<cudaStream_t>(stream)));
 }
 

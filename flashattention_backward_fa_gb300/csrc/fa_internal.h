@@ -149,13 +149,6 @@ __device__ __forceinline__ void alibi_ramp16(uint32_t (&sr)[16], float slope) {
   for (int e = 0; e < 16; ++e) sr[e] = __float_as_uint(fmaf(slope, (float)(kX0 + e), __uint_as_float(sr[e])));
 }
 
-// Start of the bias row of local query row i in unit u (elements of T).
-template <typename T>
-__device__ __forceinline__ const T* bias_row(const AttnParams& p, const Unit& u, int i) {
-  return static_cast<const T*>(p.bias) + (long long)u.b * p.bias_sb + (long long)u.h * p.bias_sh +
-         (long long)(u.row0 + i) * p.bias_sn;
-}
-
 // 16-bit value (bf16 or fp16 bits in the low half) to fp32.
 template <bool kBf16>
 __device__ __forceinline__ float h16_bits_to_f32(uint32_t bits) {

@@ -51,7 +51,7 @@ constexpr int kModeFwd = 0;
 constexpr int kModeDq = 1;
 constexpr int kQThreads = 640;  // 4 role warps + 4 row-math warpgroups
 
-template <int D, int kMode>
+template <int D, int kMode, bool kBias = false>
 struct QCfg {
   static constexpr bool kDq = kMode == kModeDq;
   static constexpr int kPanels = D / 64;
@@ -61,8 +61,15 @@ struct QCfg {
   // forward: per-step chunk maxima [2 steps][4 warpgroups][rows], then the
   // final partial sums [4 warpgroups][rows]
   static constexpr uint32_t kStats = kDq ? 0 : (2 * 4 + 4) * kRowsQ * 4;
-  static constexpr int kNE = kDq ? 2 : (D == 64 ? 4 : 3);      // ring E stages
-  static constexpr int kNL = kDq ? (D == 64 ? 4 : 3) : 2;      // ring L stages
+  // ring depths; with an attention bias the deeper ring gives up a stage (d = 128)
+  // to make room for the bias tile
+  static constexpr int kNE = kDq ? 2 : (D == 64 ? 4 : (kBias ? 2 : 3));  // ring E stages
+  static constexpr int kNL = kDq ? (D == 64 ? 4 : (kBias ? 2 : 3)) : 2;  // ring L stages
+  // attention bias of a step: 128 query rows x 128 keys, 16-bit, as two
+  // 128-byte-swizzled panels of 64 keys (one buffer, refilled once the row
+  // math has copied its segments to registers)
+  static constexpr uint32_t kBiasPanel = 128 * 128;
+  static constexpr uint32_t kBiasTile = kBias ? 2 * kBiasPanel : 0;
   // S buffers in TMEM: two beside the dP buffer in the dQ kernel; three in the
   // forward, which has no dP.
   static constexpr int kSBuf = kDq ? 2 : 3;
@@ -70,7 +77,8 @@ struct QCfg {
   static constexpr uint32_t oDO = oQ + kTile;
   static constexpr uint32_t oE = kResident;
   static constexpr uint32_t oL = oE + kNE * kTile;
-  static constexpr uint32_t oStats = oL + kNL * kTile;         // forward: row-statistics exchange
+  static constexpr uint32_t oBias = oL + kNL * kTile;
+  static constexpr uint32_t oStats = oBias + kBiasTile;         // forward: row-statistics exchange
   static constexpr uint32_t oBar = oStats + kStats;
   static constexpr int bRes = 0;
   static constexpr int bEFull = 1;
@@ -86,7 +94,9 @@ struct QCfg {
   static constexpr int bStats = bDrain + 3;                    // forward: final sums exchanged
   static constexpr int bXchg = bStats + 1;                     // [2] forward: chunk maxima of step it exchanged
   static constexpr int bODone = bXchg + 2;                     // forward: O MMA of a step done
-  static constexpr int kBars = bODone + 1;
+  static constexpr int bBFull = bODone + 1;                    // bias tile landed
+  static constexpr int bBEmpty = bBFull + 1;                   // row math has copied the bias tile
+  static constexpr int kBars = bBEmpty + 1;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
   static constexpr uint32_t oFlags = (oAbort + 8 + 15) & ~15u;  // [buffer][16 warps] split votes
@@ -98,6 +108,10 @@ struct QCfg {
 // more than this (log2 units), bounding relative probabilities by 2^8.
 constexpr float kRescaleLog2 = 8.f;
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -108,8 +122,8 @@ template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi, bool kBias>
 __global__ void __launch_bounds__(kQThreads, 1)
     qmajor_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmDO) {
-  using C = QCfg<D, kMode>;
+                  const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmBias) {
+  using C = QCfg<D, kMode, kBias>;
   constexpr bool kDq = kMode == kModeDq;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -172,6 +186,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(bar(C::bXchg), 512);
     mbar_init(bar(C::bXchg + 1), 512);
     mbar_init(bar(C::bODone), 1);
+    mbar_init(bar(C::bBFull), 1);
+    mbar_init(bar(C::bBEmpty), 512);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -184,6 +200,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     if (kDq) prefetch_tmap(&tmDO);
+    if (kBias) prefetch_tmap(&tmBias);
   }
   tc_fence_before();
   __syncthreads();
@@ -203,7 +220,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tma_load_4d(sb + C::oQ + pn * C::kPanel, &tmQ, bar(C::bRes), 64 * pn, u.row0 + i0, h, b);
         if (kDq) tma_load_4d(sb + C::oDO + pn * C::kPanel, &tmDO, bar(C::bRes), 64 * pn, u.row0 + i0, h, b);
       }
-      int issuedE = 0, issuedL = 0;
+      int issuedE = 0, issuedL = 0, issuedB = 0;
       bool ok = true;
       for (int it = 0; ok && it < nsteps; ++it) {
         const int jj = key_block(it);
@@ -224,6 +241,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tma_load_4d(sb + C::oL + sl * C::kTile + pn * C::kPanel, mL, bar(C::bLFull + sl), 64 * pn, u.row0 + jj,
                       h, b);
         issuedL = it + 1;
+        if constexpr (kBias) {
+          // the step's bias tile, once the row math has copied the previous one
+          if (!mbar_wait(bar(C::bBEmpty), (it & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::bBFull), C::kBiasTile);
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_4d(sb + C::oBias + pn * C::kBiasPanel, &tmBias, bar(C::bBFull), jj + 64 * pn, u.row0 + i0,
+                        p.bias_sh ? h : 0, p.bias_sb ? b : 0);
+          issuedB = it + 1;
+        }
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
@@ -232,6 +261,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           mbar_wait_drain(bar(C::bEFull + it % C::kNE), (it / C::kNE) & 1, p.status);
         for (int li = max(0, issuedL - C::kNL); li < issuedL; ++li)
           mbar_wait_drain(bar(C::bLFull + li % C::kNL), (li / C::kNL) & 1, p.status);
+        if (issuedB > 0) mbar_wait_drain(bar(C::bBFull), (issuedB - 1) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -364,9 +394,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
     const float inv_scale = kBias ? 1.f / p.scale : 0.f;
-    // this row's attention bias (null past the sequence: those rows store nothing)
-    const uint16_t* brow = nullptr;
-    if constexpr (kBias) brow = i < Nl ? bias_row<uint16_t>(p, u, i) : nullptr;
     float mref = -INFINITY, lsum = 0.f;
     float* xchg = reinterpret_cast<float*>(smem + C::oStats);
     bool ok = true;
@@ -374,35 +401,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int bb = it % C::kSBuf, xb = it & 1;
       const int base = key_block(it) + 32 * c;
       const uint32_t tSc = tS + lane_off + 128 * bb + 32 * c;
-      // The bias of this chunk's 32 keys, loaded before the wait for S so that
-      // its latency overlaps it: four 16-byte loads, or per-key loads where the
-      // chunk runs past the last key.
+      // This row's bias over the chunk's 32 keys (four 16-byte pieces of the
+      // swizzled tile; zeros past N), copied to registers so that the buffer is
+      // released, and the next step's tile loads, before this step's row math.
       uint32_t bw[16];
       if constexpr (kBias) {
-        // pull the segment of two steps ahead into L2 (64 bytes, within one line)
-        if (brow != nullptr && it + 2 < nsteps) {
-          const int ahead = key_block(it + 2) + 32 * c;
-          if (ahead < p.N) asm volatile("prefetch.global.L2 [%0];" ::"l"(brow + ahead));
+        if (!warp_wait<kRowMathPoll>(bar(C::bBFull), it & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
         }
-        if (brow != nullptr && base + 32 <= p.N) {
-          const uint4* src = reinterpret_cast<const uint4*>(brow + base);
+        const uint32_t rowa = sb + C::oBias + (uint32_t)(c >> 1) * C::kBiasPanel + (uint32_t)il * 128;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint4 v4 = __ldg(src + t);
-            bw[4 * t] = v4.x;
-            bw[4 * t + 1] = v4.y;
-            bw[4 * t + 2] = v4.z;
-            bw[4 * t + 3] = v4.w;
-          }
-        } else {
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int j = base + 2 * x;
-            const uint32_t lo = (brow != nullptr && j < p.N) ? __ldg(brow + j) : 0u;
-            const uint32_t hi = (brow != nullptr && j + 1 < p.N) ? __ldg(brow + j + 1) : 0u;
-            bw[x] = lo | (hi << 16);
-          }
-        }
+        for (int t = 0; t < 4; ++t)
+          ld_shared_v4(rowa + ((uint32_t)((4 * (c & 1) + t) ^ (il & 7)) << 4), bw[4 * t], bw[4 * t + 1],
+                       bw[4 * t + 2], bw[4 * t + 3]);
+        warp_arrive(bar(C::bBEmpty));
       }
       if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it / C::kSBuf) & 1, abort_flag, p.status)) {
         ok = false;
@@ -692,7 +705,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 template <int D, bool kBf16, int kMode, bool kDrop, bool kAlibi, bool kBias>
 static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  using C = QCfg<D, kMode>;
+  using C = QCfg<D, kMode, kBias>;
   auto kern = qmajor_kernel<D, kBf16, kMode, kDrop, kAlibi, kBias>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -700,7 +713,7 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
   const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
   const int tiles = (rows + kRowsQ - 1) / kRowsQ;
   const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
-  kern<<<grid, kQThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3]);
+  kern<<<grid, kQThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4]);
   return cudaGetLastError();
 }
 
@@ -724,7 +737,9 @@ static cudaError_t launch_q_d(const AttnParams& p, bool dq_mode, const CUtensorM
   return dq_mode ? launch_q_m<D, kBf16, kModeDq>(p, maps, st) : launch_q_m<D, kBf16, kModeFwd>(p, maps, st);
 }
 
-// maps: Q, K, V, dO (Q/dO boxes of kRowsQ rows, K/V boxes of kStepKV rows).
+// maps: Q, K, V, dO (Q/dO boxes of kRowsQ rows, K/V boxes of kStepKV rows), and
+// the attention bias (boxes of 128 rows x 64 keys, 128-byte swizzle; any valid
+// map when p.bias is null).
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st) {
   if (p.d == 128)
