@@ -39,8 +39,10 @@ def counted_flops(w) -> float:
     """10*N^2*d per head, halved under causal; windowed: 10*d per allowed pair."""
     if w.window > 0:
         W = min(w.window, w.N)
+        # causal: keys (i - W, i]; without the causal mask the window is one-sided,
+        # keys (i - W, N)
         pairs = (W * (W + 1) // 2 + (w.N - W) * W) if w.causal else sum(
-            min(w.N, i + w.window) for i in range(w.N))
+            w.N - max(0, i - w.window + 1) for i in range(w.N))
         return 10.0 * w.d * pairs * w.B * w.H
     per_head = 10.0 * w.N * w.N * w.d
     return w.B * w.H * (per_head / 2 if w.causal else per_head)
