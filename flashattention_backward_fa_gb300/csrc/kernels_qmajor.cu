@@ -445,15 +445,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld16(tSc + 16, sr2[1]);
         tmem_ld_wait16x2(sr2[0], sr2[1]);
       }
+      // attention bias, in score units (the dQ kernel's second half follows its load)
+      if constexpr (kBias) {
+        bias_fold16_regs<kBf16>(sr2[0], bw, inv_scale);
+        if constexpr (!kDq) bias_fold16_regs<kBf16>(sr2[1], bw + 8, inv_scale);
+      }
       // ALiBi: where every allowed key of this chunk lies on one side of the
       // diagonal (always under a causal mask), the bias -m|i - j| is a row
       // constant plus a ramp over the chunk's columns: the ramp goes into the
       // raw scores (one FMA a score) and the constant, rc2 (log2 domain), into
       // the exp2 addend. A chunk that straddles the diagonal folds |i - j| in.
-      if constexpr (kBias) {
-        bias_fold16_regs<kBf16>(sr2[0], bw, inv_scale);
-        if constexpr (!kDq) bias_fold16_regs<kBf16>(sr2[1], bw + 8, inv_scale);
-      }
       float rc2 = 0.f, ramp = 0.f;
       bool straddle = false;
       if constexpr (kAlibi) {
