@@ -430,3 +430,32 @@ def flash_attn_func(q, k, v, causal=False, window=0, dropout_p=0.0, softmax_scal
     v = v if v.stride() == q.stride() else _match_layout(v, q)
     return _FlashAttnFunc.apply(q, k, v, softmax_scale, causal, window, dropout_p, seed, offset, deterministic,
                                 alibi_slopes, attn_bias)
+
+
+class _FlashAttnVarlenFunc(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens, max_seqlen, scale, causal, window, deterministic, alibi_slopes):
+        o, lse = varlen_attention_forward(q, k, v, cu_seqlens, max_seqlen, scale, causal, window, alibi_slopes)
+        ctx.save_for_backward(q, k, v, o, lse, cu_seqlens)
+        ctx.cfg = (max_seqlen, scale, causal, window, deterministic, alibi_slopes)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, cu_seqlens = ctx.saved_tensors
+        max_seqlen, scale, causal, window, deterministic, alibi_slopes = ctx.cfg
+        if do.stride() != q.stride():
+            do = _match_layout(do, q)
+        dq, dk, dv = varlen_attention_backward(q, k, v, o, do, lse, cu_seqlens, max_seqlen, scale, causal, window,
+                                               deterministic, alibi_slopes)
+        return dq, dk, dv, None, None, None, None, None, None, None
+
+
+def flash_attn_varlen_func(q, k, v, cu_seqlens, max_seqlen, causal=False, window=0, softmax_scale=None,
+                           deterministic=True, alibi_slopes=None):
+    """Attention over packed sequences ([total, H, D] tensors, int32 cu_seqlens on the
+    device) with autograd (forward fa_varlen_fwd, backward fa_varlen_bwd)."""
+    k = k if k.stride() == q.stride() else _match_layout(k, q)
+    v = v if v.stride() == q.stride() else _match_layout(v, q)
+    return _FlashAttnVarlenFunc.apply(q, k, v, cu_seqlens, int(max_seqlen), softmax_scale, causal, window,
+                                      deterministic, alibi_slopes)

@@ -115,3 +115,19 @@ def test_varlen_rejects_unsupported():
     with pytest.raises(fa.FaError) as e:
         fa.fa_varlen_bwd(qh, qh, qh, qh, qh, lse, qh.clone(), qh.clone(), qh.clone(), cu, 16, ws)
     assert e.value.code == -4
+
+
+def test_varlen_autograd_function():
+    lengths = [100, 1, 257, 64]
+    H, d = 2, 64
+    q, k, v, do, cu = (t.cuda() for t in make_varlen_inputs(lengths, H, d, "f16", seed=41))
+    msl = max(lengths)
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = fa.flash_attn_varlen_func(qa, ka, va, cu, msl, causal=True)
+    out.backward(do)
+    o, lse = fa.varlen_attention_forward(q, k, v, cu, msl, causal=True)
+    g = fa.varlen_attention_backward(q, k, v, o, do, lse, cu, msl, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.detach(), o)
+    for a, b in zip((qa.grad, ka.grad, va.grad), g):
+        assert torch.equal(a, b)
