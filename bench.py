@@ -247,7 +247,21 @@ def time_ours(w, steps, warmup, deterministic, world):
     f1.record(stream)
     torch.cuda.synchronize()
     fwd_ms = f0.elapsed_time(f1) / e2e_steps
-    return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, fwd_ms=fwd_ms)
+    # The other dQ variant on the same inputs (its own workspace), timed the same
+    # way, so that one line reports both.
+    ws_other = fa.alloc_workspace(q, not deterministic)
+    for _ in range(max(3, warmup)):
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_other, **kw, deterministic=not deterministic, stream=stream)
+    torch.cuda.synchronize()
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for _ in range(steps):
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_other, **kw, deterministic=not deterministic, stream=stream)
+    v1.record(stream)
+    torch.cuda.synchronize()
+    other_ms = v0.elapsed_time(v1) / steps
+    return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, fwd_ms=fwd_ms,
+                other_ms=other_ms)
 
 
 def time_oracle(w, max_seconds=20.0):
@@ -352,6 +366,9 @@ def main():
         "forward": {"ms": r["fwd_ms"], "tflops": 0.4 * flops / (r["fwd_ms"] * 1e-3) / 1e12,
                     "bwd_over_fwd_speed": (flops / (r["ms"] * 1e-3)) / (0.4 * flops / (r["fwd_ms"] * 1e-3))},
         "clocks": r["clocks"],
+        # the dQ variant not in `value` (atomic when value is deterministic), same workload
+        "other_dq_mode": {"dq_mode": "atomic" if det else "deterministic", "ms_per_step": r["other_ms"],
+                          "value": flops / (r["other_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s"},
     }
     if rank == 0 and not a.no_cpu_baseline:
         tf, sample, cores, _ = time_oracle(w)
