@@ -53,7 +53,9 @@ struct KVCfg {
   // attention bias tile of a step: 64 query rows x 128 keys, 16-bit, unswizzled
   static constexpr uint32_t kBiasTile = kBias ? kStepQ * kRowsKV * 2 : 0;
   static constexpr uint32_t kStageBytes = 2 * kQTile + 2 * kStepQ * 4 + kBiasTile;
-  static constexpr uint32_t kFixed = 2 * kKVTile + kImgBytes + 512 + 1024 + 128;
+  // (+128: alignment of the bias tiles, only when there are any; at d = 128 with
+  // atomic dQ the budget holds exactly three stages without it)
+  static constexpr uint32_t kFixed = 2 * kKVTile + kImgBytes + 512 + 1024 + (kBias ? 128 : 0);
   static constexpr int kNSraw = (int)((227u * 1024u - kFixed) / kStageBytes);
   static constexpr int kNS = kNSraw > 4 ? 4 : kNSraw;          // Q/dO pipeline stages
   static constexpr uint32_t oK = 0;
@@ -63,7 +65,7 @@ struct KVCfg {
   static constexpr uint32_t oImg = oDO + kNS * kQTile;
   static constexpr uint32_t oL = oImg + kImgBytes;
   static constexpr uint32_t oD = oL + kNS * kStepQ * 4;
-  static constexpr uint32_t oB = (oD + kNS * kStepQ * 4 + 127) & ~127u;
+  static constexpr uint32_t oB = kBias ? (oD + kNS * kStepQ * 4 + 127) & ~127u : oD + kNS * kStepQ * 4;
   static constexpr uint32_t oBar = oB + kNS * kBiasTile;
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
@@ -84,6 +86,7 @@ struct KVCfg {
   static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
   static constexpr uint32_t kSmem = oFlags + 64 + 1024;        // + slack for 1024-byte alignment
   static_assert(kNS >= 2, "shared memory budget leaves fewer than two Q/dO stages");
+  static_assert(kBias || kNS >= (kAtomic && D == 128 ? 3 : 4), "Q/dO pipeline shallower than designed");
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
 };
 
