@@ -51,36 +51,41 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def drop_threshold(p: float) -> int:
-    """Integer threshold T = floor(p * 2**32): a word u is kept iff u >= T."""
+    """16-bit threshold T = floor(p * 2**16): a 16-bit value u is kept iff u >= T."""
     if not (0.0 <= p < 1.0):
         raise ValueError("dropout probability must lie in [0, 1)")
-    return int(np.floor(np.float64(p) * 4294967296.0))
+    return int(np.floor(np.float64(p) * 65536.0))
 
 
 def keep_mask(b: int, h: int, H: int, N: int, rows, seed: int, offset: int, p: float):
     """Boolean keep-mask Z[i, j] for query rows ``rows`` and all N keys of head (b, h).
 
-    Convention of this project (the pages leave it open):
+    Convention of this project (the pages leave it open). One Philox call
+    serves eight consecutive keys of one query, each taking a 16-bit half of
+    an output word:
       * key     = (lo32(seed), hi32(seed))
-      * group   g = ((b*H + h)*N + i) * ceil(N/4) + floor(j/4)
+      * group   g = ((b*H + h)*N + i) * ceil(N/8) + floor(j/8)
       * counter = (lo32(g), hi32(g), lo32(offset), hi32(offset))
-      * the word for key j is output word (j mod 4)
-      * keep  <=>  word >= floor(p * 2**32)
+      * the value for key j is half (j mod 2) of output word ((j mod 8) div 2):
+        the low 16 bits for even j, the high 16 bits for odd j
+      * keep  <=>  value >= floor(p * 2**16)
     With p == 0 every entry is kept.
     """
     rows = np.asarray(rows, dtype=np.int64)
     if p == 0.0:
         return np.ones((rows.size, N), dtype=bool)
     T = np.uint32(drop_threshold(p))
-    n4 = (N + 3) // 4
-    grp = np.arange(n4, dtype=np.uint64)
+    n8 = (N + 7) // 8
+    grp = np.arange(n8, dtype=np.uint64)
     g = ((np.uint64(b * H + h) * np.uint64(N) + rows.astype(np.uint64))[:, None]
-         * np.uint64(n4) + grp[None, :])
+         * np.uint64(n8) + grp[None, :])
     seed = int(seed) & 0xFFFFFFFFFFFFFFFF
     offset = int(offset) & 0xFFFFFFFFFFFFFFFF
     words = philox4x32_10(g & _MASK32, g >> np.uint64(32),
                           np.uint64(offset & 0xFFFFFFFF), np.uint64(offset >> 32),
                           np.uint64(seed & 0xFFFFFFFF), np.uint64(seed >> 32))
-    # words[w][r, q] is the word for key 4q + w; interleave to key order.
-    full = np.stack(words, axis=-1).reshape(rows.size, 4 * n4)[:, :N]
+    # key 8q + 2w + half takes half `half` of words[w][r, q]
+    w4 = np.stack(words, axis=-1)                                  # [rows, n8, 4]
+    halves = np.stack([w4 & np.uint32(0xFFFF), w4 >> np.uint32(16)], axis=-1)  # [rows, n8, 4, 2]
+    full = halves.reshape(rows.size, 8 * n8)[:, :N]
     return full >= T

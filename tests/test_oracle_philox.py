@@ -13,8 +13,9 @@ from oracle.philox import drop_threshold, keep_mask, philox4x32_10
 
 def test_threshold():
     assert drop_threshold(0.0) == 0
-    assert drop_threshold(0.5) == 1 << 31
-    assert drop_threshold(0.1) == int(np.floor(0.1 * 2.0 ** 32))
+    assert drop_threshold(0.5) == 1 << 15
+    assert drop_threshold(0.1) == 6553  # floor(0.1 * 2**16)
+    assert drop_threshold(1.0 - 2.0 ** -20) == 65535
     with pytest.raises(ValueError):
         drop_threshold(1.0)
 
@@ -68,16 +69,18 @@ def test_keep_fraction(p):
 
 
 def test_mask_layout_convention():
-    """Mask entry (b, h, i, j) is word j%4 of Philox at counter g = ((b*H+h)*N+i)*ceil(N/4)+j//4."""
+    """Mask entry (b, h, i, j) is 16-bit half j%2 (low half for even j) of word (j%8)//2 of
+    Philox at counter g = ((b*H+h)*N+i)*ceil(N/8)+j//8, kept iff >= floor(p * 2**16)."""
     B, H, N, p, seed, off = 2, 3, 37, 0.3, (7 << 32) | 99, (5 << 32) | 11
     rng = np.random.default_rng(1)
     T = drop_threshold(p)
-    n4 = (N + 3) // 4
-    for _ in range(200):
+    n8 = (N + 7) // 8
+    for _ in range(300):
         b, h, i, j = (int(rng.integers(0, x)) for x in (B, H, N, N))
-        g = ((b * H + h) * N + i) * n4 + j // 4
+        g = ((b * H + h) * N + i) * n8 + j // 8
         w = philox4x32_10(g & 0xFFFFFFFF, g >> 32, off & 0xFFFFFFFF, off >> 32, seed & 0xFFFFFFFF, seed >> 32)
-        assert keep_mask(b, h, H, N, [i], seed, off, p)[0, j] == (int(w[j % 4]) >= T)
+        value = (int(w[(j % 8) // 2]) >> (16 * (j % 2))) & 0xFFFF
+        assert keep_mask(b, h, H, N, [i], seed, off, p)[0, j] == (value >= T)
 
 
 def test_mask_depends_on_seed_and_offset():
