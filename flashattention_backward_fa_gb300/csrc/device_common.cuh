@@ -538,69 +538,73 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 struct DropoutParams {
-  uint32_t threshold;  // keep iff word >= threshold; 0 disables dropout
+  uint32_t on;         // dropout enabled (dropout_p > 0)
+  uint32_t threshold;  // keep iff a 16-bit value >= threshold = floor(p * 2^16)
   float rp;            // 1 / (1 - p)
   uint32_t seed_lo, seed_hi, off_lo, off_hi;
   uint32_t bh_off;     // added to the launch's (batch * H + head) index: a launch over a
                        // slice of the heads or batches draws the full problem's masks
 };
 
-// Keep decision for element (bh, i, j) of an N x N head: word (j mod 4) of
-// Philox at counter (g, offset), g = (bh * N + i) * ceil(N/4) + j/4.
+// Dropout keep decisions. One Philox call serves eight consecutive keys of one
+// query: key 8q + 2w + h takes 16-bit half h (low for even keys) of output word
+// w, at counter (g, offset) with g = (bh * N + i) * ceil(N/8) + q, and is kept
+// iff that half >= threshold.
+
+// The eight keep bits of one Philox output (bit 2w + h <-> half h of word w).
+__device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
+  return (uint32_t)((w.x & 0xFFFFu) >= T) | ((uint32_t)((w.x >> 16) >= T) << 1) |
+         ((uint32_t)((w.y & 0xFFFFu) >= T) << 2) | ((uint32_t)((w.y >> 16) >= T) << 3) |
+         ((uint32_t)((w.z & 0xFFFFu) >= T) << 4) | ((uint32_t)((w.z >> 16) >= T) << 5) |
+         ((uint32_t)((w.w & 0xFFFFu) >= T) << 6) | ((uint32_t)((w.w >> 16) >= T) << 7);
+}
+
+__device__ __forceinline__ uint4 philox_at(const DropoutParams& dp, uint64_t g) {
+  return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi), dp.seed_lo, dp.seed_hi);
+}
+
+// Keep decision for element (bh, i, j) of an N x N head.
 __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t bh, int N, int i, int j) {
-  const uint64_t n4 = (uint64_t)((N + 3) >> 2);
-  const uint64_t g = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j >> 2);
-  const uint4 w = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi),
-                                dp.seed_lo, dp.seed_hi);
-  const uint32_t sel = (j & 3) == 0 ? w.x : (j & 3) == 1 ? w.y : (j & 3) == 2 ? w.z : w.w;
-  return sel >= dp.threshold;
+  const uint64_t n8 = (uint64_t)((N + 7) >> 3);
+  const uint4 w = philox_at(dp, ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n8 + (uint64_t)(j >> 3));
+  const int ww = (j >> 1) & 3;
+  const uint32_t word = ww == 0 ? w.x : ww == 1 ? w.y : ww == 2 ? w.z : w.w;
+  return ((j & 1) ? (word >> 16) : (word & 0xFFFFu)) >= dp.threshold;
 }
 
 // Keep bits (bit x <-> query i0 + x) of 32 consecutive queries for this lane's
 // key j, computed by the whole (converged) warp, whose lanes hold 32
-// consecutive keys with j % 4 == lane % 4. One Philox call yields the words of
-// four keys (one 4-lane group) for one query, so lane 4g + r evaluates the
-// queries i0 + 4t + r (t < 8) for its group and the four lanes trade their
-// results through shuffles: 8 calls per lane instead of 32.
+// consecutive keys with j % 8 == lane % 8. One Philox call yields the bits of
+// eight keys (one 8-lane group) for one query, so lane 8g + r evaluates the
+// queries i0 + 8t + r (t < 4) for its group and the eight lanes trade their
+// results through shuffles: 4 calls per lane instead of 32.
 static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
-  const int lane = threadIdx.x & 31, r = lane & 3;
-  const uint64_t n4 = (uint64_t)((N + 3) >> 2);
+  const int lane = threadIdx.x & 31, r = lane & 7;
+  const uint64_t n8 = (uint64_t)((N + 7) >> 3);
   const uint64_t row0 = (uint64_t)(bh + dp.bh_off) * (uint64_t)N;
-  uint32_t mine = 0;  // nibble t: keep bits of the group's four keys for query i0 + 4t + r
+  uint32_t mine = 0;  // byte t: keep bits of the group's eight keys for query i0 + 8t + r
 #pragma unroll 1
-  for (int t = 0; t < 8; ++t) {
-    const uint64_t g = (row0 + (uint64_t)(i0 + 4 * t + r)) * n4 + (uint64_t)(j >> 2);
-    const uint4 w =
-        philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi), dp.seed_lo, dp.seed_hi);
-    const uint32_t nib = (uint32_t)(w.x >= dp.threshold) | ((uint32_t)(w.y >= dp.threshold) << 1) |
-                         ((uint32_t)(w.z >= dp.threshold) << 2) | ((uint32_t)(w.w >= dp.threshold) << 3);
-    mine |= nib << (4 * t);
-  }
+  for (int t = 0; t < 4; ++t)
+    mine |= keep_byte(philox_at(dp, (row0 + (uint64_t)(i0 + 8 * t + r)) * n8 + (uint64_t)(j >> 3)), dp.threshold)
+            << (8 * t);
   uint32_t bits = 0;
 #pragma unroll
-  for (int rs = 0; rs < 4; ++rs) {
-    const uint32_t v = __shfl_sync(0xffffffffu, mine, (lane & ~3) + rs);  // queries i0 + 4t + rs
+  for (int rs = 0; rs < 8; ++rs) {
+    const uint32_t v = __shfl_sync(0xffffffffu, mine, (lane & ~7) + rs);  // queries i0 + 8t + rs
 #pragma unroll
-    for (int t = 0; t < 8; ++t) bits |= ((v >> (4 * t + r)) & 1u) << (4 * t + rs);
+    for (int t = 0; t < 4; ++t) bits |= ((v >> (8 * t + r)) & 1u) << (8 * t + rs);
   }
   return bits;
 }
 
-// Keep bits (bit x <-> key j0 + x) of 32 consecutive keys for one query i; j0 % 4 == 0,
-// so each Philox call yields the words of four keys.
+// Keep bits (bit x <-> key j0 + x) of 32 consecutive keys for one query i;
+// j0 % 8 == 0, so each Philox call yields the bits of eight keys.
 static __device__ __noinline__ uint32_t keep_bits_for_query(const DropoutParams dp, uint32_t bh, int N, int i, int j0) {
-  const uint64_t n4 = (uint64_t)((N + 3) >> 2);
-  const uint64_t g0 = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n4 + (uint64_t)(j0 >> 2);
+  const uint64_t n8 = (uint64_t)((N + 7) >> 3);
+  const uint64_t g0 = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n8 + (uint64_t)(j0 >> 3);
   uint32_t bits = 0;
 #pragma unroll 1
-  for (int x = 0; x < 32; x += 4) {
-    const uint64_t g = g0 + (uint64_t)(x >> 2);
-    const uint4 w =
-        philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), dp.off_lo, dp.off_hi), dp.seed_lo, dp.seed_hi);
-    bits |= ((uint32_t)(w.x >= dp.threshold) | ((uint32_t)(w.y >= dp.threshold) << 1) |
-             ((uint32_t)(w.z >= dp.threshold) << 2) | ((uint32_t)(w.w >= dp.threshold) << 3))
-            << x;
-  }
+  for (int x = 0; x < 4; ++x) bits |= keep_byte(philox_at(dp, g0 + (uint64_t)x), dp.threshold) << (8 * x);
   return bits;
 }
 

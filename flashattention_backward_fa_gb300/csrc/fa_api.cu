@@ -153,8 +153,8 @@ void fill_params(AttnParams& p, int B, int H, int N, int d, fa_strides s, float 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
   p.window = window;
-  const double t = std::floor((double)dropout_p * 4294967296.0);
-  p.drop.threshold = dropout_p > 0.f ? (uint32_t)t : 0u;
+  p.drop.on = dropout_p > 0.f ? 1u : 0u;
+  p.drop.threshold = (uint32_t)std::floor((double)dropout_p * 65536.0);  // < 2^16 for dropout_p < 1
   p.drop.rp = 1.f / (1.f - dropout_p);
   p.drop.seed_lo = (uint32_t)seed;
   p.drop.seed_hi = (uint32_t)(seed >> 32);

@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(32 * kF32Warps) fwd_f32_kernel(const __grid_co
     if (j <= jhi) {
       pj = ex2_approx(fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) +
                       bias_log2_f32(p, b, h, i, j) - L2);
-      if (p.drop.threshold) pj = dropout_keep(p.drop, bh, p.N, i, j) ? pj * p.drop.rp : 0.f;
+      if (p.drop.on) pj = dropout_keep(p.drop, bh, p.N, i, j) ? pj * p.drop.rp : 0.f;
     }
     const int cnt = min(32, jhi - jb + 1);
     for (int t = 0; t < cnt; ++t) {
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dkdv_f32_kernel(const __gr
           bias_log2_f32(p, b, h, i, j) + nL2[i]);
       float dp = dot_row(vrow[w], row_ptr(p, p.dout, b, i, h), p.d);
       pt = pv;
-      if (p.drop.threshold) {
+      if (p.drop.on) {
         const bool keep = dropout_keep(p.drop, bh, p.N, i, j);
         pt = keep ? pv * p.drop.rp : 0.f;
         dp = keep ? dp * p.drop.rp : 0.f;
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid
           fmaf(-am, fabsf((float)(i - j)), dot_row(qrow[w], row_ptr(p, p.k, b, j, h), p.d) * p.scale_log2) +
           bias_log2_f32(p, b, h, i, j) + nL2);
       float dp = dot_row(grow[w], row_ptr(p, p.v, b, j, h), p.d);
-      if (p.drop.threshold) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
+      if (p.drop.on) dp = dropout_keep(p.drop, bh, p.N, i, j) ? dp * p.drop.rp : 0.f;
       ds = pv * (dp + nD);
     }
     const int cnt = min(32, jhi - jb + 1);

@@ -580,7 +580,7 @@ static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, c
 
 template <int D, bool kBf16, bool kAtomic, bool kBias>
 static cudaError_t launch_dkdv_b(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  const bool drop = p.drop.threshold != 0;
+  const bool drop = p.drop.on != 0;
   if (p.alibi)
     return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true, kBias>(p, maps, st)
                 : launch_dkdv_t<D, kBf16, kAtomic, false, true, kBias>(p, maps, st);

@@ -720,7 +720,7 @@ static cudaError_t launch_q_t(const AttnParams& p, const CUtensorMap* maps, cuda
 
 template <int D, bool kBf16, int kMode, bool kBias>
 static cudaError_t launch_q_b(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  const bool drop = p.drop.threshold != 0;
+  const bool drop = p.drop.on != 0;
   if (p.alibi)
     return drop ? launch_q_t<D, kBf16, kMode, true, true, kBias>(p, maps, st)
                 : launch_q_t<D, kBf16, kMode, false, true, kBias>(p, maps, st);

@@ -21,14 +21,16 @@
  * window > 0 keeps pairs j > i - window; with causal this is the two-sided
  * sliding window i - window < j <= i. window == 0 means no window.
  *
- * Dropout. 0 <= dropout_p < 1. The keep decision of element (b, h, i, j) is
- * word (j mod 4) of Philox4x32-10 (Salmon et al., SC'11) with
+ * Dropout. 0 <= dropout_p < 1. The keep decision of element (b, h, i, j)
+ * uses Philox4x32-10 (Salmon et al., SC'11) with
  *   key     = (lo32(seed), hi32(seed))
  *   counter = (lo32(g), hi32(g), lo32(offset), hi32(offset)),
- *   g       = ((b*H + h)*N + i) * ceil(N/4) + floor(j/4)
- * and the element is kept iff that word >= floor(dropout_p * 2^32). Kept
- * elements are scaled by 1/(1 - dropout_p). fa_fwd and fa_bwd draw the same
- * mask for the same (seed, offset).
+ *   g       = ((b*H + h)*N + i) * ceil(N/8) + floor(j/8)
+ * One call serves eight keys: key j takes 16-bit half (j mod 2) (the low half
+ * for even j) of output word ((j mod 8) div 2), and the element is kept iff
+ * that half >= floor(dropout_p * 2^16). Kept elements are scaled by
+ * 1/(1 - dropout_p). fa_fwd and fa_bwd draw the same mask for the same
+ * (seed, offset).
  *
  * Layout. Q, K, V, O, dO, dQ, dK, dV share one element-stride triple
  * fa_strides {b, n, h}: element (b, i, h, k) lives at b*s.b + i*s.n + h*s.h + k
