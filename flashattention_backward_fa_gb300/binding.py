@@ -63,6 +63,7 @@ def load_library(path: str = LIB_PATH):
     lib.fa_bwd_stage.argtypes, lib.fa_bwd_stage.restype = [i] + bwd_args, i
     lib.fa_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
     lib.fa_get_device_status.restype = i
+    lib.fa_selftest_timeout.argtypes, lib.fa_selftest_timeout.restype = [vp, vp], i
     lib.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, FaStrides, i, f, i, i, f, u64, u64, vp]
     lib.fa_bwd_noalloc.restype = i
     i64 = ctypes.c_int64
@@ -290,6 +291,17 @@ def fa_get_device_status(clear: bool = True) -> int:
     if code not in (0, -6):
         _check(code)
     return int(s.value)
+
+
+def fa_selftest_timeout(device=None, stream=None) -> int:
+    """Run the bounded-wait self-test kernel (about 8 s) and return its outcome bits.
+
+    Bit w is set when warp w's wait gave up (3 = both). The device status word
+    then carries the timeout bit: read and clear it with fa_get_device_status().
+    """
+    outcome = torch.zeros(1, dtype=torch.int32, device=device if device is not None else "cuda")
+    _check(load_library().fa_selftest_timeout(outcome.data_ptr(), _stream(stream)))
+    return int(outcome.item())
 
 
 def alloc_workspace(q: torch.Tensor, deterministic: bool = True) -> torch.Tensor:

@@ -427,7 +427,59 @@ int check_bwd_args(int B, int H, int N, int d, fa_strides strides, fa_dtype dtyp
 
 }  // namespace fa
 
+namespace {
+
+// Failure-detection self-test (fa_selftest_timeout): one CTA of two warps holds
+// 32 TMEM columns and waits on an mbarrier that nothing ever arrives on. Warp 1
+// polls (test_wait), warp 0 blocks (try_wait), as the row-math and MMA-issuing
+// warps of the attention kernels do. The first wait to pass the wall-clock
+// limit sets the timeout bit and the CTA's abort flag; the other leaves at its
+// next abort check. Thread 0 then runs the bounded drain wait on the same
+// barrier, which gives up after the limit as well. Warp 0 frees TMEM and the
+// CTA exits, leaving the context usable.
+__global__ void __launch_bounds__(64, 1) selftest_timeout_kernel(unsigned int* status, int* outcome) {
+  __shared__ __align__(8) unsigned long long bar_word;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const uint32_t bar = fa::smem_u32(&bar_word);
+  if (threadIdx.x == 0) {
+    fa::mbar_init(bar, 1);
+    abort_flag = 0;
+    fa::fence_mbar_init();
+  }
+  if (warp == 0) {
+    fa::tmem_alloc(fa::smem_u32(&tmem_slot), 32);
+    fa::tmem_relinquish();
+  }
+  fa::tc_fence_before();
+  __syncthreads();
+  fa::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const bool ok = warp == 1 ? fa::warp_wait<true>(bar, 0, &abort_flag, status)
+                            : fa::warp_wait<false>(bar, 0, &abort_flag, status);
+  if ((threadIdx.x & 31) == 0) atomicOr(outcome, ok ? 0 : (1 << warp));
+  if (threadIdx.x == 0) fa::mbar_wait_drain(bar, 0, status);
+  fa::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fa::tc_fence_after();
+    fa::tmem_dealloc(tmem, 32);
+  }
+}
+
+}  // namespace
+
 extern "C" {
+
+int fa_selftest_timeout(int* outcome, void* stream) {
+  if (!outcome) return FA_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  int rc = status_ptr(&status);
+  if (rc) return rc;
+  selftest_timeout_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(status, outcome);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 int fa_get_device_status(unsigned int* status, int clear) {
   if (!status) return FA_ERR_INVALID_ARG;

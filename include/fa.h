@@ -253,6 +253,19 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
  * when the timeout bit is set, or FA_ERR_CUDA. This call synchronises the device. */
 int fa_get_device_status(unsigned int* status, int clear);
 
+/* Self-test of the failure detection (the bounded waits of the tensor-core
+ * kernels). Launches, on `stream`, one CTA of two warps that allocates 32 TMEM
+ * columns and waits on an mbarrier that nothing arrives on: one warp with the
+ * polling wait of the row-math warps, one with the blocking wait of the
+ * MMA-issuing warps. After the wall-clock limit of a wait (4 s) the kernel sets
+ * the timeout bit of the device status word and its CTA's abort flag, then
+ * runs the bounded drain wait (another 4 s), frees its TMEM and returns, so the
+ * context stays usable. `outcome` is a device int the caller zeroes; the kernel
+ * ORs in bit w for each warp w whose wait gave up (3 = both). Afterwards
+ * fa_get_device_status reports FA_ERR_TIMEOUT. Returns FA_OK, or FA_ERR_CUDA if
+ * the launch failed. No other state is touched; about 8 s of GPU time. */
+int fa_selftest_timeout(int* outcome, void* stream);
+
 /* Static string for an FA_* code. */
 const char* fa_strerror(int code);
 
