@@ -603,10 +603,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         uint32_t hv[8], ev[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) hv[x] = pack2<kBf16>(outv[2 * x], outv[2 * x + 1]);
-        // Residuals where the (relative) probability exceeds the split threshold;
-        // in the forward the probabilities are relative to mref, which keeps the
-        // test conservative.
-        const bool split_h = __any_sync(0xFFFFFFFFu, cmax > kSplitThreshold);
+        // Residuals where a probability can exceed the split threshold. In the
+        // forward the values are relative to the reference (exp(s - m)) and
+        // lsum, this warpgroup's sum over the keys seen so far including these
+        // columns, is a part of the final row sum: P = exp(s - m) / (full sum)
+        // <= cmax / lsum, whatever keys and reference moves come later.
+        const bool split_h = __any_sync(0xFFFFFFFFu, kDq ? cmax > kSplitThreshold : cmax > kSplitThreshold * lsum);
         lo_any |= split_h;
         if (split_h) {
 #pragma unroll
