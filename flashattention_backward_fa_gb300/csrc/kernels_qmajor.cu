@@ -503,7 +503,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if constexpr (kAlibi) cm += rc2;  // -inf stays -inf
         xchg[(xb * 4 + c) * kRowsQ + il] = cm;
         warp_arrive(bar(C::bXchg + xb));
-        if (!warp_wait<kRowMathPoll>(bar(C::bXchg + xb), (it >> 1) & 1, abort_flag, p.status)) {
+        // A blocking wait: the warps still computing their maxima share the
+        // schedulers with the ones waiting here, and a spinning wait would take
+        // their issue slots.
+        if (!warp_wait<false>(bar(C::bXchg + xb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -657,7 +660,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         float* xl = xchg + 8 * kRowsQ;
         xl[c * kRowsQ + il] = lsum;
         warp_arrive(bar(C::bStats));
-        ok = warp_wait<kRowMathPoll>(bar(C::bStats), 0, abort_flag, p.status);
+        ok = warp_wait<false>(bar(C::bStats), 0, abort_flag, p.status);
         float ltot = 0.f;
 #pragma unroll
         for (int g = 0; g < 4; ++g) ltot += xl[g * kRowsQ + il];
