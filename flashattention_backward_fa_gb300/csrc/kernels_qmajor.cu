@@ -92,8 +92,8 @@ struct QCfg {
   static constexpr int bAcc = bPFull + kSBuf;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
   static constexpr int bStats = bDrain + 3;                    // forward: final sums exchanged
-  static constexpr int bXchg = bStats + 1;                     // [2] forward: chunk maxima of step it exchanged
-  static constexpr int bODone = bXchg + 2;                     // forward: O MMA of a step done
+  static constexpr int bXchg = bStats + 1;                     // [2][4] forward: chunk maxima of step it exchanged (per row quarter)
+  static constexpr int bODone = bXchg + 8;                     // forward: O MMA of a step done
   static constexpr int bBFull = bODone + 1;                    // bias tile landed
   static constexpr int bBEmpty = bBFull + 1;                   // row math has copied the bias tile
   static constexpr int kBars = bBEmpty + 1;
@@ -183,8 +183,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(bar(C::bAcc), 1);
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bStats), 512);
-    mbar_init(bar(C::bXchg), 512);
-    mbar_init(bar(C::bXchg + 1), 512);
+    for (int x = 0; x < 8; ++x) mbar_init(bar(C::bXchg + x), 128);
     mbar_init(bar(C::bODone), 1);
     mbar_init(bar(C::bBFull), 1);
     mbar_init(bar(C::bBEmpty), 512);
@@ -502,11 +501,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         if constexpr (kAlibi) cm += rc2;  // -inf stays -inf
         xchg[(xb * 4 + c) * kRowsQ + il] = cm;
-        warp_arrive(bar(C::bXchg + xb));
+        // Rows 32 wq .. 32 wq + 31 are shared by the four warps with this wq (one
+        // per warpgroup, all on one scheduler): only they exchange.
+        warp_arrive(bar(C::bXchg + 4 * xb + wq));
         // A blocking wait: the warps still computing their maxima share the
         // schedulers with the ones waiting here, and a spinning wait would take
         // their issue slots.
-        if (!warp_wait<false>(bar(C::bXchg + xb), (it >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<false>(bar(C::bXchg + 4 * xb + wq), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
