@@ -11,7 +11,9 @@ halved under the causal mask, per step. Prints one JSON line.
 Under torchrun each rank runs the same workload on its own GPU (independent
 replicas: heads shard with no exchange, so there is no data-path collective);
 value = units of all ranks / max-over-ranks time. ``--impl reference`` times
-the float64 CPU oracle on a bounded sample of the same workload.
+the float64 CPU oracle on the host cores (rank 0 only): W warm-up and K timed
+steps, each the oracle backward of one head of the same workload, within a
+few minutes.
 """
 from __future__ import annotations
 
@@ -287,6 +289,46 @@ def time_oracle(w, max_seconds=20.0):
     return flops / el / 1e12, sample, cores, el / heads
 
 
+def run_reference_steps(w, steps, warmup, budget_s=150.0):
+    """The reference arm: the float64 oracle's backward of one head per step.
+
+    W untimed warm-up steps, then K timed steps, each the oracle backward of the
+    same single-head sample of the workload. If one head is so slow that K + W
+    steps would not fit in about budget_s seconds, fewer steps run (at least one
+    warm-up and one timed step) and the sample text says how many.
+    Returns (TFLOP/s, sample text, cores, seconds per head).
+    """
+    import numpy as np
+
+    import oracle
+    q, k, v, do = make_inputs(w.with_(B=1, H=1))
+    q, k, v, do = (t.float().numpy() for t in (q, k, v, do))
+    args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
+    O, L = oracle.forward(q, k, v, *args)
+
+    def step():
+        oracle.backward(q, k, v, O, do, L, *args)
+
+    t0 = time.perf_counter()
+    step()                                   # first warm-up step, also sizes the run
+    t_head = time.perf_counter() - t0
+    fit = max(2, int(budget_s / max(t_head, 1e-9)))
+    w_rest = min(max(warmup - 1, 0), fit // 4)
+    k_run = max(1, min(steps, fit - 1 - w_rest))
+    for _ in range(w_rest):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(k_run):
+        step()
+    el = time.perf_counter() - t0
+    flops = counted_flops(w.with_(B=1, H=1)) * k_run
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"{k_run} timed step(s) after {1 + w_rest} warm-up step(s); each step is the float64 oracle "
+              f"backward of one head (B=1,H=1,N={w.N},d={w.d}) of the workload, numpy/OpenBLAS")
+    del np
+    return flops / el / 1e12, sample, cores, el / k_run
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -323,7 +365,7 @@ def main():
     if a.impl == "reference":
         if rank != 0:
             return
-        tf, sample, cores, sec_per_head = time_oracle(w)
+        tf, sample, cores, sec_per_head = run_reference_steps(w, a.steps, a.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": a.gpus,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec_per_head * w.B * w.H * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

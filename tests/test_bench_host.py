@@ -49,3 +49,15 @@ def test_max_over_ranks_gloo_two_ranks():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 2.0), (1, 2.0)]
+
+
+def test_reference_arm_runs_warmup_and_timed_steps():
+    """--impl reference: W warm-up and K timed steps of the oracle, one head each."""
+    w = WORKLOADS["fp32_n128_d64"]
+    tf, sample, cores, sec = bench.run_reference_steps(w, steps=3, warmup=2)
+    assert tf > 0 and sec > 0 and cores >= 1
+    assert sample.startswith("3 timed step(s) after 2 warm-up step(s)")
+    # A budget too small for K + W steps keeps at least one of each and says so.
+    tf, sample, _, _ = bench.run_reference_steps(w, steps=50, warmup=10, budget_s=1e-9)
+    assert tf > 0
+    assert sample.startswith("1 timed step(s) after 1 warm-up step(s)")
