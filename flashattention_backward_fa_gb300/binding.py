@@ -125,7 +125,17 @@ def _same_layout(ref: torch.Tensor, *others: torch.Tensor):
         s2, st2 = _layout(o)
         if s2 != shp or (st2.b, st2.n, st2.h) != (st.b, st.n, st.h) or o.dtype != ref.dtype:
             raise ValueError("all [B, N, H, d] tensors must share shape, strides and dtype")
+        if o.device != ref.device:
+            raise ValueError("all tensors must live on the same CUDA device")
+    if ref.device.index is not None and ref.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensors live on {ref.device} but the current device is cuda:{torch.cuda.current_device()}"
+                         " (use torch.cuda.device(...))")
     return shp, st
+
+
+def _on_device(t: torch.Tensor, ref: torch.Tensor, name: str):
+    if not t.is_cuda or t.device != ref.device:
+        raise ValueError(f"{name} must be a CUDA tensor on {ref.device}")
 
 
 def _stream(stream):
@@ -180,6 +190,7 @@ def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, s
     (B, N, H, d), st = _same_layout(q, k, v, o)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _on_device(lse, q, "lse")
     lib = load_library()
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, st,
             _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
@@ -199,6 +210,8 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
     (B, N, H, d), st = _same_layout(q, k, v, o, do, dq, dk, dv)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _on_device(lse, q, "lse")
+    _on_device(workspace, q, "workspace")
     return (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
             default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p),
@@ -243,6 +256,7 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale=None, causal=False, wi
     (B, N, H, d), st = _same_layout(q, k, v, o, do, dq, dk, dv)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    _on_device(lse, q, "lse")
     _check(load_library().fa_bwd_noalloc(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
@@ -274,8 +288,8 @@ def fa_bwd_host(q, k, v, o, do, lse, dq, dk, dv, dev_buf, scale=None, causal=Fal
     (B, N, H, d), st = _host_layout(q, k, v, o, do, dq, dk, dv)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous() or lse.is_cuda:
         raise ValueError("lse must be a contiguous float32 CPU [B, H, N] tensor")
-    if not dev_buf.is_cuda:
-        raise ValueError("dev_buf must be device memory")
+    if not dev_buf.is_cuda or dev_buf.device.index not in (None, torch.cuda.current_device()):
+        raise ValueError("dev_buf must be device memory of the current device")
     _check(load_library().fa_bwd_host(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
@@ -340,9 +354,11 @@ def _varlen_layout(ref: torch.Tensor, cu_seqlens: torch.Tensor, *others: torch.T
     for o in others:
         if tuple(o.shape) != tuple(ref.shape) or o.stride() != ref.stride() or o.dtype != ref.dtype:
             raise ValueError("all packed tensors must share shape, strides and dtype")
+        _on_device(o, ref, "every packed tensor")
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_cuda \
             or not cu_seqlens.is_contiguous() or cu_seqlens.numel() < 2:
         raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor of nseq + 1 offsets")
+    _on_device(cu_seqlens, ref, "cu_seqlens")
     total, H, d = ref.shape
     return total, H, d, ref.stride(0), ref.stride(1), cu_seqlens.numel() - 1
 

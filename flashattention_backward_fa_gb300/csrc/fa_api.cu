@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "fa.h"
@@ -122,6 +123,26 @@ WsLayout ws_layout(int B, int H, int N, int d, int dtype, int deterministic) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every buffer a kernel touches must be memory of the current device (or
+// managed memory): a host or another device's pointer would make the kernels
+// fault. Checked last, after the cheap argument checks and before any launch.
+// Null entries are optional inputs that are absent.
+int check_device_ptrs(std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  for (const void* ptr : ptrs) {
+    if (!ptr) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+      cudaGetLastError();  // not a pointer the runtime knows: clear the (non-sticky) error
+      return FA_ERR_INVALID_ARG;
+    }
+    if (at.type == cudaMemoryTypeManaged) continue;
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
 
 // Validation shared by the forward and the backward. Returns FA_OK or an error.
 int check_common(int B, int H, int N, int d, fa_strides s, int dtype, float scale, int window, float dropout_p) {
@@ -369,6 +390,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   const WsLayout w = ws_layout(B, H, N, d, dtype, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
+  if ((rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, ex.alibi, ex.bias}))) return rc;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
   apply_extras(p, ex);
@@ -398,6 +420,7 @@ int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, in
   if ((rc = check_bias(ex.bias, ex.bias_st, N, dtype, scale))) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if ((rc = check_device_ptrs({q, k, v, o, lse, ex.alibi, ex.bias}))) return rc;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
   apply_extras(p, ex);
@@ -605,6 +628,7 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
   if (rc) return rc;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
+  if ((rc = check_device_ptrs({q, k, v, o, lse, cu_seqlens, alibi_slopes}))) return rc;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -637,6 +661,7 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
   const VarlenWs w = varlen_ws_layout(nseq, max_seqlen, total, H, d, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
+  if ((rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, alibi_slopes}))) return rc;
   p.q = q;
   p.k = k;
   p.v = v;

@@ -46,7 +46,11 @@
  *
  * Ownership and execution. The caller owns every buffer; the library never
  * allocates device memory and keeps no per-call state. All pointers are
- * device pointers. Calls are asynchronous on `stream` (a cudaStream_t, NULL =
+ * device pointers of the current device (or managed memory), except the host
+ * buffers of fa_bwd_host. After the other argument checks, and before anything
+ * is launched, every buffer is looked up with cudaPointerGetAttributes: a host
+ * pointer, another device's pointer or an unknown address returns
+ * FA_ERR_INVALID_ARG. Calls are asynchronous on `stream` (a cudaStream_t, NULL =
  * the legacy default stream). Outputs are overwritten, never accumulated into.
  * Return value: FA_OK, or a negative FA_ERR_* code when an argument is
  * rejected (nothing is launched) or a launch fails. Faults during execution
