@@ -377,7 +377,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
                   uint64_t seed, uint64_t offset, const Extras& ex, int deterministic, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+                  size_t workspace_bytes, void* stream, bool check_ptrs) {
   int rc = check_common(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
   if ((rc = check_alibi(ex.alibi, ex.alibi_sb, scale))) return rc;
@@ -390,7 +390,8 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   const WsLayout w = ws_layout(B, H, N, d, dtype, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
-  if ((rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, ex.alibi, ex.bias}))) return rc;
+  if (check_ptrs && (rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, ex.alibi, ex.bias})))
+    return rc;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
   apply_extras(p, ex);
@@ -555,8 +556,10 @@ int bwd_run(const void* q, const void* k, const void* v, const void* o, const vo
             const Extras& ex, int deterministic, void* workspace, size_t workspace_bytes, void* stream,
             bool allow_side_stream) {
   auto stage = [&](fa_bwd_stage_id s, void* st) {
+    // The buffers are the same for all three steps: the first one checks them.
     return bwd_stage_run(s, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                         dropout_p, seed, offset, ex, deterministic, workspace, workspace_bytes, st);
+                         dropout_p, seed, offset, ex, deterministic, workspace, workspace_bytes, st,
+                         s == FA_BWD_PREPROCESS);
   };
   return run_backward(stage, deterministic, dtype, allow_side_stream, stream);
 }

@@ -35,7 +35,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
                   const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   fa_strides strides, fa_dtype dtype, float scale, int causal, int window, float dropout_p,
                   uint64_t seed, uint64_t offset, const Extras& ex, int deterministic, void* workspace,
-                  size_t workspace_bytes, void* stream);
+                  size_t workspace_bytes, void* stream, bool check_ptrs = true);
 
 // The forward with the optional inputs of Extras.
 int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
