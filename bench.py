@@ -57,10 +57,13 @@ def causal_pairs(w) -> float:
 def dkdv_traffic(w, deterministic: bool):
     """DRAM bytes per launch of the key/value-major kernel from the committed ncu capture,
     scaled to this workload's head count; None unless the kernel source still matches
-    the capture (and for the atomic variant, which that capture does not cover)."""
+    the capture, and for workloads the capture does not cover: the atomic variant, or
+    another dtype, length, head dimension or mask than its bf16 causal N=8192 d=128."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dkdv_traffic.json")
     if not deterministic or not os.path.exists(path):
+        return None
+    if (w.dtype, w.N, w.d, w.causal, w.window, w.dropout_p) != ("bf16", 8192, 128, True, 0, 0.0):
         return None
     with open(path) as f:
         rec = json.load(f)
