@@ -39,7 +39,9 @@
  * L (lse) is a contiguous fp32 [B, H, N] array.
  *
  * Supported. fp16 / bf16: d in {64, 128}, tensor-core (tcgen05) kernels.
- * fp32: 1 <= d <= 128, CUDA-core kernels. Any N >= 1, B >= 1, H >= 1.
+ * fp32: 1 <= d <= 128, CUDA-core kernels. Any N >= 1, B >= 1, H >= 1 up to
+ * B*H <= 2^24 and N <= 2^30 (FA_ERR_UNSUPPORTED beyond: the kernels index in
+ * 32-bit grids and 64-bit offsets).
  * Alignment: every tensor base 16-byte aligned; for fp16/bf16 every stride a
  * multiple of 8 elements (the TMA rule of 16-byte strides); for fp32 strides
  * only need to be positive.
