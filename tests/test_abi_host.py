@@ -240,3 +240,11 @@ def test_oracle_not_imported_by_product_path():
     for f in pkg.rglob("*.py"):
         text = f.read_text()
         assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_size_limits_are_unsupported(lib):
+    """B*H above 2^24 or N above 2^30 are refused before any pointer is used."""
+    assert _fwd(lib, B=1 << 13, H=(1 << 11) + 1, N=64) == EUNSUP
+    assert _bwd(lib, B=1 << 13, H=(1 << 11) + 1, N=64) == EUNSUP
+    assert _fwd(lib, N=(1 << 30) + 1) == EUNSUP
+    assert _bwd(lib, N=(1 << 30) + 1) == EUNSUP
