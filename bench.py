@@ -169,6 +169,82 @@ def flush_l2(buf: torch.Tensor):
     buf.add_(1)
 
 
+def _gpu_busy(stream, ms: float = 2.0):
+    """Keep the stream busy for about ``ms`` (a spin kernel) so that the host
+    work of the launches enqueued after it (argument checks, pointer lookups,
+    tensor-map encoding) happens while the GPU is still busy and stays outside
+    the event intervals that follow."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
+def time_stages(fa, q, k, v, o, do, lse, dq, dk, dv, ws, kw, deterministic, stream, steps):
+    """Device time of each of the three backward stages, launched back to back
+    on one stream behind a spin kernel, with an event between consecutive
+    launches: each interval holds one kernel's execution and no host work."""
+    stage_ms = [0.0, 0.0, 0.0]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(steps):
+        _gpu_busy(stream)
+        evs[0].record(stream)
+        for s in range(3):
+            fa.fa_bwd_stage(s, q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=deterministic,
+                            stream=stream)
+            evs[s + 1].record(stream)
+        torch.cuda.synchronize()
+        for s in range(3):
+            stage_ms[s] += evs[s].elapsed_time(evs[s + 1]) / steps
+    return stage_ms
+
+
+def time_workload(fa, w, steps=5, warmup=3):
+    """Backward ms and TFLOP/s of one workload in both dQ modes (the per-workload
+    block of the JSON line), plus the forward's ms. Inputs resident in HBM."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
+              offset=w.philox_offset)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+    flops = counted_flops(w)
+    out = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal, "window": w.window,
+           "dropout_p": w.dropout_p}
+    modes = (True,) if w.dtype == "f32" else (True, False)
+    for det in modes:
+        ws = fa.alloc_workspace(q, det)
+        for _ in range(warmup):
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=det, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _gpu_busy(stream, 1.0)
+        e0.record(stream)
+        for _ in range(steps):
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=det, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        out["deterministic" if det else "atomic"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+        del ws
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    for _ in range(warmup):
+        fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _gpu_busy(stream, 1.0)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fms = e0.elapsed_time(e1) / steps
+    out["forward"] = {"ms": fms, "tflops": 0.4 * flops / (fms * 1e-3) / 1e12}
+    status = fa.fa_get_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status} after timing {w.name}")
+    return out
+
+
 def time_ours(w, steps, warmup, deterministic, world):
     import flashattention_backward_fa_gb300 as fa
     fa.load_library()
@@ -203,17 +279,7 @@ def time_ours(w, steps, warmup, deterministic, world):
     barrier(world)
     ms = ev0.elapsed_time(ev1) / steps
     # Per-stage durations (same stream), for the roofline of the dominant kernel.
-    stage_ms = [0.0, 0.0, 0.0]
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    for _ in range(steps):
-        evs[0].record(stream)
-        for s in range(3):
-            fa.fa_bwd_stage(s, q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=deterministic,
-                            stream=stream)
-            evs[s + 1].record(stream)
-        torch.cuda.synchronize()
-        for s in range(3):
-            stage_ms[s] += evs[s].elapsed_time(evs[s + 1]) / steps
+    stage_ms = time_stages(fa, q, k, v, o, do, lse, dq, dk, dv, ws, kw, deterministic, stream, steps)
     sampler.stop()
     status = fa.fa_get_device_status(clear=True)
     if status:
@@ -318,6 +384,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--dq", default="deterministic", choices=["deterministic", "atomic"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload block")
     ap.add_argument("--shape", default=None, help="B,H,N override (smaller cases for profiler captures)")
     ap.add_argument("--profile", action="store_true",
                     help="forward, then --warmup + 1 backward steps, no timing (for ncu captures)")
@@ -346,10 +413,15 @@ def main():
         if rank != 0:
             return
         tf, sample, cores, sec_per_head = run_reference_steps(w, a.steps, a.warmup)
+        # Each timed step is one head of the workload (the oracle needs about a
+        # second per head at N = 8192): ms_per_step is that measured time, and
+        # config says how much of the workload a step covers.
+        ref_config = dict(config, reference_step=f"one head (B=1, H=1) of the {w.B * w.H} (batch, head) "
+                                                 f"units of {w.name}")
         line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": a.gpus,
-                "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec_per_head * w.B * w.H * 1e3,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": sec_per_head * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
+                "data": "synthetic", "config": ref_config,
                 "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": sample, "value": tf,
                                  "unit": "TFLOP/s"},
                 "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -369,6 +441,11 @@ def main():
     kv_flops = causal_pairs(w) * w.d * (8.0 if det else 10.0)
     kv_tflops = kv_flops / (kv_ms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    esz = 4 if w.dtype == "f32" else 2
+    n_pad = -(-w.N // 128) * 128
+    # O and dO read, L read, -D and -L*log2e written; atomic mode also zero-fills the fp32 dQ accumulator
+    pre_bytes = w.B * w.H * (w.N * (2 * w.d * esz + 4) + n_pad * 8 + (0 if det else n_pad * w.d * 4))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -377,6 +454,11 @@ def main():
         "pct_of_dense_bf16_peak": 100.0 * value / peak,
         "stages_ms": {"preprocess": r["stage_ms"][0], "dkdv": r["stage_ms"][1],
                       ("dq_qmajor" if det else "dq_convert"): r["stage_ms"][2]},
+        # the D pass: reads O and dO, writes -D and -L*log2e (HBM-bound)
+        "preprocess_hbm": {"bytes": pre_bytes, "gbs": pre_bytes / (r["stage_ms"][0] * 1e-3) / 1e9,
+                           "peak_gbs": hbm_peak,
+                           "frac": pre_bytes / (r["stage_ms"][0] * 1e-3) / 1e9 / hbm_peak,
+                           "peak_source": f"{peak_src} copy bandwidth"},
         "roofline": {"kernel": "bwd_dkdv (key/value-major, tcgen05)", "bound": "tensor", "achieved": kv_tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": kv_tflops / peak,
                      "traffic": dkdv_traffic(w, det),
@@ -392,6 +474,12 @@ def main():
         "other_dq_mode": {"dq_mode": "atomic" if det else "deterministic", "ms_per_step": r["other_ms"],
                           "value": flops / (r["other_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s"},
     }
+    if rank == 0 and not a.no_workloads:
+        # every other workload of the plan, both dQ modes, timed the same way
+        import flashattention_backward_fa_gb300 as fa
+        line["workloads"] = {name: time_workload(fa, wl) for name, wl in sorted(WORKLOADS.items())
+                             if name != w.name}
+        torch.cuda.empty_cache()
     if rank == 0 and not a.no_cpu_baseline:
         # a bounded sample: one warm-up and up to four timed heads, about 30 s at most
         tf, sample, cores, _ = run_reference_steps(w, steps=4, warmup=1, budget_s=30.0)

@@ -295,6 +295,7 @@ const char* fa_strerror(int code) {
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic) {
   if (B < 1 || H < 1 || N < 1 || d < 1 || d > 128) return 0;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return 0;
+  if ((long long)B * H > (1ll << 24) || N > (1 << 30)) return 0;  // beyond the size limits (and pad_rows' int range)
   return ws_layout(B, H, N, d, dtype, deterministic).total;
 }
 

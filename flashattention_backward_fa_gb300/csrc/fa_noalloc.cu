@@ -59,12 +59,15 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                               fa_strides strides, fa_dtype dtype, float scale, int causal, int window,
                               float dropout_p, uint64_t seed, uint64_t offset, void* stream) {
+  // The same size, dtype and stride checks as fa_bwd first, so that both entry
+  // points return the same code for the same bad argument; then the scratch limit.
+  int rc = fa::check_bwd_args(B, H, N, d, strides, dtype, scale, window, dropout_p);
+  if (rc) return rc;
   const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype, 1);
   if (need == 0) return FA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
-  const int rc = noalloc_scratch(&scratch);
-  if (rc) return rc;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
   // Single stream: this entry point creates nothing, not even the side stream.
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
                      dropout_p, seed, offset, fa::Extras{}, 1, scratch, kNoAllocScratchBytes, stream, false);

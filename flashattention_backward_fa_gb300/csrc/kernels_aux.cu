@@ -53,47 +53,52 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // One warp per (b, i, h) row; rows enumerated in [B, n_pad, H] order so that a
-// contiguous [B, N, H, d] tensor is read front to back.
+// contiguous [B, N, H, d] tensor is read front to back. The row index and its
+// decomposition are 64-bit and the warps stride over the rows, so that any
+// B * H * n_pad the size limits admit is covered (a 32-bit row index would
+// wrap once B * H * n_pad passes 2^27 rows at 8 warps a block).
 template <typename T>
 __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__ AttnParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.n_pad * p.H;
-  if (warp >= rows) return;
-  const int h = warp % p.H;
-  const int i = (warp / p.H) % p.n_pad;
-  const int b = warp / (p.H * p.n_pad);
-  const int bh = b * p.H + h;
-  const long long ws = (long long)bh * p.n_pad + i;
-  float acc = 0.f;
-  if (i < p.N) {
-    const long long off = (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
-    const T* o = static_cast<const T*>(p.o) + off;
-    const T* g = static_cast<const T*>(p.dout) + off;
-    if (sizeof(T) == 2 && (p.d & 63) == 0) {
-      // 16-bit types, d in {64, 128}: lanes read 2 or 4 contiguous elements.
-      const int per = p.d >> 5;
-      for (int e = 0; e < per; e += 2) {
-        const int k = lane * per + e;
-        const uint32_t ow = *reinterpret_cast<const uint32_t*>(o + k);
-        const uint32_t gw = *reinterpret_cast<const uint32_t*>(g + k);
-        const T* o2 = reinterpret_cast<const T*>(&ow);
-        const T* g2 = reinterpret_cast<const T*>(&gw);
-        acc = fmaf(to_f32(o2[0]), to_f32(g2[0]), acc);
-        acc = fmaf(to_f32(o2[1]), to_f32(g2[1]), acc);
+  const long long stride = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += stride) {
+    const long long bi = row / p.H;              // b * n_pad + i
+    const int h = (int)(row - bi * p.H);
+    const long long b = bi / p.n_pad;
+    const int i = (int)(bi - b * p.n_pad);
+    const long long bh = b * p.H + h;
+    const long long ws = bh * p.n_pad + i;
+    float acc = 0.f;
+    if (i < p.N) {
+      const long long off = b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+      const T* o = static_cast<const T*>(p.o) + off;
+      const T* g = static_cast<const T*>(p.dout) + off;
+      if (sizeof(T) == 2 && (p.d & 63) == 0) {
+        // 16-bit types, d in {64, 128}: lanes read 2 or 4 contiguous elements.
+        const int per = p.d >> 5;
+        for (int e = 0; e < per; e += 2) {
+          const int k = lane * per + e;
+          const uint32_t ow = *reinterpret_cast<const uint32_t*>(o + k);
+          const uint32_t gw = *reinterpret_cast<const uint32_t*>(g + k);
+          const T* o2 = reinterpret_cast<const T*>(&ow);
+          const T* g2 = reinterpret_cast<const T*>(&gw);
+          acc = fmaf(to_f32(o2[0]), to_f32(g2[0]), acc);
+          acc = fmaf(to_f32(o2[1]), to_f32(g2[1]), acc);
+        }
+      } else {
+        for (int k = lane; k < p.d; k += 32) acc = fmaf(to_f32(o[k]), to_f32(g[k]), acc);
       }
-    } else {
-      for (int k = lane; k < p.d; k += 32) acc = fmaf(to_f32(o[k]), to_f32(g[k]), acc);
+      acc = warp_sum(acc);
     }
-    acc = warp_sum(acc);
-  }
-  if (lane == 0) {
-    p.ws_nD[ws] = -acc;
-    p.ws_nL2[ws] = (i < p.N) ? neg_l2(p.lse[(long long)bh * p.N + i]) : __int_as_float(0xff800000);
-  }
-  if (p.ws_dq != nullptr) {
-    float* dq = p.ws_dq + ws * p.d;
-    for (int k = lane; k < p.d; k += 32) dq[k] = 0.f;
+    if (lane == 0) {
+      p.ws_nD[ws] = -acc;
+      p.ws_nL2[ws] = (i < p.N) ? neg_l2(p.lse[bh * p.N + i]) : __int_as_float(0xff800000);
+    }
+    if (p.ws_dq != nullptr) {
+      float* dq = p.ws_dq + ws * p.d;
+      for (int k = lane; k < p.d; k += 32) dq[k] = 0.f;
+    }
   }
 }
 
@@ -224,18 +229,22 @@ __global__ void __launch_bounds__(256) dq_convert_vec_kernel(const __grid_consta
   }
 }
 
+// The general case (other dtypes or head dimensions): one warp per (b, i, h)
+// row, 64-bit row index, warps striding over the rows as in preprocess_kernel.
 template <typename T>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const __grid_constant__ AttnParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.N * p.H;
-  if (warp >= rows) return;
-  const int h = warp % p.H;
-  const int i = (warp / p.H) % p.N;
-  const int b = warp / (p.H * p.N);
-  const float* src = p.ws_dq + ((long long)(b * p.H + h) * p.n_pad + i) * p.d;
-  T* dst = static_cast<T*>(p.out) + (long long)b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
-  for (int k = lane; k < p.d; k += 32) dst[k] = from_f32<T>(src[k] * p.scale);
+  const long long stride = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += stride) {
+    const long long bi = row / p.H;              // b * N + i
+    const int h = (int)(row - bi * p.H);
+    const long long b = bi / p.N;
+    const int i = (int)(bi - b * p.N);
+    const float* src = p.ws_dq + ((b * p.H + h) * p.n_pad + i) * p.d;
+    T* dst = static_cast<T*>(p.out) + b * p.sb + (long long)i * p.sn + (long long)h * p.sh;
+    for (int k = lane; k < p.d; k += 32) dst[k] = from_f32<T>(src[k] * p.scale);
+  }
 }
 
 // ------------------------------- fp32 path ---------------------------------
@@ -446,8 +455,11 @@ __global__ void __launch_bounds__(32 * kF32Warps) bwd_dq_f32_kernel(const __grid
 }
 
 // ------------------------------- launchers ---------------------------------
-static inline unsigned grid_for_rows(long long rows, int rows_per_block) {
-  return (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+// Grid of a row-striding kernel: enough blocks to cover the rows, at most 2^20
+// (the kernel's warps stride over the rest).
+static inline unsigned grid_for_rows_strided(long long rows, int rows_per_block) {
+  const long long g = (rows + rows_per_block - 1) / rows_per_block;
+  return (unsigned)(g < (1ll << 20) ? (g > 0 ? g : 1) : (1ll << 20));
 }
 
 cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
@@ -466,7 +478,7 @@ cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
                  : preprocess_vec_kernel<__nv_bfloat16, 64><<<g64, 256, 0, st>>>(p);
     return cudaGetLastError();
   }
-  const unsigned grid = grid_for_rows(rows, 8);
+  const unsigned grid = grid_for_rows_strided(rows, 8);
   if (dtype == 0) preprocess_kernel<float><<<grid, 256, 0, st>>>(p);
   else if (dtype == 1) preprocess_kernel<__half><<<grid, 256, 0, st>>>(p);
   else preprocess_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
@@ -486,7 +498,7 @@ cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st) {
     return cudaGetLastError();
   }
   const long long rows = (long long)p.B * p.N * p.H;
-  const unsigned grid = grid_for_rows(rows, 8);
+  const unsigned grid = grid_for_rows_strided(rows, 8);
   if (dtype == 0) dq_convert_kernel<float><<<grid, 256, 0, st>>>(p);
   else if (dtype == 1) dq_convert_kernel<__half><<<grid, 256, 0, st>>>(p);
   else dq_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
@@ -494,19 +506,25 @@ cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st) {
 }
 
 cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st) {
-  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  const long long blocks = ((long long)p.B * p.H * p.N + kF32Warps - 1) / kF32Warps;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;  // one warp per row: the grid must fit
+  const unsigned grid = (unsigned)blocks;
   fwd_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st) {
-  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  const long long blocks = ((long long)p.B * p.H * p.N + kF32Warps - 1) / kF32Warps;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;  // one warp per row: the grid must fit
+  const unsigned grid = (unsigned)blocks;
   bwd_dkdv_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st) {
-  const unsigned grid = grid_for_rows((long long)p.B * p.H * p.N, kF32Warps);
+  const long long blocks = ((long long)p.B * p.H * p.N + kF32Warps - 1) / kF32Warps;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;  // one warp per row: the grid must fit
+  const unsigned grid = (unsigned)blocks;
   bwd_dq_f32_kernel<<<grid, 32 * kF32Warps, 0, st>>>(p);
   return cudaGetLastError();
 }

@@ -46,8 +46,13 @@
  * multiple of 8 elements (the TMA rule of 16-byte strides); for fp32 strides
  * only need to be positive.
  *
- * Ownership and execution. The caller owns every buffer; the library never
- * allocates device memory and keeps no per-call state. All pointers are
+ * Ownership and execution. The caller owns every buffer, and no call
+ * allocates device memory. The library does hold a little module state per
+ * device: the device status word (see fa_get_device_status), the fixed 8 MiB
+ * scratch array of fa_bwd_noalloc (shared by all of its calls, which keeps the
+ * last call's contents; see its declaration), and, created on first use, one
+ * side stream with two events for the deterministic fa_bwd and two copy
+ * streams for fa_bwd_host. All pointers are
  * device pointers of the current device (or managed memory), except the host
  * buffers of fa_bwd_host. After the other argument checks, and before anything
  * is launched, every buffer is looked up with cudaPointerGetAttributes: a host

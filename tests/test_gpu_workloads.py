@@ -1,11 +1,13 @@
 """Parity of the five full-size workloads against the float64 oracle.
 
-The GPU runs every workload at its full size. The oracle checks what it can
-compute cheaply at that size: whole heads for the smaller workloads, and for
-the long ones the dQ rows and dK / dV rows of sampled queries and keys
-(first, last and random positions) of sampled heads, plus the forward's O and
-L on the same rows. Deterministic mode is also checked for bit-identical
-results over ten runs at the headline size.
+The GPU runs every workload at its full size. The oracle compares every
+element of dQ, dK and dV of whole heads: all 32 heads of the headline
+workload (bf16 causal 1x32x8192x128) in both dQ modes, two whole heads of the
+N = 32768 workload in both modes, and sampled whole heads of the others. On
+top of that the sampled-row checks (first, last and random positions of
+sampled heads) cover the forward's O and L and the dropout workload. The
+headline deterministic mode is also checked for bit-identical results over
+ten runs.
 """
 import numpy as np
 import pytest
@@ -101,6 +103,60 @@ def test_bf16_causal_b1h32_n8192_sampled(deterministic):
     w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
     res = _gpu(w, deterministic)
     failures = _check_sampled(w, res, [(0, 0), (0, 13), (0, 31)], seed=1)
+    assert not failures, failures
+
+
+def _gpu_both_modes(w):
+    """Forward once, then the backward in both dQ modes on the same O and L."""
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
+              offset=w.philox_offset)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    out = {"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse}
+    for det in (True, False):
+        dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=det)
+        torch.cuda.synchronize()
+        assert fa.fa_get_device_status(clear=True) == 0
+        for t in (dq, dk, dv):
+            assert torch.isfinite(t).all()
+        out["det" if det else "atomic"] = tuple(t.cpu() for t in (dq, dk, dv))
+        del dq, dk, dv
+    for n in ("q", "k", "v", "do", "o", "lse"):
+        out[n] = out[n].cpu()
+    torch.cuda.empty_cache()
+    return out
+
+
+def _check_whole_heads(w, res, heads):
+    """Every element of dQ, dK, dV of the listed heads, both dQ modes, against
+    the oracle in function mode (the O and L the GPU forward produced)."""
+    args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
+    failures = []
+    for (b, h) in heads:
+        a = {n: to_np(res[n][b:b + 1, :, h:h + 1, :]) for n in ("q", "k", "v", "do", "o")}
+        lse = res["lse"][b:b + 1, h:h + 1].double().numpy()
+        rq, rk, rv, _ = oracle.backward(a["q"], a["k"], a["v"], a["o"], a["do"], lse, *args)
+        for mode in ("det", "atomic"):
+            for name, g, r in zip(("dq", "dk", "dv"), res[mode], (rq, rk, rv)):
+                ok, rep = within(to_np(g[b:b + 1, :, h:h + 1, :]), r, w.dtype)
+                if not ok:
+                    failures.append((mode, b, h, name, rep))
+    return failures
+
+
+def test_bf16_causal_b1h32_n8192_whole_tensor():
+    """The headline workload: all 32 heads, every element, both dQ modes."""
+    w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
+    res = _gpu_both_modes(w)
+    failures = _check_whole_heads(w, res, [(0, h) for h in range(w.H)])
+    assert not failures, failures
+
+
+def test_bf16_causal_b1h8_n32768_whole_heads():
+    """The longest workload: two whole heads (first and last), every element, both dQ modes."""
+    w = WORKLOADS["bf16_causal_b1h8_n32768_d128"]
+    res = _gpu_both_modes(w)
+    failures = _check_whole_heads(w, res, [(0, 0), (0, w.H - 1)])
     assert not failures, failures
 
 
