@@ -217,7 +217,7 @@ def time_workload(fa, w, steps=5, warmup=3):
             fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=det, stream=stream)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        _gpu_busy(stream, 1.0)
+        _gpu_busy(stream, 5.0)  # covers the host's enqueue of all steps: device time per step
         e0.record(stream)
         for _ in range(steps):
             fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=det, stream=stream)
@@ -231,7 +231,7 @@ def time_workload(fa, w, steps=5, warmup=3):
         fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _gpu_busy(stream, 1.0)
+    _gpu_busy(stream, 5.0)
     e0.record(stream)
     for _ in range(steps):
         fa.fa_fwd(q, k, v, o2, lse2, **kw, stream=stream)
