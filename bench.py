@@ -6,7 +6,7 @@ inputs resident in HBM. Throughput is counted as 10*N^2*d FLOPs per head,
 halved under the causal mask, per step. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--dq deterministic|atomic]
+                  [--workload NAME] [--dq deterministic|recompute|atomic|ordered]
 
 Under torchrun each rank runs the same workload on its own GPU (independent
 replicas: heads shard with no exchange, so there is no data-path collective);
@@ -34,6 +34,16 @@ sys.path.insert(0, ROOT)
 from flashattention_backward_fa_gb300.inputs import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "attn bwd TFLOP/s and % of dense bf16 peak (causal, d=128, N=8192), 1 GB300"
+# --dq choices -> the `deterministic` argument of the backward (fa.h FA_DQ_*):
+# the library's deterministic default, the query-major recompute, atomic and
+# ordered accumulation.
+DQ_MODES = {"deterministic": 1, "recompute": 2, "atomic": 0, "ordered": 3}
+DQ_ALGOS = ("recompute", "atomic", "ordered")
+
+
+def accumulates(mode: int) -> bool:
+    """True for the dQ modes whose key/value-major kernel also forms dQ (5 contractions a pair)."""
+    return mode in (0, 3)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -210,8 +220,9 @@ def time_workload(fa, w, steps=5, warmup=3):
     flops = counted_flops(w)
     out = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal, "window": w.window,
            "dropout_p": w.dropout_p}
-    modes = (True,) if w.dtype == "f32" else (True, False)
-    for det in modes:
+    modes = ("recompute",) if w.dtype == "f32" else DQ_ALGOS
+    for name in modes:
+        det = DQ_MODES[name]
         ws = fa.alloc_workspace(q, det)
         for _ in range(warmup):
             fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, **kw, deterministic=det, stream=stream)
@@ -224,7 +235,7 @@ def time_workload(fa, w, steps=5, warmup=3):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
-        out["deterministic" if det else "atomic"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+        out[name] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
         del ws
     o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
     for _ in range(warmup):
@@ -318,21 +329,28 @@ def time_ours(w, steps, warmup, deterministic, world):
     f1.record(stream)
     torch.cuda.synchronize()
     fwd_ms = f0.elapsed_time(f1) / e2e_steps
-    # The other dQ variant on the same inputs (its own workspace), timed the same
-    # way, so that one line reports both.
-    ws_other = fa.alloc_workspace(q, not deterministic)
-    for _ in range(max(3, warmup)):
-        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_other, **kw, deterministic=not deterministic, stream=stream)
-    torch.cuda.synchronize()
-    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    v0.record(stream)
-    for _ in range(steps):
-        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_other, **kw, deterministic=not deterministic, stream=stream)
-    v1.record(stream)
-    torch.cuda.synchronize()
-    other_ms = v0.elapsed_time(v1) / steps
+    # Every dQ algorithm on the same inputs (each with its own workspace), timed
+    # the same way, so that one line reports all of them.
+    mode_ms = {}
+    for name in DQ_ALGOS:
+        m = DQ_MODES[name]
+        ws_m = fa.alloc_workspace(q, m)
+        for _ in range(max(3, warmup)):
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_m, **kw, deterministic=m, stream=stream)
+        torch.cuda.synchronize()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for _ in range(steps):
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws_m, **kw, deterministic=m, stream=stream)
+        v1.record(stream)
+        torch.cuda.synchronize()
+        mode_ms[name] = v0.elapsed_time(v1) / steps
+        del ws_m
+    status = fa.fa_get_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status} after timing the dQ modes")
     return dict(ms=ms, stage_ms=stage_ms, clocks=sampler.summary(), e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, fwd_ms=fwd_ms,
-                other_ms=other_ms)
+                mode_ms=mode_ms)
 
 
 def run_reference_steps(w, steps, warmup, budget_s=150.0):
@@ -382,7 +400,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
-    ap.add_argument("--dq", default="deterministic", choices=["deterministic", "atomic"])
+    ap.add_argument("--dq", default="deterministic", choices=sorted(DQ_MODES))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload block")
     ap.add_argument("--shape", default=None, help="B,H,N override (smaller cases for profiler captures)")
@@ -400,7 +418,7 @@ def main():
                   offset=w.philox_offset)
         o, lse = fa.attention_forward(q, k, v, **kw)
         for _ in range(a.warmup + 1):
-            fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=a.dq == "deterministic")
+            fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=DQ_MODES[a.dq])
         torch.cuda.synchronize()
         print(json.dumps({"profile_case": w.name, "status": fa.fa_get_device_status(clear=True)}))
         return
@@ -427,25 +445,26 @@ def main():
                 "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
-    r = time_ours(w, a.steps, a.warmup, a.dq == "deterministic", world)
+    mode = DQ_MODES[a.dq]
+    r = time_ours(w, a.steps, a.warmup, mode, world)
     ms = max_over_ranks(r["ms"], world)
     e2e_ms = max_over_ranks(r["e2e_ms"], world)
     flops = counted_flops(w)
     value = world * flops / (ms * 1e-3) / 1e12
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
-    det = a.dq == "deterministic"
+    acc = accumulates(mode)
     # Dominant kernel: the key/value-major backward. Its algorithmic work is the
     # S, dP, dV and dK contractions (8*d FLOPs per allowed pair), plus dQ (2*d)
-    # in atomic mode.
+    # when it accumulates dQ (atomic, ordered).
     kv_ms = r["stage_ms"][1]
-    kv_flops = causal_pairs(w) * w.d * (8.0 if det else 10.0)
+    kv_flops = causal_pairs(w) * w.d * (10.0 if acc else 8.0)
     kv_tflops = kv_flops / (kv_ms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     esz = 4 if w.dtype == "f32" else 2
     n_pad = -(-w.N // 128) * 128
     # O and dO read, L read, -D and -L*log2e written; atomic mode also zero-fills the fp32 dQ accumulator
-    pre_bytes = w.B * w.H * (w.N * (2 * w.d * esz + 4) + n_pad * 8 + (0 if det else n_pad * w.d * 4))
+    pre_bytes = w.B * w.H * (w.N * (2 * w.d * esz + 4) + n_pad * 8 + (n_pad * w.d * 4 if acc else 0))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -453,7 +472,7 @@ def main():
         "config": config,
         "pct_of_dense_bf16_peak": 100.0 * value / peak,
         "stages_ms": {"preprocess": r["stage_ms"][0], "dkdv": r["stage_ms"][1],
-                      ("dq_qmajor" if det else "dq_convert"): r["stage_ms"][2]},
+                      ("dq_convert" if acc else "dq_qmajor"): r["stage_ms"][2]},
         # the D pass: reads O and dO, writes -D and -L*log2e (HBM-bound)
         "preprocess_hbm": {"bytes": pre_bytes, "gbs": pre_bytes / (r["stage_ms"][0] * 1e-3) / 1e9,
                            "peak_gbs": hbm_peak,
@@ -461,7 +480,7 @@ def main():
                            "peak_source": f"{peak_src} copy bandwidth"},
         "roofline": {"kernel": "bwd_dkdv (key/value-major, tcgen05)", "bound": "tensor", "achieved": kv_tflops,
                      "peak": peak, "unit": "TFLOP/s", "frac": kv_tflops / peak,
-                     "traffic": dkdv_traffic(w, det),
+                     "traffic": dkdv_traffic(w, not acc),
                      "peak_source": f"{peak_src} burst bf16"},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
@@ -470,12 +489,13 @@ def main():
         "forward": {"ms": r["fwd_ms"], "tflops": 0.4 * flops / (r["fwd_ms"] * 1e-3) / 1e12,
                     "bwd_over_fwd_speed": (flops / (r["ms"] * 1e-3)) / (0.4 * flops / (r["fwd_ms"] * 1e-3))},
         "clocks": r["clocks"],
-        # the dQ variant not in `value` (atomic when value is deterministic), same workload
-        "other_dq_mode": {"dq_mode": "atomic" if det else "deterministic", "ms_per_step": r["other_ms"],
-                          "value": flops / (r["other_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s"},
+        # every dQ algorithm on the same workload (recompute and ordered are the
+        # deterministic ones), timed the same way as `value`
+        "dq_modes": {name: {"ms_per_step": ms_m, "value": flops / (ms_m * 1e-3) / 1e12, "unit": "TFLOP/s",
+                            "deterministic": name != "atomic"} for name, ms_m in r["mode_ms"].items()},
     }
     if rank == 0 and not a.no_workloads:
-        # every other workload of the plan, both dQ modes, timed the same way
+        # every other workload of the plan, every dQ algorithm, timed the same way
         import flashattention_backward_fa_gb300 as fa
         line["workloads"] = {name: time_workload(fa, wl) for name, wl in sorted(WORKLOADS.items())
                              if name != w.name}

@@ -22,6 +22,19 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
 
 FA_F32, FA_F16, FA_BF16 = 0, 1, 2
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ = 0, 1, 2
+# dQ algorithms (the `deterministic` argument of the backward calls, fa.h FA_DQ_*)
+FA_DQ_ATOMIC, FA_DQ_DETERMINISTIC, FA_DQ_RECOMPUTE, FA_DQ_ORDERED = 0, 1, 2, 3
+
+
+def _dq_mode(deterministic) -> int:
+    """A `deterministic` argument as the C ABI's dQ mode: True / False are
+    FA_DQ_DETERMINISTIC / FA_DQ_ATOMIC; integers pass through (FA_DQ_*)."""
+    if isinstance(deterministic, bool):
+        return FA_DQ_DETERMINISTIC if deterministic else FA_DQ_ATOMIC
+    mode = int(deterministic)
+    if mode not in (FA_DQ_ATOMIC, FA_DQ_DETERMINISTIC, FA_DQ_RECOMPUTE, FA_DQ_ORDERED):
+        raise ValueError(f"deterministic must be a bool or one of FA_DQ_* (0..3), not {deterministic!r}")
+    return mode
 ERROR_CODES = {
     0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED", -3: "FA_ERR_ALIGNMENT",
     -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_CUDA", -6: "FA_ERR_TIMEOUT",
@@ -178,7 +191,7 @@ def default_scale(d: int) -> float:
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int, dtype, deterministic: bool = True) -> int:
     code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return int(load_library().fa_bwd_workspace_size(B, H, N, d, code, int(bool(deterministic))))
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d, code, _dq_mode(deterministic)))
 
 
 def fa_fwd(q, k, v, o, lse, scale=None, causal=False, window=0, dropout_p=0.0, seed=0, offset=0, stream=None,
@@ -215,7 +228,7 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, scale, causal, window, dropout_p,
     return (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
             default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p),
-            int(seed), int(offset), int(bool(deterministic)), workspace.data_ptr(),
+            int(seed), int(offset), _dq_mode(deterministic), workspace.data_ptr(),
             workspace.numel() * workspace.element_size(), _stream(stream))
 
 
@@ -276,7 +289,7 @@ def _host_layout(ref: torch.Tensor, *others: torch.Tensor):
 
 def fa_bwd_host_buffer_size(B: int, H: int, N: int, d: int, dtype, deterministic: bool = True) -> int:
     code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    return int(load_library().fa_bwd_host_buffer_size(B, H, N, d, code, int(bool(deterministic))))
+    return int(load_library().fa_bwd_host_buffer_size(B, H, N, d, code, _dq_mode(deterministic)))
 
 
 def fa_bwd_host(q, k, v, o, do, lse, dq, dk, dv, dev_buf, scale=None, causal=False, window=0, dropout_p=0.0,
@@ -294,7 +307,7 @@ def fa_bwd_host(q, k, v, o, do, lse, dq, dk, dv, dev_buf, scale=None, causal=Fal
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), B, H, N, d, st, _TORCH_TO_FA[q.dtype],
         default_scale(d) if scale is None else float(scale), int(causal), int(window), float(dropout_p), int(seed),
-        int(offset), int(bool(deterministic)), dev_buf.data_ptr(), dev_buf.numel() * dev_buf.element_size(),
+        int(offset), _dq_mode(deterministic), dev_buf.data_ptr(), dev_buf.numel() * dev_buf.element_size(),
         _stream(stream)))
 
 
@@ -372,7 +385,7 @@ def fa_varlen_bwd_workspace_size(nseq: int, max_seqlen: int, total: int, H: int,
                                  deterministic: bool = True) -> int:
     code = _TORCH_TO_FA[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return int(load_library().fa_varlen_bwd_workspace_size(nseq, max_seqlen, total, H, d, code,
-                                                           int(bool(deterministic))))
+                                                           _dq_mode(deterministic)))
 
 
 def fa_varlen_fwd(q, k, v, o, lse, cu_seqlens, max_seqlen, scale=None, causal=False, window=0, stream=None,
@@ -397,7 +410,7 @@ def fa_varlen_bwd(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, max_seqlen, works
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(), dq.data_ptr(),
         dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(), nseq, int(max_seqlen), total, H, d, sn, sh,
         _TORCH_TO_FA[q.dtype], default_scale(d) if scale is None else float(scale), int(causal), int(window),
-        *_alibi(alibi_slopes, nseq, H, q.device), int(bool(deterministic)), workspace.data_ptr(),
+        *_alibi(alibi_slopes, nseq, H, q.device), _dq_mode(deterministic), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

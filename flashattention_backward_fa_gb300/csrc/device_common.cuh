@@ -183,6 +183,58 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// TMA tensor reduce-add: the box at tensor coordinates (c0, c1, c2) gains the
+// box held in shared memory at src, element by element (fp32 add, performed at
+// L2; concurrent reductions into the same elements from other CTAs are each
+// applied atomically, in no defined order). c0 x element size must be a
+// multiple of 16 bytes; src 128-byte aligned. Tracked by the bulk async-group
+// of the issuing thread.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory sources of this thread's committed bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's committed bulk groups have completed (their global writes are done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's async-proxy global accesses (TMA) with its generic ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ptr) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+// Waits until a global counter another CTA publishes (st_release_gpu) reaches
+// `target`. Bounded like mbar_wait: on the wall-clock limit it sets the timeout
+// status bit and the CTA's abort flag and returns false; it also returns false
+// once another role of the CTA has aborted.
+__device__ __forceinline__ bool flag_wait_geq(const unsigned int* flag, unsigned int target, volatile int* abort_flag,
+                                              unsigned int* status) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(flag) >= target) return true;
+    if ((spin & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, kStatusTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Wait that ignores the abort flag, used to let in-flight copies or MMAs land
 // before a CTA that gave up exits. Also bounded.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int* status) {

@@ -106,19 +106,40 @@ bool make_bias_map(CUtensorMap* m, const AttnParams& p, bool bf16, bool query_ma
 inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int pad_rows(int N) { return (N + fa::kPadRows - 1) / fa::kPadRows * fa::kPadRows; }
 
-bool needs_dq_accum(int dtype, int deterministic) { return dtype != FA_F32 && !deterministic; }
+// The dQ algorithm a `deterministic` argument selects (fa.h, FA_DQ_*). fp32 has
+// one path (query-major, deterministic) whatever is asked.
+enum class DqAlgo { kAtomic, kRecompute, kOrdered };
+
+DqAlgo dq_algo(int dtype, int deterministic) {
+  if (dtype == FA_F32) return DqAlgo::kRecompute;
+  if (deterministic == FA_DQ_ATOMIC) return DqAlgo::kAtomic;
+  if (deterministic == FA_DQ_ORDERED) return DqAlgo::kOrdered;
+  return DqAlgo::kRecompute;  // FA_DQ_DETERMINISTIC, FA_DQ_RECOMPUTE
+}
+
+bool valid_dq_mode(int deterministic) {
+  return deterministic == FA_DQ_ATOMIC || deterministic == FA_DQ_DETERMINISTIC || deterministic == FA_DQ_RECOMPUTE ||
+         deterministic == FA_DQ_ORDERED;
+}
+
+bool needs_dq_accum(int dtype, int deterministic) { return dq_algo(dtype, deterministic) != DqAlgo::kRecompute; }
 
 struct WsLayout {
-  size_t off_L2, off_D, off_dq, total;
+  size_t off_L2, off_D, off_dq, off_flags, off_ticket, total;
 };
 
+// [-L*log2e | -D | fp32 dQ accumulator (atomic, ordered) | chunk counters and
+// the unit ticket (ordered)], each part 256-byte aligned.
 WsLayout ws_layout(int B, int H, int N, int d, int dtype, int deterministic) {
   const size_t rows = (size_t)B * H * pad_rows(N);
   WsLayout w;
   w.off_L2 = 0;
   w.off_D = round256(rows * 4);
   w.off_dq = w.off_D + round256(rows * 4);
-  w.total = w.off_dq + (needs_dq_accum(dtype, deterministic) ? round256(rows * (size_t)d * 4) : 0);
+  w.off_flags = w.off_dq + (needs_dq_accum(dtype, deterministic) ? round256(rows * (size_t)d * 4) : 0);
+  const bool ordered = dq_algo(dtype, deterministic) == DqAlgo::kOrdered;
+  w.off_ticket = w.off_flags + (ordered ? round256(rows / 32 * 4) : 0);
+  w.total = w.off_ticket + (ordered ? 256 : 0);
   return w;
 }
 
@@ -219,6 +240,23 @@ void apply_extras(AttnParams& p, const fa::Extras& ex) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// The fp32 dQ accumulator as a 3-D map (d, rows per head, heads): rows per head
+// n_pad (packed input: the per-head accumulator rows), heads B*H (packed: H);
+// boxes of d x 32 rows, unswizzled, for the key/value-major kernel's TMA
+// reduce-adds of its staged [32 rows][d] tiles.
+bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t nz = p.cu_seqlens ? (cuuint64_t)p.H : (cuuint64_t)p.B * p.H;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.n_pad, nz};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.d * 4, (cuuint64_t)p.n_pad * p.d * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)p.d, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.ws_dq, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -226,16 +264,19 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
   if (dtype == FA_F32)
     return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
   const bool bf16 = dtype == FA_BF16;
+  const bool accum = dq_algo(dtype, deterministic) != DqAlgo::kRecompute;
   if (stage == FA_BWD_DKDV) {
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
         !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
       return FA_ERR_CUDA;
     if (p.bias ? !make_bias_map(&maps[4], p, bf16, false) : false) return FA_ERR_CUDA;
     if (!p.bias) maps[4] = maps[0];  // unused
-    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, !deterministic, maps, st));
+    if (accum ? !make_dq_accum_map(&maps[5], p) : false) return FA_ERR_CUDA;
+    if (!accum) maps[5] = maps[0];  // unused
+    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, maps, st));
   }
-  if (!deterministic) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
+  if (accum) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
   CUtensorMap maps[5];
   if (!make_map(&maps[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], p.k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], p.v, p, bf16, fa::kStepKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kRowsQ))
@@ -294,6 +335,7 @@ const char* fa_strerror(int code) {
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic) {
   if (B < 1 || H < 1 || N < 1 || d < 1 || d > 128) return 0;
+  if (!valid_dq_mode(deterministic)) return 0;
   if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return 0;
   if ((long long)B * H > (1ll << 24) || N > (1 << 30)) return 0;  // beyond the size limits (and pad_rows' int range)
   return ws_layout(B, H, N, d, dtype, deterministic).total;
@@ -384,6 +426,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   if ((rc = check_alibi(ex.alibi, ex.alibi_sb, scale))) return rc;
   if ((rc = check_bias(ex.bias, ex.bias_st, N, dtype, scale))) return rc;
   if (stage != FA_BWD_PREPROCESS && stage != FA_BWD_DKDV && stage != FA_BWD_DQ) return FA_ERR_INVALID_ARG;
+  if (!valid_dq_mode(deterministic)) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
   for (const void* ptr : all)
@@ -409,6 +452,10 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   p.ws_nL2 = reinterpret_cast<float*>(ws + w.off_L2);
   p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
+  if (dq_algo(dtype, deterministic) == DqAlgo::kOrdered) {
+    p.dq_flags = reinterpret_cast<unsigned int*>(ws + w.off_flags);
+    p.dq_ticket = reinterpret_cast<unsigned int*>(ws + w.off_ticket);
+  }
   if ((rc = status_ptr(&p.status))) return rc;
   return launch_stage(stage, p, dtype, deterministic, stream);
 }
@@ -527,7 +574,7 @@ template <typename StageFn>
 int run_backward(StageFn stage, int deterministic, int dtype, bool allow_side_stream, void* stream) {
   int rc = stage(FA_BWD_PREPROCESS, stream);
   if (rc) return rc;
-  if (!allow_side_stream || !deterministic || dtype == FA_F32) {
+  if (!allow_side_stream || dq_algo(dtype, deterministic) != DqAlgo::kRecompute || dtype == FA_F32) {
     if ((rc = stage(FA_BWD_DKDV, stream))) return rc;
     return stage(FA_BWD_DQ, stream);
   }
@@ -572,7 +619,7 @@ namespace {
 
 struct VarlenWs {
   int seq_pad, acc_rows;
-  size_t off_L2, off_D, off_dq, total;
+  size_t off_L2, off_D, off_dq, off_flags, off_ticket, total;
 };
 
 VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int deterministic) {
@@ -583,7 +630,10 @@ VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int
   w.off_L2 = 0;
   w.off_D = round256(vec);
   w.off_dq = w.off_D + round256(vec);
-  w.total = w.off_dq + (deterministic ? 0 : round256((size_t)H * w.acc_rows * d * 4));
+  const DqAlgo a = dq_algo(FA_BF16, deterministic);
+  w.off_flags = w.off_dq + (a != DqAlgo::kRecompute ? round256((size_t)H * w.acc_rows * d * 4) : 0);
+  w.off_ticket = w.off_flags + (a == DqAlgo::kOrdered ? round256(vec / 32) : 0);
+  w.total = w.off_ticket + (a == DqAlgo::kOrdered ? 256 : 0);
   return w;
 }
 
@@ -619,6 +669,7 @@ size_t fa_varlen_bwd_workspace_size(int nseq, int max_seqlen, int total, int H, 
                                     int deterministic) {
   if (nseq < 1 || max_seqlen < 1 || total < 1 || H < 1 || (d != 64 && d != 128)) return 0;
   if (dtype != FA_F16 && dtype != FA_BF16) return 0;
+  if (!valid_dq_mode(deterministic)) return 0;
   return varlen_ws_layout(nseq, max_seqlen, total, H, d, deterministic).total;
 }
 
@@ -659,6 +710,7 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
                          window, alibi_slopes, alibi_stride_seq);
   if (rc) return rc;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!valid_dq_mode(deterministic)) return FA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv};
   for (const void* ptr : all)
     if (!aligned16(ptr)) return FA_ERR_ALIGNMENT;
@@ -679,7 +731,12 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
   char* ws = static_cast<char*>(workspace);
   p.ws_nL2 = reinterpret_cast<float*>(ws + w.off_L2);
   p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
-  p.ws_dq = deterministic ? nullptr : reinterpret_cast<float*>(ws + w.off_dq);
+  const DqAlgo algo = dq_algo(dtype, deterministic);
+  p.ws_dq = algo == DqAlgo::kRecompute ? nullptr : reinterpret_cast<float*>(ws + w.off_dq);
+  if (algo == DqAlgo::kOrdered) {
+    p.dq_flags = reinterpret_cast<unsigned int*>(ws + w.off_flags);
+    p.dq_ticket = reinterpret_cast<unsigned int*>(ws + w.off_ticket);
+  }
   if ((rc = status_ptr(&p.status))) return rc;
   const size_t acc_bytes = (size_t)H * w.acc_rows * d * 4;
   auto stage = [&](fa_bwd_stage_id s, void* st) {

@@ -40,7 +40,13 @@ struct AttnParams {
   float* lse_out;         // forward: L written here
   float* ws_nL2;          // [B*H, n_pad]  -L * log2(e), -inf past N (negated: feeds an FMA addend)
   float* ws_nD;           // [B*H, n_pad]  -rowsum(dO o O), 0 past N (negated: feeds an add)
-  float* ws_dq;           // [B*H, n_pad, d] fp32 dQ accumulator (atomic mode) or null
+  float* ws_dq;           // [B*H, n_pad, d] fp32 dQ accumulator (atomic and ordered modes) or null
+  // Ordered dQ mode (null otherwise): one counter per (unit, 32-row query chunk)
+  // of the completed contributions to that chunk of the accumulator, and the
+  // ticket from which the key/value-major CTAs take their units in order. Both
+  // zeroed by the preprocess.
+  unsigned int* dq_flags;
+  unsigned int* dq_ticket;
   unsigned int* status;   // device status word (timeout bits)
   // Packed variable-length input (null cu_seqlens otherwise): the tensors are
   // [total, H, d] (B = 1, N = total), sequence s occupies packed rows
@@ -84,18 +90,20 @@ constexpr int kUnitGroup = 8;
 
 // Decodes block `idx` of a grid of ntiles * units CTAs. reverse_tiles != 0
 // numbers the tiles from the last one down in launch order (heaviest first for
-// the query-major kernels under a causal mask). Returns false for tiles past
-// the end of a short sequence (the CTA has no work).
+// the query-major kernels under a causal mask). `group` units share a group
+// (default kUnitGroup; group >= units puts the tiles outermost over all units).
+// Returns false for tiles past the end of a short sequence (the CTA has no work).
 __device__ __forceinline__ bool unit_decode(const AttnParams& p, int idx, int tile_rows, bool reverse_tiles,
-                                            Unit& u) {
+                                            Unit& u, int group = kUnitGroup) {
   const bool packed = p.cu_seqlens != nullptr;
   const int units = packed ? p.nseq * p.H : p.B * p.H;
   const int ntiles = ((packed ? p.max_seqlen : p.N) + tile_rows - 1) / tile_rows;
-  const int g = idx / (kUnitGroup * ntiles), r = idx - g * (kUnitGroup * ntiles);
-  const int gsize = min(kUnitGroup, units - g * kUnitGroup);  // the last group may be short
+  group = min(group, units);
+  const int g = idx / (group * ntiles), r = idx - g * (group * ntiles);
+  const int gsize = min(group, units - g * group);  // the last group may be short
   u.tile = r / gsize;
   if (reverse_tiles) u.tile = ntiles - 1 - u.tile;
-  const int unit = g * kUnitGroup + r % gsize;
+  const int unit = g * group + r % gsize;
   if (!packed) {
     u.bh = unit;
     u.b = u.bh / p.H;

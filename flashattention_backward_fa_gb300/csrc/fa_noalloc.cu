@@ -63,12 +63,13 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   // points return the same code for the same bad argument; then the scratch limit.
   int rc = fa::check_bwd_args(B, H, N, d, strides, dtype, scale, window, dropout_p);
   if (rc) return rc;
-  const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype, 1);
+  const size_t need = fa_bwd_workspace_size(B, H, N, d, dtype, FA_DQ_RECOMPUTE);
   if (need == 0) return FA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch))) return rc;
   // Single stream: this entry point creates nothing, not even the side stream.
   return fa::bwd_run(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, strides, dtype, scale, causal, window,
-                     dropout_p, seed, offset, fa::Extras{}, 1, scratch, kNoAllocScratchBytes, stream, false);
+                     dropout_p, seed, offset, fa::Extras{}, FA_DQ_RECOMPUTE, scratch, kNoAllocScratchBytes, stream,
+                     false);
 }

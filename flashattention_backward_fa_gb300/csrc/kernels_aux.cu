@@ -3,8 +3,9 @@
 // * preprocess: D_i = rowsum(dO o O) in fp32 ("FlashAttention backward",
 //   §The gradients, and the one scalar that makes them local: one cheap pass
 //   over dO and O before the main loop), stored negated, plus -L*log2(e) into
-//   a padded workspace vector and, in atomic-dQ mode, the zero fill of the
-//   fp32 dQ accumulator. Both vectors are kept negated so that the consumers
+//   a padded workspace vector and, in the atomic and ordered dQ modes, the zero
+//   fill of the fp32 dQ accumulator (and, ordered, of the chunk counters and
+//   the unit ticket). Both vectors are kept negated so that the consumers
 //   use them as addends (S*scale*log2e + (-L*log2e) is one FMA, dP + (-D) one
 //   add, also in packed two-wide form).
 // * dq_convert: dQ = scale * dQ_accum, rounded to the tensor dtype (atomic mode).
@@ -94,6 +95,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
     if (lane == 0) {
       p.ws_nD[ws] = -acc;
       p.ws_nL2[ws] = (i < p.N) ? neg_l2(p.lse[bh * p.N + i]) : __int_as_float(0xff800000);
+      // ordered dQ: the contribution counter of each 32-row chunk and the unit ticket start at 0
+      if (p.dq_flags != nullptr && (i & 31) == 0) p.dq_flags[bh * (p.n_pad / 32) + i / 32] = 0u;
+      if (p.dq_ticket != nullptr && row == 0) *p.dq_ticket = 0u;
     }
     if (p.ws_dq != nullptr) {
       float* dq = p.ws_dq + ws * p.d;
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_consta
   const T* o = static_cast<const T*>(p.o) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh +
                (long long)row0 * p.sn + e0;
   const T* g = static_cast<const T*>(p.dout) + (o - static_cast<const T*>(p.o));
+  if (p.dq_ticket != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.dq_ticket = 0u;
   uint4 ov[kVecRows], gv[kVecRows];
 #pragma unroll
   for (int r = 0; r < kVecRows; ++r) {
@@ -181,6 +186,8 @@ __global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_consta
     if (e0 == 0) {
       p.ws_nD[ws0 + i] = -acc;
       p.ws_nL2[ws0 + i] = (i < n) ? neg_l2(p.lse[lse0 + i]) : __int_as_float(0xff800000);
+      // ordered dQ: the contribution counter of each 32-row chunk starts at 0
+      if (p.dq_flags != nullptr && (i & 31) == 0) p.dq_flags[(long long)blockIdx.y * (pad / 32) + i / 32] = 0u;
     }
     // (packed input: the dQ accumulator is zeroed separately)
     if (p.ws_dq != nullptr && p.cu_seqlens == nullptr) {

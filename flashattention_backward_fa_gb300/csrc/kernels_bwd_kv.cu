@@ -11,8 +11,8 @@
 //   P~T  = P^T o Z/(1-p),  dP^T = dP~T o Z/(1-p)  (dropout, "Lecture 7" §Dropout)
 //   dS^T = P^T o (dP^T - D_i)                     ("FlashAttention backward" §The gradients)
 //   dV  += P~T dO_i,   dK += dS^T Q_i             (fp32 in TMEM; dK scaled on store)
-//   atomic mode only: dQ_i^T = K_j^T dS^T, added into an fp32 HBM accumulator
-//   with red.add ("FlashAttention backward" §The loop structure, choice (a)).
+//   atomic and ordered modes: dQ_i^T = K_j^T dS^T, added into an fp32 HBM
+//   accumulator ("FlashAttention backward" §The loop structure, choice (a)).
 //
 // Keys sit on the 128 TMEM lanes: one thread owns one key row of S^T and dP^T.
 // Row-math warps wait warp-wide (warp_wait) and reconverge after per-lane
@@ -29,8 +29,32 @@
 // MMAs, warp 3 the dP^T MMAs and warp 2 the dV / dK (and dQ^T) MMAs, so that
 // the three MMA streams are issued in parallel (one thread issues at most about
 // one MMA per 50 cycles); four row-math warpgroups (warps 4-19)
-// take alternate query steps, warpgroup w using buffer w. They also drain dQ^T
-// in atomic mode and write the dV (warpgroup 0) / dK (warpgroup 1) epilogue.
+// take alternate query steps, warpgroup w using buffer w, and write the dV
+// (warpgroup 0) / dK (warpgroup 1) epilogue.
+//
+// dQ (atomic and ordered modes). The row-math warps move dQ^T from TMEM into a
+// staging tile in shared memory, laid out [32 query rows][d] fp32 per
+// warpgroup, over the dS^T image of the step (the dK and dQ^T MMAs have read
+// it by then, and the image of that buffer is not rewritten until the same
+// warpgroups' phase 2 two steps later). The TMA producer thread, which also
+// acts as the reducer, adds each staged tile into the fp32 accumulator with one
+// TMA tensor reduce-add, so the reduction costs the row-math warps 32 shared
+// stores a step instead of 32 global atomics. It releases the staging area as
+// soon as the TMA unit has read it. Producer and reducer duties are served by
+// one polling loop that never blocks on either.
+//  * atomic: reductions of different key blocks land in any order.
+//  * ordered (deterministic): every 32-row query chunk keeps a counter of the
+//    contributions already added; key block j waits until its predecessors
+//    (key blocks jlo .. j-1 of that chunk, in ascending order) are complete,
+//    adds its own, waits for completion and publishes count + 1. The fp32 sums
+//    are then formed in one fixed order ("Lecture 7" §Determinism: a
+//    deterministic mode orders the reductions instead of relying on atomics).
+//    CTAs take their units from a ticket counter rather than blockIdx, so a
+//    key block only ever waits for one that an earlier (hence running or
+//    finished) CTA took: no wait can depend on a CTA that is not resident.
+//    Queries run from the last step down to the diagonal in both modes, so
+//    the key blocks of a head that start together reach each query chunk at
+//    the same step.
 //
 // TMEM columns (512): S^T buffers [0,64) and [64,128), dP^T buffers [128,192)
 // and [192,256) (dS^T image, or dQ^T in atomic mode, later in the step),
@@ -39,10 +63,14 @@
 
 namespace fa {
 
-constexpr int kKVThreads = 640;  // 4 role warps + 4 row-math warpgroups
+// 4 role warps + 4 row-math warpgroups. (A 21st warp would put six warps on
+// one SM sub-partition and cap every thread at 80 registers, which spills the
+// row math; the dQ reducer therefore shares the TMA producer's thread.)
+constexpr int kKVThreads = 640;
 
 template <int D, bool kAtomic, bool kBias = false>
 struct KVCfg {
+  static constexpr int kThreads = kKVThreads;
   static constexpr int kPanels = D / 64;
   static constexpr uint32_t kKVPanel = kRowsKV * 128;          // 16 KB: 128 rows x 64 elements
   static constexpr uint32_t kKVTile = kPanels * kKVPanel;
@@ -76,9 +104,10 @@ struct KVCfg {
   static constexpr int bDPEmpty = bSEmpty + 2;
   static constexpr int bPFull = bDPEmpty + 2;
   static constexpr int bDSFull = bPFull + 2;                   // [2]: dS^T image written
-  static constexpr int bPEmpty = bDSFull + 2;
-  static constexpr int bDQFull = bPEmpty + 2;
-  static constexpr int bAcc = bDQFull + 2;
+  static constexpr int bDQFull = bDSFull + 2;                  // [2]: dQ^T MMAs (and dK) done
+  static constexpr int bStaged = bDQFull + 2;                  // [2]: dQ^T staged over the image
+  static constexpr int bStageFree = bStaged + 2;               // [2]: staging read by the TMA unit
+  static constexpr int bAcc = bStageFree + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
   static constexpr int kBars = bDrain + 3;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
@@ -101,10 +130,11 @@ __device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row,
 }
 
 template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias>
-__global__ void __launch_bounds__(kKVThreads, 1)
+__global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmBias) {
+                    const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmBias,
+                    const __grid_constant__ CUtensorMap tmDQ) {
   using C = KVCfg<D, kAtomic, kBias>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -113,12 +143,30 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oAbort);
   volatile int* flags = reinterpret_cast<volatile int*>(smem + C::oFlags);
   auto bar = [&](int idx) -> uint32_t { return sb + C::oBar + 8u * idx; };
+  const bool ordered = kAtomic && p.dq_flags != nullptr;
 
   // Work unit: (batch*head or sequence*head, key block), heaviest key blocks
   // first under a causal mask. A key block past the end of its sequence has no
-  // work: the whole CTA leaves before any setup.
+  // work: the whole CTA leaves before any setup. In ordered mode the unit
+  // comes from the ticket counter (taken in order by running CTAs), and the
+  // tiles are outermost over all units, so that the key blocks of one head
+  // that run at the same time are few.
+  int idx = blockIdx.x;
+  if (ordered) {
+    volatile int* slot = reinterpret_cast<volatile int*>(smem + C::oAbort + 4);
+    if (threadIdx.x == 0) {
+      const unsigned int t = atomicAdd(p.dq_ticket, 1u);
+      // A ticket past the grid means the counter was not reset by the
+      // preprocess before this launch: do no work and report it.
+      if (t >= gridDim.x) atomicOr(p.status, kStatusBadLaunch);
+      *slot = t >= gridDim.x ? -1 : (int)t;
+    }
+    __syncthreads();
+    idx = *slot;
+    if (idx < 0) return;
+  }
   Unit u;
-  if (!unit_decode(p, blockIdx.x, kRowsKV, false, u)) return;
+  if (!unit_decode(p, idx, kRowsKV, false, u, ordered ? (1 << 30) : kUnitGroup)) return;
   const int bh = u.bh, b = u.b, h = u.h;
   const int Nl = u.n;                    // rows of this (batch, head) or sequence
   const int j0 = u.tile * kRowsKV;
@@ -126,6 +174,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
   int i_last = Nl - 1;
   if (p.window > 0) i_last = min(i_last, j0 + kRowsKV - 2 + p.window);
   const int nsteps = (i_last >= i_first) ? (i_last - i_first) / kStepQ + 1 : 0;
+  // First query row of step `it`: ascending from the diagonal in the
+  // deterministic kernel, descending from the last step when dQ is accumulated.
+  auto step_i0 = [&](int it) { return i_first + (kAtomic ? nsteps - 1 - it : it) * kStepQ; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bKV), 1);
@@ -140,8 +191,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       mbar_init(bar(C::bDPEmpty + x), kAtomic ? 256 : 1);     // dK done / dQ^T drained
       mbar_init(bar(C::bPFull + x), 256);                      // P~T image of two warpgroups
       mbar_init(bar(C::bDSFull + x), 256);                     // dS^T image of two warpgroups
-      mbar_init(bar(C::bPEmpty + x), 1);                       // atomic: shared dS^T free
       mbar_init(bar(C::bDQFull + x), 1);
+      mbar_init(bar(C::bStaged + x), 2 * D);                   // the warps holding dQ^T rows (d of them per warpgroup)
+      mbar_init(bar(C::bStageFree + x), 1);                    // the reducer
     }
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bAcc), 1);
@@ -157,6 +209,7 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
     prefetch_tmap(&tmDO);
+    if constexpr (kAtomic) prefetch_tmap(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -172,11 +225,10 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tma_load_4d(sb + C::oK + pn * C::kKVPanel, &tmK, bar(C::bKV), 64 * pn, u.row0 + j0, h, b);
         tma_load_4d(sb + C::oV + pn * C::kKVPanel, &tmV, bar(C::bKV), 64 * pn, u.row0 + j0, h, b);
       }
-      int issued = 0;
-      for (int it = 0; it < nsteps; ++it) {
+      // Q, dO (and bias, L, D) of step `it` into its stage.
+      auto issue_stage = [&](int it) {
         const int s = it % C::kNS;
-        if (!mbar_wait(bar(C::bQEmpty + s), ((it / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
-        const int i0 = i_first + it * kStepQ;
+        const int i0 = step_i0(it);
         mbar_arrive_expect_tx(bar(C::bQFull + s), C::kStageBytes);
         for (int pn = 0; pn < C::kPanels; ++pn) {
           tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn,
@@ -190,7 +242,100 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         const long long ws = u.ws + i0;
         bulk_load(sb + C::oL + s * kStepQ * 4, p.ws_nL2 + ws, kStepQ * 4, bar(C::bQFull + s));
         bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_nD + ws, kStepQ * 4, bar(C::bQFull + s));
-        issued = it + 1;
+      };
+      int issued = 0;
+      if constexpr (!kAtomic) {
+        for (int it = 0; it < nsteps; ++it) {
+          if (!mbar_wait(bar(C::bQEmpty + it % C::kNS), ((it / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
+          issue_stage(it);
+          issued = it + 1;
+        }
+      } else {
+        // One loop serves both duties without blocking on either: issue the
+        // next stage once its buffer is free; reduce the next staged dQ tile
+        // once both warpgroups have staged it (and, ordered, once the key
+        // blocks before this one have published their contributions to its
+        // chunks). Ordered contributions are published after completion: just
+        // before the next reduction is issued, or as soon as the loop idles.
+        const bool packed = p.cu_seqlens != nullptr;
+        // accumulator map: (d, rows of one head, heads or batch*heads); this unit's rows start at y0
+        const int z = packed ? u.h : u.bh;
+        const int y0 = (int)(u.acc - (long long)z * p.n_pad);
+        const long long fl0 =
+            (long long)(packed ? u.seq * p.H + u.h : u.bh) * ((packed ? p.seq_pad : p.n_pad) / 32);
+        // Position of this key block among those that visit query step i0
+        // (jlo .. the diagonal block, ascending): exactly the key blocks with
+        // j0 <= i0 under the causal mask and j0 + 126 + window >= i0 under a window.
+        auto chain_pos = [&](int i0) -> unsigned int {
+          int jlo = 0;
+          if (p.window > 0) {
+            const int t = i0 - (kRowsKV - 2) - p.window;
+            if (t > 0) jlo = (t + kRowsKV - 1) / kRowsKV;
+          }
+          return (unsigned int)(u.tile - jlo);
+        };
+        int reduced = 0, pending = -1;  // pending: a step whose ordered contribution awaits publication
+        auto publish = [&]() {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          const int i0 = step_i0(pending);
+          const unsigned int pos = chain_pos(i0);
+          for (int c = 0; c < 2; ++c) st_release_gpu(p.dq_flags + fl0 + (i0 + 32 * c) / 32, pos + 1);
+          pending = -1;
+        };
+        unsigned long long t_idle = 0;
+        uint32_t idle = 0;
+        while (issued < nsteps || reduced < nsteps) {
+          bool progress = false;
+          if (issued < nsteps &&
+              mbar_test_wait(bar(C::bQEmpty + issued % C::kNS), ((issued / C::kNS) & 1) ^ 1)) {
+            issue_stage(issued);
+            ++issued;
+            progress = true;
+          }
+          if (reduced < nsteps && mbar_test_wait(bar(C::bStaged + (reduced & 1)), (reduced >> 1) & 1)) {
+            const int i0 = step_i0(reduced);
+            bool ready = true;
+            if (ordered) {
+              const unsigned int pos = chain_pos(i0);
+              for (int c = 0; c < 2; ++c) ready = ready && ld_acquire_gpu(p.dq_flags + fl0 + (i0 + 32 * c) / 32) >= pos;
+            }
+            if (ready) {
+              if (pending >= 0) publish();
+              if (ordered) fence_proxy_async_global();
+              const uint32_t img = sb + C::oImg + 2 * (reduced & 1) * C::kPTile;
+              for (int c = 0; c < 2; ++c) tma_reduce_add_3d(&tmDQ, img + c * C::kPTile, 0, y0 + i0 + 32 * c, z);
+              bulk_commit_group();
+              bulk_wait_read_all();
+              mbar_arrive(bar(C::bStageFree + (reduced & 1)));
+              if (ordered) pending = reduced;
+              ++reduced;
+              progress = true;
+            }
+          }
+          if (!progress && pending >= 0) {
+            publish();
+            progress = true;
+          }
+          if (progress) {
+            idle = 0;
+            continue;
+          }
+          // Nothing to do: bounded like every other wait of the kernel.
+          if (idle++ == 0) t_idle = globaltimer_ns();
+          if ((idle & 63u) == 0) {
+            if (*abort_flag) break;
+            if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+              atomicOr(p.status, kStatusTimeout);
+              *abort_flag = 1;
+              break;
+            }
+          }
+          __nanosleep(20);
+        }
+        // every reduction has landed (and, ordered, is published) before the CTA exits
+        if (pending >= 0 && !*abort_flag) publish();
+        bulk_wait_all();
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
@@ -318,7 +463,6 @@ __global__ void __launch_bounds__(kKVThreads, 1)
                           (k > 0 || part > 0) ? 1u : 0u);
           }
           tc_commit_w(bar(C::bDQFull + bt));
-          tc_commit_w(bar(C::bPEmpty + bt));
         }
         tc_commit_w(bar(C::bQEmpty + st));
       }
@@ -349,10 +493,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
     bool ok = true;
     for (int it = bb; it < nsteps; it += 2) {
       const int s = it % C::kNS;
-      const int i0 = i_first + it * kStepQ;
+      const int i0 = step_i0(it);
       if (!warp_wait<kRowMathPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
-          !warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
-          (kAtomic && !warp_wait<kRowMathPoll>(bar(C::bPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
+          !warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -445,7 +588,12 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       tc_fence_before();
       warp_arrive(bar(C::bPFull + bb));
       // ---- phase 2: dS^T = P o (dP^T (o Z/(1-p)) + (-D)) ----
-      if (!warp_wait<kRowMathPoll>(bar(C::bDPFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
+      // With dQ accumulation the image of this buffer held the dQ^T staging of
+      // step it - 2 until the reducer's TMA read it (a fresh barrier passes the
+      // first wait).
+      if (!warp_wait<kRowMathPoll>(bar(C::bDPFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
+          (kAtomic &&
+           !warp_wait<kRowMathPoll>(bar(C::bStageFree + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
@@ -504,7 +652,9 @@ __global__ void __launch_bounds__(kKVThreads, 1)
       if constexpr (kAtomic) fence_proxy_async_smem();
       warp_arrive(bar(C::bDSFull + bb));
       if constexpr (kAtomic) {
-        // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> fp32 accumulator.
+        // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> the staging
+        // tile [32 queries][d] fp32 over this warpgroup's half of the image; the
+        // reducer adds it into the accumulator.
         if (!warp_wait<kRowMathPoll>(bar(C::bDQFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
@@ -515,10 +665,13 @@ __global__ void __launch_bounds__(kKVThreads, 1)
         tmem_ld_wait(r0);
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty + bb));
-        if (jl < D) {
-          float* dst = p.ws_dq + (u.acc + base) * D + jl;
+        if (wq < D / 32) {  // lanes of the warps holding rows d < D of the M = 128 dQ^T
+          const uint32_t stg = sb + C::oImg + (2 * bb + c) * C::kPTile + (uint32_t)jl * 4;
 #pragma unroll
-          for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
+          for (int x = 0; x < 32; ++x)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)x * (D * 4)), "r"(r0[x]) : "memory");
+          fence_proxy_async_smem();
+          warp_arrive(bar(C::bStaged + bb));
         }
       }
     }
@@ -574,7 +727,7 @@ static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, c
   const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
   const int tiles = (rows + kRowsKV - 1) / kRowsKV;
   const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
-  kern<<<grid, kKVThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4]);
+  kern<<<grid, C::kThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
   return cudaGetLastError();
 }
 
@@ -599,9 +752,10 @@ static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, const CUtenso
   return atomic ? launch_dkdv_a<D, kBf16, true>(p, maps, st) : launch_dkdv_a<D, kBf16, false>(p, maps, st);
 }
 
-// maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows), and
-// the attention bias (boxes of kStepQ rows x kRowsKV keys; any valid map when
-// p.bias is null).
+// maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows), the
+// attention bias (boxes of kStepQ rows x kRowsKV keys; any valid map when
+// p.bias is null), and the fp32 dQ accumulator as (d, rows per head, heads)
+// with boxes of d x 32 rows (any valid map in the deterministic kernel).
 cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
                                cudaStream_t st) {
   if (p.d == 128)

@@ -88,14 +88,42 @@ enum {
   FA_ERR_TIMEOUT = -6      /* a kernel's bounded wait gave up (see fa_get_device_status) */
 };
 
+/* dQ algorithms, selected by the `deterministic` argument of the backward
+ * entry points ("FlashAttention backward", §The loop structure: who
+ * accumulates cleanly, who needs atomics; "Lecture 7 — Backward Pass and
+ * Validation", §Determinism):
+ *  FA_DQ_ATOMIC (0): the key/value-major kernel also forms dQ^T = K^T dS^T per
+ *    tile and adds it into an fp32 accumulator with TMA reduce-adds in no fixed
+ *    order, then a conversion pass scales and rounds it. Five contractions per
+ *    tile pair; dQ may differ in the last bits between runs.
+ *  FA_DQ_DETERMINISTIC (1): the library's deterministic default, currently
+ *    FA_DQ_RECOMPUTE.
+ *  FA_DQ_RECOMPUTE (2): a separate query-major kernel recomputes S and dP and
+ *    accumulates dQ on chip. Seven contractions per tile pair; bit-identical
+ *    run to run.
+ *  FA_DQ_ORDERED (3): as FA_DQ_ATOMIC, but the contributions of the key blocks
+ *    to each 32-row query chunk are added in ascending key-block order (each
+ *    waits for its predecessors through a counter in the workspace), so the
+ *    fp32 sums, and dQ, are bit-identical run to run. Five contractions per
+ *    tile pair.
+ * dK and dV are deterministic in every mode. fp32 inputs always take the
+ * query-major path. Other values return FA_ERR_INVALID_ARG (and a workspace
+ * size of 0). */
+#define FA_DQ_ATOMIC 0
+#define FA_DQ_DETERMINISTIC 1
+#define FA_DQ_RECOMPUTE 2
+#define FA_DQ_ORDERED 3
+
 /* Element strides of the [B, N, H, d] tensors; the d stride is 1. */
 typedef struct {
   int64_t b, n, h;
 } fa_strides;
 
 /* Bytes of device workspace fa_bwd needs: two fp32 vectors of B*H*roundup(N,128)
- * (L*log2(e) and D), plus, for fp16/bf16 with deterministic == 0, the fp32 dQ
- * accumulator of B*H*roundup(N,128)*d floats. Returns 0 for invalid sizes. */
+ * (L*log2(e) and D), plus, for fp16/bf16 with FA_DQ_ATOMIC or FA_DQ_ORDERED,
+ * the fp32 dQ accumulator of B*H*roundup(N,128)*d floats, plus, for
+ * FA_DQ_ORDERED, one 32-bit counter per 32 padded rows and a 256-byte slot for
+ * the unit ticket. Returns 0 for invalid sizes or modes. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, fa_dtype dtype, int deterministic);
 
 /* Forward: writes O ([B, N, H, d], dtype) and lse ([B, H, N] fp32, natural
@@ -105,15 +133,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            uint64_t seed, uint64_t offset, void* stream);
 
 /* Backward: from Q, K, V, the forward's O and lse, and dO, writes dQ, dK, dV
- * (same dtype and strides). deterministic != 0 (the default the library
- * recommends) computes dQ in a separate query-major kernel, bit-reproducible
- * run to run; deterministic == 0 adds dQ with fp32 atomics from the
- * key/value-major kernel and converts it afterwards (faster, dQ may differ in
- * the last bits between runs; dK and dV are deterministic in both modes).
- * fp32 inputs always use the deterministic path. `workspace` must be
- * 256-byte aligned and hold fa_bwd_workspace_size(...) bytes; its contents on
- * entry do not matter. Runs fa_bwd_stage(FA_BWD_PREPROCESS), (FA_BWD_DKDV),
- * (FA_BWD_DQ) in order on `stream`. */
+ * (same dtype and strides). `deterministic` selects the dQ algorithm (FA_DQ_*
+ * above; nonzero values are bit-reproducible run to run). `workspace` must be
+ * 256-byte aligned and hold fa_bwd_workspace_size(...) bytes for the same
+ * mode; its contents on entry do not matter. Runs fa_bwd_stage
+ * (FA_BWD_PREPROCESS), (FA_BWD_DKDV), (FA_BWD_DQ) in order on `stream`; with
+ * FA_DQ_RECOMPUTE the dQ kernel runs on a library-owned side stream beside the
+ * dK/dV kernel, joined back into `stream` before the call returns. */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, fa_strides strides, fa_dtype dtype,
            float scale, int causal, int window, float dropout_p, uint64_t seed, uint64_t offset,
@@ -122,10 +148,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 /* The three steps of fa_bwd, for callers that schedule or time them apart.
  * Arguments as fa_bwd; the stages must run in order with the same arguments.
  *  FA_BWD_PREPROCESS: D_i = rowsum(dO o O) and lse*log2(e) into the workspace;
- *                     zero-fills the dQ accumulator in atomic mode.
- *  FA_BWD_DKDV:       key/value-major kernel: dK, dV (and atomic dQ adds).
- *  FA_BWD_DQ:         deterministic: query-major dQ kernel; atomic: dQ =
- *                     scale * accumulator, rounded to the dtype. */
+ *                     zero-fills the dQ accumulator (FA_DQ_ATOMIC, FA_DQ_ORDERED)
+ *                     and the chunk counters and unit ticket (FA_DQ_ORDERED).
+ *  FA_BWD_DKDV:       key/value-major kernel: dK, dV (and the dQ adds of
+ *                     FA_DQ_ATOMIC / FA_DQ_ORDERED). With FA_DQ_ORDERED it must
+ *                     follow a FA_BWD_PREPROCESS on the same workspace (it
+ *                     consumes the ticket the preprocess resets; a second
+ *                     launch without one does no work and sets status bit 2).
+ *  FA_BWD_DQ:         FA_DQ_RECOMPUTE: query-major dQ kernel; FA_DQ_ATOMIC /
+ *                     FA_DQ_ORDERED: dQ = scale * accumulator, rounded to the
+ *                     dtype. */
 typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ = 2 } fa_bwd_stage_id;
 
 int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void* v, const void* o,
@@ -139,7 +171,7 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
  * allocations, a runtime recording work before any allocator exists, an
  * embedding that hands over only the tensors). The pages describe no such
  * entry point; it is this library's own. Arguments as fa_bwd, without the
- * deterministic flag (always deterministic) and without a workspace: the
+ * deterministic flag (always FA_DQ_RECOMPUTE) and without a workspace: the
  * scratch (D and lse*log2(e) vectors) lives in one fixed 8 MiB device array
  * inside the library, so the call allocates nothing. Limit:
  * B*H*roundup(N,128) <= 1048576; larger problems return FA_ERR_WORKSPACE and
@@ -260,7 +292,8 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
 
 /* Reads (and with clear != 0 resets) the status word of the current device.
  * Call after synchronising the streams the kernels ran on. *status receives
- * the raw bits (1 = a bounded wait timed out). Returns FA_OK, FA_ERR_TIMEOUT
+ * the raw bits (1 = a bounded wait timed out; 2 = an FA_DQ_ORDERED dK/dV
+ * launch found its unit ticket not reset and did nothing). Returns FA_OK, FA_ERR_TIMEOUT
  * when the timeout bit is set, or FA_ERR_CUDA. This call synchronises the device. */
 int fa_get_device_status(unsigned int* status, int clear);
 

@@ -20,6 +20,11 @@ F32_REL_L2 = 1e-5
 LSE_ATOL = 1e-4
 EXACT_REL_L2 = 1e-2  # composed forward -> backward, 16-bit dtypes (secondary bar)
 
+# The dQ algorithms every parity test runs: the deterministic default (query-major
+# recompute), atomic accumulation, and the ordered (deterministic) accumulation.
+DQ_MODES = [True, False, fa.FA_DQ_ORDERED]
+DQ_IDS = ["det", "atomic", "ordered"]
+
 
 def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)

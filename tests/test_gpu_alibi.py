@@ -13,7 +13,7 @@ import torch
 import flashattention_backward_fa_gb300 as fa
 import oracle
 from flashattention_backward_fa_gb300.inputs import Workload, make_inputs, make_varlen_inputs
-from gpu_check import LSE_ATOL, to_np, within
+from gpu_check import DQ_IDS, DQ_MODES, LSE_ATOL, to_np, within
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +51,7 @@ def _run(w, slopes, deterministic):
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
-@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_alibi_against_oracle(case, deterministic):
     dtype, d, N, causal, window, p, per_batch = case
     if dtype == "f32" and not deterministic:

@@ -13,7 +13,7 @@ import torch
 import flashattention_backward_fa_gb300 as fa
 import oracle
 from flashattention_backward_fa_gb300.inputs import Workload, make_inputs
-from gpu_check import LSE_ATOL, to_np, within
+from gpu_check import DQ_IDS, DQ_MODES, LSE_ATOL, to_np, within
 
 pytestmark = pytest.mark.gpu
 
@@ -88,7 +88,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
-@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_bias_against_oracle(case, deterministic):
     dtype, d, N, causal, window, p, bb, bh, pad = case
     if dtype == "f32" and not deterministic:

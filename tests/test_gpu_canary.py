@@ -19,7 +19,7 @@ gradient. After each call every byte outside the declared outputs must still
 hold the sentinel, and the outputs must match the float64 oracle under the
 usual gate. Cases: a ragged tail (N = 333), a sliding window with dropout,
 non-causal d = 64, the fp32 path, and packed variable-length sequences, each
-in both dQ modes where the path has two.
+in every dQ mode the path has (query-major recompute, atomic, ordered).
 """
 import numpy as np
 import pytest
@@ -28,7 +28,7 @@ import torch
 import flashattention_backward_fa_gb300 as fa
 import oracle
 from flashattention_backward_fa_gb300.inputs import Workload, make_inputs, make_varlen_inputs
-from gpu_check import LSE_ATOL, to_np, within
+from gpu_check import DQ_IDS, DQ_MODES, LSE_ATOL, to_np, within
 
 pytestmark = pytest.mark.gpu
 
@@ -127,15 +127,15 @@ CASES = {
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
-@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_guard_bands_fixed_length(case, deterministic):
     w = CASES[case]
-    if w.dtype == "f32" and not deterministic:
+    if w.dtype == "f32" and deterministic is not True:
         pytest.skip("fp32 has one dQ path")
     _run_fixed(w, deterministic)
 
 
-@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 @pytest.mark.parametrize("dtype,d,causal,window", [("bf16", 128, True, 0), ("f16", 64, True, 100)])
 def test_guard_bands_varlen(dtype, d, causal, window, deterministic):
     lengths = [1, 127, 300, 0, 129, 64]

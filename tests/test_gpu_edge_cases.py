@@ -15,7 +15,7 @@ import torch
 
 import flashattention_backward_fa_gb300 as fa
 from flashattention_backward_fa_gb300.inputs import Workload, make_inputs
-from gpu_check import check_against_oracle, run_gpu, to_np
+from gpu_check import DQ_IDS, DQ_MODES, check_against_oracle, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def test_window_longer_than_sequence_is_no_window(dtype, d):
 
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 64)])
-@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_zero_upstream_gradient_gives_zero_gradients(dtype, d, deterministic):
     if dtype == "f32" and not deterministic:
         pytest.skip("fp32 has one dQ path")
@@ -100,7 +100,7 @@ def test_large_scores_stay_finite(dtype, d):
 @pytest.mark.parametrize("N", [127, 128, 129, 255, 256, 257, 511])
 def test_tile_boundaries(N):
     w = Workload(f"tb{N}", 1, 2, N, 128, "bf16", causal=True, input_seed=N)
-    for det in (True, False):
+    for det in DQ_MODES:
         res = run_gpu(w, deterministic=det)
         fails, _ = check_against_oracle(w, res, exact=False)
         assert not fails, (det, fails)

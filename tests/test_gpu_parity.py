@@ -10,7 +10,7 @@ import torch
 
 import flashattention_backward_fa_gb300 as fa
 from flashattention_backward_fa_gb300.inputs import Workload
-from gpu_check import check_against_oracle, run_gpu, to_np
+from gpu_check import DQ_IDS, DQ_MODES, check_against_oracle, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ for dtype in ("bf16", "f16"):
 
 
 @pytest.mark.parametrize("w", TC_CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_tensor_core_path(w, deterministic):
     res = run_gpu(w, deterministic=deterministic)
     failures, report = check_against_oracle(w, res)
@@ -58,19 +58,42 @@ def test_bhnd_strides(dtype):
     assert not failures, (failures, report)
 
 
+@pytest.mark.parametrize("mode", [fa.FA_DQ_RECOMPUTE, fa.FA_DQ_ORDERED], ids=["recompute", "ordered"])
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("f32", 64)])
-def test_deterministic_bit_identical(dtype, d):
-    """Deterministic mode: ten backward runs on the same inputs are bit-identical."""
+def test_deterministic_bit_identical(dtype, d, mode):
+    """Both deterministic dQ modes: ten backward runs on the same inputs are bit-identical."""
     w = _w(dtype, d, 700 if dtype != "f32" else 200, True, 0, 0.1 if dtype == "f16" else 0.0, B=1, H=4, seed=700)
     from flashattention_backward_fa_gb300.inputs import make_inputs
     q, k, v, do = (t.cuda() for t in make_inputs(w))
     kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed)
     o, lse = fa.attention_forward(q, k, v, **kw)
-    ref = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=True)
+    ref = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=mode)
     for _ in range(9):
-        again = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=True)
+        again = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=mode)
         for a, b in zip(ref, again):
             assert torch.equal(a, b)
+
+
+def test_ordered_dq_equals_a_fixed_order_sum():
+    """The ordered mode's dQ is the same fp32 sum whatever the launch timing:
+    with many key blocks per query chunk (N = 2048, 16 key blocks) and several
+    heads, runs interleaved with other work still agree bit for bit, and dK, dV
+    equal the other modes' (they do not depend on the dQ algorithm)."""
+    w = _w("bf16", 128, 2048, True, B=2, H=3, seed=710)
+    from flashattention_backward_fa_gb300.inputs import make_inputs
+    q, k, v, do = (t.cuda() for t in make_inputs(w))
+    o, lse = fa.attention_forward(q, k, v, causal=True)
+    ref = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_ORDERED)
+    rec = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_RECOMPUTE)
+    busy = torch.randn(4096, 4096, device="cuda")
+    for i in range(5):
+        if i % 2:
+            busy = busy @ busy.T * 1e-3  # other work queued ahead on the stream
+        again = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_ORDERED)
+        for a, b in zip(ref, again):
+            assert torch.equal(a, b)
+    assert torch.equal(ref[1], rec[1]) and torch.equal(ref[2], rec[2])
+    assert fa.fa_get_device_status(clear=True) == 0
 
 
 def test_atomic_mode_dk_dv_deterministic():
@@ -94,7 +117,7 @@ def test_zero_gradient_across_causal_boundary(dtype, d):
     r = 150
     do[:, r:] = 0
     o, lse = fa.attention_forward(q, k, v, causal=True)
-    for det in (True, False):
+    for det in DQ_MODES:
         dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=det)
         assert torch.all(dk[:, r:] == 0) and torch.all(dv[:, r:] == 0) and torch.all(dq[:, r:] == 0)
         assert torch.all(dv[:, :r].abs().sum(-1) > 0)

@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import flashattention_backward_fa_gb300 as fa
+from gpu_check import DQ_IDS, DQ_MODES
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -76,7 +77,7 @@ def test_backward_mask_bit_exact(dtype):
     v = torch.randn(B, N, H, d, generator=g).to(dtype).cuda()
     do = torch.eye(N, d).reshape(1, N, 1, d).expand(B, N, H, d).contiguous().to(dtype).cuda()
     o, lse = fa.attention_forward(q, k, v, dropout_p=p, seed=seed, offset=off)
-    for det in (True, False):
+    for det in DQ_MODES:
         _, _, dv = fa.attention_backward(q, k, v, o, do, lse, dropout_p=p, seed=seed, offset=off, deterministic=det)
         got = (dv.float().cpu() != 0).numpy()
         for h in range(H):

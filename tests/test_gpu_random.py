@@ -31,7 +31,9 @@ def _configs(n=40, seed=2026):
         p = float(r.choice([0.0, 0.0, 0.1, 0.25]))
         extra = str(r.choice(["none", "none", "alibi", "bias"]))
         det = bool(r.random() < 0.6) or dtype == "f32"
-        out.append((t, dtype, d, N, B, H, causal, window, p, extra, det))
+        # the accumulating dQ modes alternate: atomic on odd t, ordered on even t
+        mode = True if det else (False if t % 2 else fa.FA_DQ_ORDERED)
+        out.append((t, dtype, d, N, B, H, causal, window, p, extra, mode))
     return out
 
 

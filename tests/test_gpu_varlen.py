@@ -13,7 +13,7 @@ import torch
 import flashattention_backward_fa_gb300 as fa
 import oracle
 from flashattention_backward_fa_gb300.inputs import make_varlen_inputs, varlen_lengths
-from gpu_check import LSE_ATOL, to_np, within
+from gpu_check import DQ_IDS, DQ_MODES, LSE_ATOL, to_np, within
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def _check(inputs, outs, dtype, causal, window):
 @pytest.mark.parametrize("dtype,d,causal,window", [("bf16", 128, True, 0), ("f16", 64, True, 0),
                                                    ("bf16", 64, False, 0), ("f16", 128, True, 100),
                                                    ("bf16", 128, False, 200)])
-@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_varlen_ragged(dtype, d, causal, window, deterministic):
     inputs, outs = _run(RAGGED, 3, d, dtype, causal, window, deterministic, seed=d + window)
     _check(inputs, outs, dtype, causal, window)

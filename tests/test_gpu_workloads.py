@@ -16,7 +16,7 @@ import torch
 import flashattention_backward_fa_gb300 as fa
 import oracle
 from flashattention_backward_fa_gb300.inputs import WORKLOADS, make_inputs
-from gpu_check import LSE_ATOL, check_against_oracle, to_np, within
+from gpu_check import DQ_IDS, DQ_MODES, LSE_ATOL, check_against_oracle, to_np, within
 
 pytestmark = pytest.mark.gpu
 
@@ -85,7 +85,7 @@ def test_fp32_n128_d64_full():
     assert not failures, (failures, report)
 
 
-@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_bf16_causal_b4h16_n2048_whole_heads(deterministic):
     w = WORKLOADS["bf16_causal_b4h16_n2048_d128"]
     res = _gpu(w, deterministic)
@@ -98,7 +98,7 @@ def test_bf16_causal_b4h16_n2048_whole_heads(deterministic):
             assert ok, (b, h, name, rep)
 
 
-@pytest.mark.parametrize("deterministic", [True, False], ids=["det", "atomic"])
+@pytest.mark.parametrize("deterministic", DQ_MODES, ids=DQ_IDS)
 def test_bf16_causal_b1h32_n8192_sampled(deterministic):
     w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
     res = _gpu(w, deterministic)
@@ -107,19 +107,19 @@ def test_bf16_causal_b1h32_n8192_sampled(deterministic):
 
 
 def _gpu_both_modes(w):
-    """Forward once, then the backward in both dQ modes on the same O and L."""
+    """Forward once, then the backward in every dQ mode on the same O and L."""
     q, k, v, do = (t.cuda() for t in make_inputs(w))
     kw = dict(scale=w.scale, causal=w.causal, window=w.window, dropout_p=w.dropout_p, seed=w.philox_seed,
               offset=w.philox_offset)
     o, lse = fa.attention_forward(q, k, v, **kw)
     out = {"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse}
-    for det in (True, False):
-        dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=det)
+    for mode, name in zip(DQ_MODES, DQ_IDS):
+        dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, **kw, deterministic=mode)
         torch.cuda.synchronize()
         assert fa.fa_get_device_status(clear=True) == 0
         for t in (dq, dk, dv):
             assert torch.isfinite(t).all()
-        out["det" if det else "atomic"] = tuple(t.cpu() for t in (dq, dk, dv))
+        out[name] = tuple(t.cpu() for t in (dq, dk, dv))
         del dq, dk, dv
     for n in ("q", "k", "v", "do", "o", "lse"):
         out[n] = out[n].cpu()
@@ -128,7 +128,7 @@ def _gpu_both_modes(w):
 
 
 def _check_whole_heads(w, res, heads):
-    """Every element of dQ, dK, dV of the listed heads, both dQ modes, against
+    """Every element of dQ, dK, dV of the listed heads, every dQ mode, against
     the oracle in function mode (the O and L the GPU forward produced)."""
     args = (w.scale, w.causal, w.window, w.dropout_p, w.philox_seed, w.philox_offset)
     failures = []
@@ -136,7 +136,7 @@ def _check_whole_heads(w, res, heads):
         a = {n: to_np(res[n][b:b + 1, :, h:h + 1, :]) for n in ("q", "k", "v", "do", "o")}
         lse = res["lse"][b:b + 1, h:h + 1].double().numpy()
         rq, rk, rv, _ = oracle.backward(a["q"], a["k"], a["v"], a["o"], a["do"], lse, *args)
-        for mode in ("det", "atomic"):
+        for mode in DQ_IDS:
             for name, g, r in zip(("dq", "dk", "dv"), res[mode], (rq, rk, rv)):
                 ok, rep = within(to_np(g[b:b + 1, :, h:h + 1, :]), r, w.dtype)
                 if not ok:
@@ -145,7 +145,7 @@ def _check_whole_heads(w, res, heads):
 
 
 def test_bf16_causal_b1h32_n8192_whole_tensor():
-    """The headline workload: all 32 heads, every element, both dQ modes."""
+    """The headline workload: all 32 heads, every element, every dQ mode."""
     w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
     res = _gpu_both_modes(w)
     failures = _check_whole_heads(w, res, [(0, h) for h in range(w.H)])
@@ -153,7 +153,7 @@ def test_bf16_causal_b1h32_n8192_whole_tensor():
 
 
 def test_bf16_causal_b1h8_n32768_whole_heads():
-    """The longest workload: two whole heads (first and last), every element, both dQ modes."""
+    """The longest workload: two whole heads (first and last), every element, every dQ mode."""
     w = WORKLOADS["bf16_causal_b1h8_n32768_d128"]
     res = _gpu_both_modes(w)
     failures = _check_whole_heads(w, res, [(0, 0), (0, w.H - 1)])
@@ -175,19 +175,21 @@ def test_bf16_causal_b1h8_n32768_sampled():
 
 def test_fp16_window_dropout_b2h16_n4096_sampled():
     w = WORKLOADS["fp16_window1024_drop0.1_b2h16_n4096_d64"]
-    for det in (True, False):
+    for det in DQ_MODES:
         res = _gpu(w, det)
         failures = _check_sampled(w, res, [(0, 0), (1, 15)], seed=3)
         assert not failures, (det, failures)
 
 
-def test_headline_deterministic_bit_identical_ten_runs():
+@pytest.mark.parametrize("mode", [fa.FA_DQ_RECOMPUTE, fa.FA_DQ_ORDERED], ids=["recompute", "ordered"])
+def test_headline_deterministic_bit_identical_ten_runs(mode):
     w = WORKLOADS["bf16_causal_b1h32_n8192_d128"]
     q, k, v, do = (t.cuda() for t in make_inputs(w))
     o, lse = fa.attention_forward(q, k, v, causal=True)
-    ws = fa.alloc_workspace(q, True)
-    ref = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws)
+    ws = fa.alloc_workspace(q, mode)
+    ref = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws, deterministic=mode)
     for _ in range(9):
-        again = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws)
+        again = fa.attention_backward(q, k, v, o, do, lse, causal=True, workspace=ws, deterministic=mode)
         for a_, b_ in zip(ref, again):
             assert torch.equal(a_, b_)
+    assert fa.fa_get_device_status(clear=True) == 0
