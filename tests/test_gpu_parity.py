@@ -78,13 +78,14 @@ def test_ordered_dq_equals_a_fixed_order_sum():
     """The ordered mode's dQ is the same fp32 sum whatever the launch timing:
     with many key blocks per query chunk (N = 2048, 16 key blocks) and several
     heads, runs interleaved with other work still agree bit for bit, and dK, dV
-    equal the other modes' (they do not depend on the dQ algorithm)."""
+    equal the atomic mode's (the same kernel forms them; only the order in
+    which dQ contributions land differs)."""
     w = _w("bf16", 128, 2048, True, B=2, H=3, seed=710)
     from flashattention_backward_fa_gb300.inputs import make_inputs
     q, k, v, do = (t.cuda() for t in make_inputs(w))
     o, lse = fa.attention_forward(q, k, v, causal=True)
     ref = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_ORDERED)
-    rec = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_RECOMPUTE)
+    ato = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_ATOMIC)
     busy = torch.randn(4096, 4096, device="cuda")
     for i in range(5):
         if i % 2:
@@ -92,7 +93,7 @@ def test_ordered_dq_equals_a_fixed_order_sum():
         again = fa.attention_backward(q, k, v, o, do, lse, causal=True, deterministic=fa.FA_DQ_ORDERED)
         for a, b in zip(ref, again):
             assert torch.equal(a, b)
-    assert torch.equal(ref[1], rec[1]) and torch.equal(ref[2], rec[2])
+    assert torch.equal(ref[1], ato[1]) and torch.equal(ref[2], ato[2])
     assert fa.fa_get_device_status(clear=True) == 0
 
 
