@@ -201,40 +201,24 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // This thread's committed bulk groups have completed (their global writes are done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// All but the most recently committed bulk group of this thread have completed.
+__device__ __forceinline__ void bulk_wait_all_but_last() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
 // Orders this thread's async-proxy global accesses (TMA) with its generic ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ptr) {
+// A plain (relaxed) GPU-scope read for polling: it does not hold back this
+// thread's later memory operations; acquire with fence_acquire_gpu once the
+// value is the one waited for.
+__device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* ptr) {
   unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
 }
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
-// Waits until a global counter another CTA publishes (st_release_gpu) reaches
-// `target`. Bounded like mbar_wait: on the wall-clock limit it sets the timeout
-// status bit and the CTA's abort flag and returns false; it also returns false
-// once another role of the CTA has aborted.
-__device__ __forceinline__ bool flag_wait_geq(const unsigned int* flag, unsigned int target, volatile int* abort_flag,
-                                              unsigned int* status) {
-  if (ld_acquire_gpu(flag) >= target) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    __nanosleep(32);
-    if (ld_acquire_gpu(flag) >= target) return true;
-    if ((spin & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(status, kStatusTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // Wait that ignores the abort flag, used to let in-flight copies or MMAs land
 // before a CTA that gave up exits. Also bounded.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int* status) {

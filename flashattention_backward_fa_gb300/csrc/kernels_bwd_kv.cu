@@ -32,18 +32,23 @@
 // take alternate query steps, warpgroup w using buffer w, and write the dV
 // (warpgroup 0) / dK (warpgroup 1) epilogue.
 //
-// dQ (atomic and ordered modes). The row-math warps move dQ^T from TMEM into a
-// staging tile in shared memory, laid out [32 query rows][d] fp32 per
-// warpgroup, over the dS^T image of the step (the dK and dQ^T MMAs have read
-// it by then, and the image of that buffer is not rewritten until the same
-// warpgroups' phase 2 two steps later). The TMA producer thread, which also
-// acts as the reducer, adds each staged tile into the fp32 accumulator with one
-// TMA tensor reduce-add, so the reduction costs the row-math warps 32 shared
-// stores a step instead of 32 global atomics. It releases the staging area as
-// soon as the TMA unit has read it. Producer and reducer duties are served by
-// one polling loop that never blocks on either.
-//  * atomic: reductions of different key blocks land in any order.
-//  * ordered (deterministic): every 32-row query chunk keeps a counter of the
+// dQ (atomic and ordered modes).
+//  * atomic: each row-math thread adds its 32 dQ^T values (one d row, the
+//    warpgroup's 32 queries) into the fp32 accumulator with red.add straight
+//    from the TMEM load; a warp's reduction covers 128 contiguous bytes.
+//    Reductions of different key blocks land in any order. (Staging the tile
+//    in shared memory for one TMA reduce-add, as the ordered mode does,
+//    measured slower: this kernel is bound by shared-memory bandwidth, and
+//    staging adds a write and a TMA read of 32 KB a step.)
+//  * ordered (deterministic): the row-math warps move dQ^T from TMEM into a
+//    staging tile in shared memory, laid out [32 query rows][d] fp32 per
+//    warpgroup, over the dS^T image of the step (the dK and dQ^T MMAs have read
+//    it by then, and the image of that buffer is not rewritten until the same
+//    warpgroups' phase 2 two steps later). The TMA producer thread, which also
+//    acts as the reducer, adds each staged tile into the accumulator with one
+//    TMA tensor reduce-add and releases the staging area as soon as the TMA
+//    unit has read it; producer and reducer duties share one polling loop
+//    that never blocks on either. Every 32-row query chunk keeps a counter of the
 //    contributions already added; key block j waits until its predecessors
 //    (key blocks jlo .. j-1 of that chunk, in ascending order) are complete,
 //    adds its own, waits for completion and publishes count + 1. The fp32 sums
@@ -244,19 +249,21 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         bulk_load(sb + C::oD + s * kStepQ * 4, p.ws_nD + ws, kStepQ * 4, bar(C::bQFull + s));
       };
       int issued = 0;
-      if constexpr (!kAtomic) {
+      if (!ordered) {
         for (int it = 0; it < nsteps; ++it) {
           if (!mbar_wait(bar(C::bQEmpty + it % C::kNS), ((it / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
           issue_stage(it);
           issued = it + 1;
         }
-      } else {
+      } else if constexpr (kAtomic) {
         // One loop serves both duties without blocking on either: issue the
         // next stage once its buffer is free; reduce the next staged dQ tile
         // once both warpgroups have staged it (and, ordered, once the key
         // blocks before this one have published their contributions to its
-        // chunks). Ordered contributions are published after completion: just
-        // before the next reduction is issued, or as soon as the loop idles.
+        // chunks). An ordered contribution is published once it has completed:
+        // right after the next step's reduction has been issued (waiting for
+        // every bulk group but that newest one), or as soon as the loop idles,
+        // so a step's reduction never waits for the previous one to land.
         const bool packed = p.cu_seqlens != nullptr;
         // accumulator map: (d, rows of one head, heads or batch*heads); this unit's rows start at y0
         const int z = packed ? u.h : u.bh;
@@ -275,8 +282,8 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           return (unsigned int)(u.tile - jlo);
         };
         int reduced = 0, pending = -1;  // pending: a step whose ordered contribution awaits publication
+        // Publishes `pending`, whose bulk group has completed (the caller waited).
         auto publish = [&]() {
-          bulk_wait_all();
           fence_proxy_async_global();
           const int i0 = step_i0(pending);
           const unsigned int pos = chain_pos(i0);
@@ -295,25 +302,30 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           }
           if (reduced < nsteps && mbar_test_wait(bar(C::bStaged + (reduced & 1)), (reduced >> 1) & 1)) {
             const int i0 = step_i0(reduced);
-            bool ready = true;
-            if (ordered) {
-              const unsigned int pos = chain_pos(i0);
-              for (int c = 0; c < 2; ++c) ready = ready && ld_acquire_gpu(p.dq_flags + fl0 + (i0 + 32 * c) / 32) >= pos;
-            }
-            if (ready) {
-              if (pending >= 0) publish();
-              if (ordered) fence_proxy_async_global();
+            // both chunk counters are read before either value is used, with
+            // relaxed loads (acquired once they show every predecessor)
+            const unsigned int pos = chain_pos(i0);
+            const unsigned int f0 = ld_relaxed_gpu(p.dq_flags + fl0 + i0 / 32);
+            const unsigned int f1 = ld_relaxed_gpu(p.dq_flags + fl0 + i0 / 32 + 1);
+            if (f0 >= pos && f1 >= pos) {
+              fence_acquire_gpu();
+              fence_proxy_async_global();
               const uint32_t img = sb + C::oImg + 2 * (reduced & 1) * C::kPTile;
               for (int c = 0; c < 2; ++c) tma_reduce_add_3d(&tmDQ, img + c * C::kPTile, 0, y0 + i0 + 32 * c, z);
               bulk_commit_group();
               bulk_wait_read_all();
               mbar_arrive(bar(C::bStageFree + (reduced & 1)));
-              if (ordered) pending = reduced;
+              if (pending >= 0) {
+                bulk_wait_all_but_last();  // the previous step's group has landed
+                publish();
+              }
+              pending = reduced;
               ++reduced;
               progress = true;
             }
           }
           if (!progress && pending >= 0) {
+            bulk_wait_all();
             publish();
             progress = true;
           }
@@ -334,8 +346,8 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           __nanosleep(20);
         }
         // every reduction has landed (and, ordered, is published) before the CTA exits
-        if (pending >= 0 && !*abort_flag) publish();
         bulk_wait_all();
+        if (pending >= 0 && !*abort_flag) publish();
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
@@ -588,11 +600,11 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
       tc_fence_before();
       warp_arrive(bar(C::bPFull + bb));
       // ---- phase 2: dS^T = P o (dP^T (o Z/(1-p)) + (-D)) ----
-      // With dQ accumulation the image of this buffer held the dQ^T staging of
-      // step it - 2 until the reducer's TMA read it (a fresh barrier passes the
+      // In ordered mode the image of this buffer held the dQ^T staging of step
+      // it - 2 until the reducer's TMA read it (a fresh barrier passes the
       // first wait).
       if (!warp_wait<kRowMathPoll>(bar(C::bDPFull + bb), (it >> 1) & 1, abort_flag, p.status) ||
-          (kAtomic &&
+          (ordered &&
            !warp_wait<kRowMathPoll>(bar(C::bStageFree + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status))) {
         ok = false;
         break;
@@ -666,12 +678,18 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         tc_fence_before();
         warp_arrive(bar(C::bDPEmpty + bb));
         if (wq < D / 32) {  // lanes of the warps holding rows d < D of the M = 128 dQ^T
-          const uint32_t stg = sb + C::oImg + (2 * bb + c) * C::kPTile + (uint32_t)jl * 4;
+          if (ordered) {
+            const uint32_t stg = sb + C::oImg + (2 * bb + c) * C::kPTile + (uint32_t)jl * 4;
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)x * (D * 4)), "r"(r0[x]) : "memory");
-          fence_proxy_async_smem();
-          warp_arrive(bar(C::bStaged + bb));
+            for (int x = 0; x < 32; ++x)
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (uint32_t)x * (D * 4)), "r"(r0[x]) : "memory");
+            fence_proxy_async_smem();
+            warp_arrive(bar(C::bStaged + bb));
+          } else {
+            float* dst = p.ws_dq + (u.acc + base) * D + jl;
+#pragma unroll
+            for (int x = 0; x < 32; ++x) atomicAdd(dst + x * D, __uint_as_float(r0[x]));
+          }
         }
       }
     }
