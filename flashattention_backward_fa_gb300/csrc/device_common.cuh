@@ -215,9 +215,12 @@ __device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* ptr) 
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+// GPU-scope acquire-release fence: after relaxed reads, it acquires what they
+// observed; before relaxed writes, it releases every earlier memory operation
+// of this thread (one fence serves several flag stores).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_gpu(unsigned int* ptr, unsigned int v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 // Wait that ignores the abort flag, used to let in-flight copies or MMAs land
 // before a CTA that gave up exits. Also bounded.

@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         // blocks before this one have published their contributions to its
         // chunks). An ordered contribution is published once it has completed:
         // right after the next step's reduction has been issued (waiting for
-        // every bulk group but that newest one), or as soon as the loop idles,
-        // so a step's reduction never waits for the previous one to land.
+        // every bulk group but that newest one; the last one after the loop),
+        // so the loop never blocks on a reduction that is still in flight and
+        // the stage loads it also issues are not held up.
         const bool packed = p.cu_seqlens != nullptr;
         // accumulator map: (d, rows of one head, heads or batch*heads); this unit's rows start at y0
         const int z = packed ? u.h : u.bh;
@@ -282,12 +283,14 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           return (unsigned int)(u.tile - jlo);
         };
         int reduced = 0, pending = -1;  // pending: a step whose ordered contribution awaits publication
-        // Publishes `pending`, whose bulk group has completed (the caller waited).
+        // Publishes `pending`, whose bulk group has completed (the caller waited):
+        // one release fence, then both chunk counters.
         auto publish = [&]() {
           fence_proxy_async_global();
+          fence_acq_rel_gpu();
           const int i0 = step_i0(pending);
           const unsigned int pos = chain_pos(i0);
-          for (int c = 0; c < 2; ++c) st_release_gpu(p.dq_flags + fl0 + (i0 + 32 * c) / 32, pos + 1);
+          for (int c = 0; c < 2; ++c) st_relaxed_gpu(p.dq_flags + fl0 + (i0 + 32 * c) / 32, pos + 1);
           pending = -1;
         };
         unsigned long long t_idle = 0;
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
             const unsigned int f0 = ld_relaxed_gpu(p.dq_flags + fl0 + i0 / 32);
             const unsigned int f1 = ld_relaxed_gpu(p.dq_flags + fl0 + i0 / 32 + 1);
             if (f0 >= pos && f1 >= pos) {
-              fence_acquire_gpu();
+              fence_acq_rel_gpu();
               fence_proxy_async_global();
               const uint32_t img = sb + C::oImg + 2 * (reduced & 1) * C::kPTile;
               for (int c = 0; c < 2; ++c) tma_reduce_add_3d(&tmDQ, img + c * C::kPTile, 0, y0 + i0 + 32 * c, z);
@@ -323,11 +326,6 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
               ++reduced;
               progress = true;
             }
-          }
-          if (!progress && pending >= 0) {
-            bulk_wait_all();
-            publish();
-            progress = true;
           }
           if (progress) {
             idle = 0;
