@@ -84,6 +84,30 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same two probes with acquire at cluster scope, for barriers that other
+// CTAs of the cluster arrive on (their earlier writes become visible here).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Blocking waits let the hardware suspend the waiting warp (kPoll = false);
 // polling waits spin on test_wait (kPoll = true), which wakes sooner at the
 // cost of issue slots. Measured on the causal d=128 backward: polling in the
@@ -97,10 +121,14 @@ constexpr bool kConsumerPoll = false;
 
 // Returns false (after setting the timeout status bit and *abort) when the
 // wall-clock limit passes or another role of the CTA has already aborted.
-template <bool kPoll = false>
+// kCluster: acquire at cluster scope (barriers with arrivals from other CTAs).
+template <bool kPoll = false, bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status) {
-  auto probe = [&]() { return kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity); };
+  auto probe = [&]() {
+    if constexpr (kCluster) return kPoll ? mbar_test_wait_cl(bar, parity) : mbar_try_wait_cl(bar, parity);
+    return kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+  };
   if (probe()) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
@@ -120,10 +148,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // the wait together and converged (for the warp-wide issue forms below). Having
 // lane 0 wait alone while the other lanes park at a shuffle measured twice as
 // slow on the MMA-issuing warps.
-template <bool kPoll = false>
+template <bool kPoll = false, bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status) {
-  const bool ok = mbar_wait<kPoll>(bar, parity, abort_flag, status);
+  const bool ok = mbar_wait<kPoll, kCluster>(bar, parity, abort_flag, status);
   return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 
@@ -208,7 +236,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 // A plain (relaxed) GPU-scope read for polling: it does not hold back this
-// thread's later memory operations; acquire with fence_acquire_gpu once the
+// thread's later memory operations; acquire with fence_acq_rel_gpu once the
 // value is the one waited for.
 __device__ __forceinline__ unsigned int ld_relaxed_gpu(const unsigned int* ptr) {
   unsigned int v;
@@ -320,6 +348,77 @@ __device__ __forceinline__ void tc_commit_w(uint32_t bar) {
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+// ------------------------- CTA pairs (cta_group::2) -------------------------
+// Two CTAs of a cluster work as one pair: the leader (rank 0) issues MMAs with
+// M = 256 whose A operand is split by rows between the two CTAs (each supplies
+// its own 128 rows, from its shared memory or its TMEM, at the same address)
+// and whose B operand is split along N (each CTA holds N/2 columns at the same
+// address); D lands in each CTA's TMEM (its 128 rows, all N columns). TMEM is
+// allocated and freed by one warp of each CTA together; every tcgen05 op of a
+// pair kernel uses cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// One arrival worth `count` on an mbarrier of another CTA of the cluster
+// (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote_cnt(uint32_t cluster_addr, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Every thread of both CTAs (release, then acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_mma_ss_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at this shared-memory offset in both CTAs of the
+// pair when every tcgen05 op this thread issued so far is done.
+__device__ __forceinline__ void tc_commit_pair_w(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
+      "h"((uint16_t)3)
       : "memory");
 }
 

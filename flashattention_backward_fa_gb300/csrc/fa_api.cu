@@ -18,8 +18,9 @@ cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st);
 cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st);
-cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
+cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, bool pair, const CUtensorMap* maps,
                                cudaStream_t st);
+bool dkdv_pair_supported(const AttnParams& p, bool atomic);
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st);
 }  // namespace fa
@@ -257,6 +258,10 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The key/value-major kernel runs as CTA pairs (cta_group::2) wherever that
+// form applies (d = 128, deterministic dQ, no bias tensor, fixed length).
+constexpr bool kDkdvPairs = true;
+
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -266,7 +271,7 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
   const bool bf16 = dtype == FA_BF16;
   const bool accum = dq_algo(dtype, deterministic) != DqAlgo::kRecompute;
   if (stage == FA_BWD_DKDV) {
-    CUtensorMap maps[6];
+    CUtensorMap maps[8];
     if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
         !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
       return FA_ERR_CUDA;
@@ -274,7 +279,12 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
     if (!p.bias) maps[4] = maps[0];  // unused
     if (accum ? !make_dq_accum_map(&maps[5], p) : false) return FA_ERR_CUDA;
     if (!accum) maps[5] = maps[0];  // unused
-    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, maps, st));
+    // the CTA-pair form of the deterministic kernel also reads Q and dO in 32-row boxes
+    const bool pair = kDkdvPairs && fa::dkdv_pair_supported(p, accum);
+    if (pair ? (!make_map(&maps[6], p.q, p, bf16, 32) || !make_map(&maps[7], p.dout, p, bf16, 32)) : false)
+      return FA_ERR_CUDA;
+    if (!pair) maps[6] = maps[7] = maps[0];  // unused
+    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, pair, maps, st));
   }
   if (accum) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
   CUtensorMap maps[5];

@@ -114,11 +114,14 @@ struct KVCfg {
   static constexpr int bStageFree = bStaged + 2;               // [2]: staging read by the TMA unit
   static constexpr int bAcc = bStageFree + 2;
   static constexpr int bDrain = bAcc + 1;                      // one per MMA-issuing warp
-  static constexpr int kBars = bDrain + 3;
+  // CTA pairs: the peer's K/V tiles and Q/dO stages landed (leader's barriers)
+  static constexpr int bPeerKV = bDrain + 3;
+  static constexpr int bPeerQFull = bPeerKV + 1;
+  static constexpr int kBars = bPeerQFull + kNS;
   static constexpr uint32_t oTmemSlot = oBar + kBars * 8;
   static constexpr uint32_t oAbort = oTmemSlot + 8;
-  static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][warp] split votes
-  static constexpr uint32_t kSmem = oFlags + 64 + 1024;        // + slack for 1024-byte alignment
+  static constexpr uint32_t oFlags = oAbort + 8;               // [buffer][CTA of the pair][warp] split votes
+  static constexpr uint32_t kSmem = oFlags + 128 + 1024;       // + slack for 1024-byte alignment
   static_assert(kNS >= 2, "shared memory budget leaves fewer than two Q/dO stages");
   static_assert(kBias || kNS >= (kAtomic && D == 128 ? 3 : 4), "Q/dO pipeline shallower than designed");
   static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
@@ -134,12 +137,17 @@ __device__ __forceinline__ void store_tile_row_chunk(uint32_t row_addr, int row,
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias>
+// kPair: the CTA pair form (a cluster of two CTAs on two adjacent key blocks
+// of one head; see the comment at launch_dkdv_t). tmQ32 / tmDO32 are the
+// 32-row maps of the pair's split Sᵀ / dPᵀ operands (unused otherwise).
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias, bool kPair>
 __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ CUtensorMap tmBias,
-                    const __grid_constant__ CUtensorMap tmDQ) {
+                    const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmQ32,
+                    const __grid_constant__ CUtensorMap tmDO32) {
+  static_assert(!kPair || (D == 128 && !kAtomic && !kBias), "CTA pairs: d = 128, deterministic, no bias tensor");
   using C = KVCfg<D, kAtomic, kBias>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -170,18 +178,56 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
     idx = *slot;
     if (idx < 0) return;
   }
+  // CTA pairs: a unit is two adjacent key blocks (cluster rank r takes the
+  // second-level block 2 * tile + r); both CTAs run the union of the two
+  // blocks' query steps, which the leader's MMAs need from both.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  constexpr int kUnitRows = (kPair ? 2 : 1) * kRowsKV;
   Unit u;
-  if (!unit_decode(p, idx, kRowsKV, false, u, ordered ? (1 << 30) : kUnitGroup)) return;
+  if (!unit_decode(p, kPair ? (int)(blockIdx.x >> 1) : idx, kUnitRows, false, u, ordered ? (1 << 30) : kUnitGroup))
+    return;
   const int bh = u.bh, b = u.b, h = u.h;
   const int Nl = u.n;                    // rows of this (batch, head) or sequence
-  const int j0 = u.tile * kRowsKV;
-  const int i_first = p.causal ? j0 : 0;
+  const int ju = u.tile * kUnitRows;     // first key of the unit
+  const int j0 = ju + (int)rank * kRowsKV;  // first key of this CTA
+  const int i_first = p.causal ? ju : 0;
   int i_last = Nl - 1;
-  if (p.window > 0) i_last = min(i_last, j0 + kRowsKV - 2 + p.window);
+  if (p.window > 0) i_last = min(i_last, ju + kUnitRows - 2 + p.window);
   const int nsteps = (i_last >= i_first) ? (i_last - i_first) / kStepQ + 1 : 0;
   // First query row of step `it`: ascending from the diagonal in the
   // deterministic kernel, descending from the last step when dQ is accumulated.
   auto step_i0 = [&](int it) { return i_first + (kAtomic ? nsteps - 1 - it : it) * kStepQ; };
+
+  // MMA and commit forms: cta_group::2 (leader of a pair, M = 256; commits
+  // arrive on the barrier in both CTAs) or cta_group::1.
+  auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t bd, uint32_t id, uint32_t acc) {
+    if constexpr (kPair) tc_mma_ss_pair_w(d, a, bd, id, acc); else tc_mma_ss_w(d, a, bd, id, acc);
+  };
+  auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t bd, uint32_t id, uint32_t acc) {
+    if constexpr (kPair) tc_mma_ts_pair_w(d, a, bd, id, acc); else tc_mma_ts_w(d, a, bd, id, acc);
+  };
+  auto commit = [&](uint32_t br) {
+    if constexpr (kPair) tc_commit_pair_w(br); else tc_commit_w(br);
+  };
+  constexpr int kM = kPair ? 256 : 128;
+  // B panels of the S^T / dP^T operands: 64 query rows, or 32 in a pair
+  constexpr uint32_t kSPanel = kPair ? 4096u : C::kQPanel;
+  // B operands of dV / dK: the whole stage tile, or (pair) this CTA's d half after the two 32-row panels
+  constexpr uint32_t kGOff = kPair ? C::kQPanel : 0u;
+  // an arrival of this warp on a barrier the leader's MMA issuers wait on
+  auto arrive_leader = [&](uint32_t br) {
+    if constexpr (kPair) {
+      if (leader) {
+        warp_arrive(br);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_cnt(mapa_shared(br, 0), 32);
+      }
+    } else {
+      warp_arrive(br);
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bKV), 1);
@@ -194,30 +240,39 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
       mbar_init(bar(C::bDPFull + x), 1);                       // dP^T landed
       mbar_init(bar(C::bSEmpty + x), 1);                       // dV done with the P~T image
       mbar_init(bar(C::bDPEmpty + x), kAtomic ? 256 : 1);     // dK done / dQ^T drained
-      mbar_init(bar(C::bPFull + x), 256);                      // P~T image of two warpgroups
-      mbar_init(bar(C::bDSFull + x), 256);                     // dS^T image of two warpgroups
+      mbar_init(bar(C::bPFull + x), kPair ? 512 : 256);        // P~T image of two warpgroups (of both CTAs)
+      mbar_init(bar(C::bDSFull + x), kPair ? 512 : 256);       // dS^T image of two warpgroups (of both CTAs)
       mbar_init(bar(C::bDQFull + x), 1);
       mbar_init(bar(C::bStaged + x), 2 * D);                   // the warps holding dQ^T rows (d of them per warpgroup)
       mbar_init(bar(C::bStageFree + x), 1);                    // the reducer
     }
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bAcc), 1);
+    mbar_init(bar(C::bPeerKV), 1);
+    for (int x = 0; x < C::kNS; ++x) mbar_init(bar(C::bPeerQFull + x), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + C::oTmemSlot, 512);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(sb + C::oTmemSlot, 512);  // one warp of each CTA, together
+    } else {
+      tmem_alloc(sb + C::oTmemSlot, 512);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmQ);
+    prefetch_tmap(kPair ? &tmQ32 : &tmQ);
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    prefetch_tmap(&tmDO);
+    prefetch_tmap(kPair ? &tmDO32 : &tmDO);
     if constexpr (kAtomic) prefetch_tmap(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
+  // pair: both CTAs' barriers are initialised (and TMEM allocated) before either
+  // signals the other
+  if constexpr (kPair) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::oTmemSlot);
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
@@ -235,11 +290,26 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         const int s = it % C::kNS;
         const int i0 = step_i0(it);
         mbar_arrive_expect_tx(bar(C::bQFull + s), C::kStageBytes);
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn,
+        if constexpr (kPair) {
+          // S^T / dP^T operands: this CTA's 32 queries x all of d (two 32-row
+          // panels); dK / dV operands: all 64 queries x this CTA's half of d.
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_4d(sb + C::oQ + s * C::kQTile + pn * 4096, &tmQ32, bar(C::bQFull + s), 64 * pn,
+                        u.row0 + i0 + 32 * (int)rank, h, b);
+            tma_load_4d(sb + C::oDO + s * C::kQTile + pn * 4096, &tmDO32, bar(C::bQFull + s), 64 * pn,
+                        u.row0 + i0 + 32 * (int)rank, h, b);
+          }
+          tma_load_4d(sb + C::oQ + s * C::kQTile + C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * (int)rank,
                       u.row0 + i0, h, b);
-          tma_load_4d(sb + C::oDO + s * C::kQTile + pn * C::kQPanel, &tmDO, bar(C::bQFull + s), 64 * pn,
+          tma_load_4d(sb + C::oDO + s * C::kQTile + C::kQPanel, &tmDO, bar(C::bQFull + s), 64 * (int)rank,
                       u.row0 + i0, h, b);
+        } else {
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_4d(sb + C::oQ + s * C::kQTile + pn * C::kQPanel, &tmQ, bar(C::bQFull + s), 64 * pn,
+                        u.row0 + i0, h, b);
+            tma_load_4d(sb + C::oDO + s * C::kQTile + pn * C::kQPanel, &tmDO, bar(C::bQFull + s), 64 * pn,
+                        u.row0 + i0, h, b);
+          }
         }
         if constexpr (kBias)  // 64 query rows x 128 keys of the bias (rows / keys past N read as 0)
           tma_load_4d(sb + C::oB + s * C::kBiasTile, &tmBias, bar(C::bQFull + s), u.row0 + j0, u.row0 + i0,
@@ -354,15 +424,34 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           mbar_wait_drain(bar(C::bQFull + it % C::kNS), (it / C::kNS) & 1, p.status);
       }
     }
+  } else if (kPair && !leader && warp == 1) {
+    // ------------------------ pair: peer's load forwarder -----------------------
+    // The leader's MMAs read this CTA's K/V tiles and Q/dO stages: pass each
+    // completion on to the leader's barriers.
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(C::bKV), 0, abort_flag, p.status);
+      if (ok) mbar_arrive_remote_cnt(mapa_shared(bar(C::bPeerKV), 0), 1);
+      for (int it = 0; ok && it < nsteps; ++it) {
+        const int s = it % C::kNS;
+        if (!mbar_wait(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status)) break;
+        mbar_arrive_remote_cnt(mapa_shared(bar(C::bPeerQFull + s), 0), 1);
+      }
+    }
+    __syncwarp();
+  } else if (kPair && !leader && (warp == 2 || warp == 3)) {
+    // pair: the leader issues every MMA
   } else if (warp == 1) {
     // ------------------------------ S^T MMA issuer -----------------------------
     {
-      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
+      constexpr uint32_t idS = make_idesc(kM, kStepQ, kBf16, false, false);
       const uint64_t dK0 = make_sdesc(sb + C::oK, 16, 1024), dQ0 = make_sdesc(sb + C::oQ, 16, 1024);
-      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status) &&
+                (!kPair || warp_wait<kIssuerPoll, true>(bar(C::bPeerKV), 0, abort_flag, p.status));
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
         if (!warp_wait<kIssuerPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            (kPair &&
+             !warp_wait<kIssuerPoll, true>(bar(C::bPeerQFull + s), (it / C::kNS) & 1, abort_flag, p.status)) ||
             !warp_wait<kIssuerPoll>(bar(C::bSEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
@@ -371,24 +460,27 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         const uint64_t q = desc_add(dQ0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss_w(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
-                      desc_add(q, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit_w(bar(C::bSFull + bb));
+          mma_ss(tS + 64 * bb, desc_add(dK0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                 desc_add(q, (k >> 2) * kSPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        commit(bar(C::bSFull + bb));
       }
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
-      tc_commit_w(bar(C::bDrain));
+      commit(bar(C::bDrain));
       if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
       __syncwarp();
     }
   } else if (warp == 3) {
     // ----------------------------- dP^T MMA issuer -----------------------------
     {
-      constexpr uint32_t idS = make_idesc(128, kStepQ, kBf16, false, false);
+      constexpr uint32_t idS = make_idesc(kM, kStepQ, kBf16, false, false);
       const uint64_t dV0 = make_sdesc(sb + C::oV, 16, 1024), dO0 = make_sdesc(sb + C::oDO, 16, 1024);
-      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status);
+      bool ok = warp_wait<kIssuerPoll>(bar(C::bKV), 0, abort_flag, p.status) &&
+                (!kPair || warp_wait<kIssuerPoll, true>(bar(C::bPeerKV), 0, abort_flag, p.status));
       for (int it = 0; ok && it < nsteps; ++it) {
         const int s = it % C::kNS, bb = it & 1;
         if (!warp_wait<kIssuerPoll>(bar(C::bQFull + s), (it / C::kNS) & 1, abort_flag, p.status) ||
+            (kPair &&
+             !warp_wait<kIssuerPoll, true>(bar(C::bPeerQFull + s), (it / C::kNS) & 1, abort_flag, p.status)) ||
             !warp_wait<kIssuerPoll>(bar(C::bDPEmpty + bb), ((it >> 1) & 1) ^ 1, abort_flag, p.status)) {
           ok = false;
           break;
@@ -397,48 +489,49 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         const uint64_t g = desc_add(dO0, s * C::kQTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc_mma_ss_w(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
-                      desc_add(g, (k >> 2) * C::kQPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
-        tc_commit_w(bar(C::bDPFull + bb));
+          mma_ss(tdP + 64 * bb, desc_add(dV0, (k >> 2) * C::kKVPanel + (k & 3) * 32),
+                 desc_add(g, (k >> 2) * kSPanel + (k & 3) * 32), idS, k > 0 ? 1u : 0u);
+        commit(bar(C::bDPFull + bb));
       }
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
-      tc_commit_w(bar(C::bDrain + 2));
+      commit(bar(C::bDrain + 2));
       if (lane == 0) mbar_wait_drain(bar(C::bDrain + 2), 0, p.status);
       __syncwarp();
     }
   } else if (warp == 2) {
     // ----------------------- dV / dK (/ dQ^T) MMA issuer ----------------------
     {
-      constexpr uint32_t idG = make_idesc(128, D, kBf16, false, true);         // dV, dK
+      constexpr uint32_t idG = make_idesc(kM, D, kBf16, false, true);          // dV, dK
       constexpr uint32_t idQ = make_idesc(128, kStepQ, kBf16, true, true);     // dQ^T
-      const uint64_t mQ0 = make_sdesc(sb + C::oQ, C::kQPanel, 1024), mO0 = make_sdesc(sb + C::oDO, C::kQPanel, 1024);
+      const uint64_t mQ0 = make_sdesc(sb + C::oQ + kGOff, C::kQPanel, 1024),
+                     mO0 = make_sdesc(sb + C::oDO + kGOff, C::kQPanel, 1024);
       const uint64_t mK0 = make_sdesc(sb + C::oK, C::kKVPanel, 1024);
       bool ok = true;
       for (int t = 0; ok && t < nsteps; ++t) {
         const int bt = t & 1, st = t % C::kNS;
-        if (!warp_wait<kConsumerPoll>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kConsumerPoll, kPair>(bar(C::bPFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         bool split = false;
 #pragma unroll
-        for (int x = 0; x < 8; ++x) split |= flags[8 * bt + x] != 0;
+        for (int x = 0; x < (kPair ? 16 : 8); ++x) split |= flags[16 * bt + x] != 0;
         const uint32_t first = t > 0 ? 1u : 0u;
         const uint64_t q = desc_add(mQ0, st * C::kQTile), g = desc_add(mO0, st * C::kQTile);
         // dV += P~T dO: K step k reads the 8 rounded columns at 16k of the P~T image
         // and, on split tiles, the 8 residual columns at 16k + 8.
 #pragma unroll
         for (int k = 0; k < kStepQ / 16; ++k)
-          tc_mma_ts_w(tdV, tS + 64 * bt + 16 * k, desc_add(g, 2048 * k), idG, k > 0 ? 1u : first);
+          mma_ts(tdV, tS + 64 * bt + 16 * k, desc_add(g, 2048 * k), idG, k > 0 ? 1u : first);
         if (split) {
 #pragma unroll
           for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ts_w(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
+            mma_ts(tdV, tS + 64 * bt + 16 * k + 8, desc_add(g, 2048 * k), idG, 1u);
         }
-        tc_commit_w(bar(C::bSEmpty + bt));
+        commit(bar(C::bSEmpty + bt));
         // dK (and dQ^T) once the dS^T image is in place; dV above only needed P~T.
-        if (!warp_wait<kConsumerPoll>(bar(C::bDSFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait<kConsumerPoll, kPair>(bar(C::bDSFull + bt), (t >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -447,13 +540,13 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           // dK += dS^T Q from the dS^T image over the dP^T columns.
 #pragma unroll
           for (int k = 0; k < kStepQ / 16; ++k)
-            tc_mma_ts_w(tdK, tdP + 64 * bt + 16 * k, desc_add(q, 2048 * k), idG, k > 0 ? 1u : first);
+            mma_ts(tdK, tdP + 64 * bt + 16 * k, desc_add(q, 2048 * k), idG, k > 0 ? 1u : first);
           if (split) {
 #pragma unroll
             for (int k = 0; k < kStepQ / 16; ++k)
-              tc_mma_ts_w(tdK, tdP + 64 * bt + 16 * k + 8, desc_add(q, 2048 * k), idG, 1u);
+              mma_ts(tdK, tdP + 64 * bt + 16 * k + 8, desc_add(q, 2048 * k), idG, 1u);
           }
-          tc_commit_w(bar(C::bDPEmpty + bt));
+          commit(bar(C::bDPEmpty + bt));
         } else {
           // dK += dS^T Q and dQ^T = K^T dS^T from the shared dS^T tiles; dQ^T lands in
           // this buffer's dP^T columns, which the row math has consumed. For d = 64
@@ -474,11 +567,11 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           }
           tc_commit_w(bar(C::bDQFull + bt));
         }
-        tc_commit_w(bar(C::bQEmpty + st));
+        commit(bar(C::bQEmpty + st));
       }
-      tc_commit_w(bar(C::bAcc));
+      commit(bar(C::bAcc));
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
-      tc_commit_w(bar(C::bDrain + 1));
+      commit(bar(C::bDrain + 1));
       if (lane == 0) mbar_wait_drain(bar(C::bDrain + 1), 0, p.status);
       __syncwarp();
     }
@@ -594,9 +687,20 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         tmem_st8<0>(tSc + 16 * hh + 8, ep);
       }
       tmem_st_wait();
-      if (lane == 0) flags[8 * bb + 4 * c + wq] = (split_h[0] || split_h[1]) ? 1 : 0;
+      {
+        // split vote of this warp for the MMA issuer (pair: into the leader's
+        // votes, second half for the peer)
+        const int vote = (split_h[0] || split_h[1]) ? 1 : 0;
+        const int vi = 16 * bb + 8 * (int)rank + 4 * c + wq;
+        if (lane == 0) {
+          if (leader)
+            flags[vi] = vote;
+          else
+            st_shared_cluster_u32(mapa_shared(sb + C::oFlags + 4u * vi, 0), (uint32_t)vote);
+        }
+      }
       tc_fence_before();
-      warp_arrive(bar(C::bPFull + bb));
+      arrive_leader(bar(C::bPFull + bb));
       // ---- phase 2: dS^T = P o (dP^T (o Z/(1-p)) + (-D)) ----
       // In ordered mode the image of this buffer held the dQ^T staging of step
       // it - 2 until the reducer's TMA read it (a fresh barrier passes the
@@ -660,7 +764,7 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
       if constexpr (!kAtomic) tmem_st_wait();
       tc_fence_before();
       if constexpr (kAtomic) fence_proxy_async_smem();
-      warp_arrive(bar(C::bDSFull + bb));
+      arrive_leader(bar(C::bDSFull + bb));
       if constexpr (kAtomic) {
         // dQ^T (d on lanes, this warpgroup's 32 queries on columns) -> the staging
         // tile [32 queries][d] fp32 over this warpgroup's half of the image; the
@@ -726,57 +830,108 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // pair: the leader's MMAs (drained above) read the peer's shared memory and
+  // write its TMEM, so neither CTA frees anything before both get here
+  if constexpr (kPair) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
-template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias>
+// One CTA per (unit, key block), or, with kPair, one cluster of two CTAs per
+// (unit, pair of adjacent key blocks): the leader issues every MMA with M = 256
+// (both CTAs' keys); each CTA holds half of each B operand (32 of the step's 64
+// queries for S^T and dP^T, half of d for dV and dK), so a CTA's shared-memory
+// operand reads per step fall from 128 KB to 96 KB. A key block past N in the
+// last pair of an odd tile count takes part with out-of-range keys, which the
+// row math masks and the epilogue does not store.
+template <int D, bool kBf16, bool kAtomic, bool kDrop, bool kAlibi, bool kBias, bool kPair>
 static cudaError_t launch_dkdv_t(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
   using C = KVCfg<D, kAtomic, kBias>;
-  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop, kAlibi, kBias>;
+  auto kern = bwd_dkdv_kernel<D, kBf16, kAtomic, kDrop, kAlibi, kBias, kPair>;
   const int smem = (int)(C::kSmem > kMinSmemOneCtaPerSm ? C::kSmem : kMinSmemOneCtaPerSm);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int rows = p.cu_seqlens ? p.max_seqlen : p.N;
-  const int tiles = (rows + kRowsKV - 1) / kRowsKV;
-  const unsigned grid = (unsigned)(tiles * (p.cu_seqlens ? p.nseq * p.H : p.B * p.H));
-  kern<<<grid, C::kThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
-  return cudaGetLastError();
+  const int units = p.cu_seqlens ? p.nseq * p.H : p.B * p.H;
+  if constexpr (!kPair) {
+    const int tiles = (rows + kRowsKV - 1) / kRowsKV;
+    const unsigned grid = (unsigned)(tiles * units);
+    kern<<<grid, C::kThreads, smem, st>>>(p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+                                          maps[7]);
+    return cudaGetLastError();
+  } else {
+    const int pairs = (rows + 2 * kRowsKV - 1) / (2 * kRowsKV);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs * units));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7]);
+  }
 }
 
 template <int D, bool kBf16, bool kAtomic, bool kBias>
-static cudaError_t launch_dkdv_b(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
+static cudaError_t launch_dkdv_b(const AttnParams& p, bool pair, const CUtensorMap* maps, cudaStream_t st) {
   const bool drop = p.drop.on != 0;
+  if constexpr (D == 128 && !kAtomic && !kBias) {
+    if (pair) {
+      if (p.alibi)
+        return drop ? launch_dkdv_t<D, kBf16, false, true, true, false, true>(p, maps, st)
+                    : launch_dkdv_t<D, kBf16, false, false, true, false, true>(p, maps, st);
+      return drop ? launch_dkdv_t<D, kBf16, false, true, false, false, true>(p, maps, st)
+                  : launch_dkdv_t<D, kBf16, false, false, false, false, true>(p, maps, st);
+    }
+  }
   if (p.alibi)
-    return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true, kBias>(p, maps, st)
-                : launch_dkdv_t<D, kBf16, kAtomic, false, true, kBias>(p, maps, st);
-  return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, false, kBias>(p, maps, st)
-              : launch_dkdv_t<D, kBf16, kAtomic, false, false, kBias>(p, maps, st);
+    return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, true, kBias, false>(p, maps, st)
+                : launch_dkdv_t<D, kBf16, kAtomic, false, true, kBias, false>(p, maps, st);
+  return drop ? launch_dkdv_t<D, kBf16, kAtomic, true, false, kBias, false>(p, maps, st)
+              : launch_dkdv_t<D, kBf16, kAtomic, false, false, kBias, false>(p, maps, st);
 }
 
 template <int D, bool kBf16, bool kAtomic>
-static cudaError_t launch_dkdv_a(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  return p.bias ? launch_dkdv_b<D, kBf16, kAtomic, true>(p, maps, st)
-                : launch_dkdv_b<D, kBf16, kAtomic, false>(p, maps, st);
+static cudaError_t launch_dkdv_a(const AttnParams& p, bool pair, const CUtensorMap* maps, cudaStream_t st) {
+  return p.bias ? launch_dkdv_b<D, kBf16, kAtomic, true>(p, pair, maps, st)
+                : launch_dkdv_b<D, kBf16, kAtomic, false>(p, pair, maps, st);
 }
 
 template <int D, bool kBf16>
-static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, const CUtensorMap* maps, cudaStream_t st) {
-  return atomic ? launch_dkdv_a<D, kBf16, true>(p, maps, st) : launch_dkdv_a<D, kBf16, false>(p, maps, st);
+static cudaError_t launch_dkdv_d(const AttnParams& p, bool atomic, bool pair, const CUtensorMap* maps,
+                                 cudaStream_t st) {
+  return atomic ? launch_dkdv_a<D, kBf16, true>(p, pair, maps, st) : launch_dkdv_a<D, kBf16, false>(p, pair, maps, st);
+}
+
+// Whether the CTA-pair form applies: d = 128, deterministic, no bias tensor, fixed length.
+bool dkdv_pair_supported(const AttnParams& p, bool atomic) {
+  return p.d == 128 && !atomic && p.bias == nullptr && p.cu_seqlens == nullptr;
 }
 
 // maps: Q, K, V, dO (Q/dO boxes of kStepQ rows, K/V boxes of kRowsKV rows), the
 // attention bias (boxes of kStepQ rows x kRowsKV keys; any valid map when
-// p.bias is null), and the fp32 dQ accumulator as (d, rows per head, heads)
-// with boxes of d x 32 rows (any valid map in the deterministic kernel).
-cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
+// p.bias is null), the fp32 dQ accumulator as (d, rows per head, heads) with
+// boxes of d x 32 rows (any valid map in the deterministic kernel), and Q, dO
+// with boxes of 32 rows (the pair form's S^T / dP^T operands; any valid map
+// otherwise). `pair` asks for the CTA-pair form where dkdv_pair_supported.
+cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, bool pair, const CUtensorMap* maps,
                                cudaStream_t st) {
+  pair = pair && dkdv_pair_supported(p, atomic);
   if (p.d == 128)
-    return bf16 ? launch_dkdv_d<128, true>(p, atomic, maps, st) : launch_dkdv_d<128, false>(p, atomic, maps, st);
-  return bf16 ? launch_dkdv_d<64, true>(p, atomic, maps, st) : launch_dkdv_d<64, false>(p, atomic, maps, st);
+    return bf16 ? launch_dkdv_d<128, true>(p, atomic, pair, maps, st)
+                : launch_dkdv_d<128, false>(p, atomic, pair, maps, st);
+  return bf16 ? launch_dkdv_d<64, true>(p, atomic, false, maps, st) : launch_dkdv_d<64, false>(p, atomic, false, maps, st);
 }
 
 }  // namespace fa
