@@ -258,9 +258,9 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The key/value-major kernel runs as CTA pairs (cta_group::2) wherever that
-// form applies (d = 128, deterministic dQ, no bias tensor, fixed length).
-constexpr bool kDkdvPairs = true;
+// Whether the key/value-major kernel runs as CTA pairs (cta_group::2) where
+// that form applies (d = 128, deterministic dQ, no bias tensor, fixed length).
+constexpr bool kDkdvPairs = false;
 
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
