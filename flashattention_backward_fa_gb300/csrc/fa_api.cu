@@ -21,6 +21,8 @@ cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, bool pair, const CUtensorMap* maps,
                                cudaStream_t st);
 bool dkdv_pair_supported(const AttnParams& p, bool atomic);
+bool dq_tmem_supported(const AttnParams& p);
+cudaError_t launch_dq_tmem(const AttnParams& p, bool bf16, const CUtensorMap* maps, cudaStream_t st);
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st);
 }  // namespace fa
@@ -261,6 +263,9 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
 // Whether the key/value-major kernel runs as CTA pairs (cta_group::2) where
 // that form applies (d = 128, deterministic dQ, no bias tensor, fixed length).
 constexpr bool kDkdvPairs = false;
+// Whether the deterministic dQ step uses the kernel with Q and dO resident in
+// TMEM (kernels_dq.cu) where it applies (16-bit, d in {64, 128}, no bias tensor).
+constexpr bool kDqTmem = true;
 
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
@@ -287,6 +292,14 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
     return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, pair, maps, st));
   }
   if (accum) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
+  if (kDqTmem && fa::dq_tmem_supported(p)) {
+    // Q and dO in TMEM (TS MMAs), 64-key steps
+    CUtensorMap m4[4];
+    if (!make_map(&m4[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&m4[1], p.k, p, bf16, 64) ||
+        !make_map(&m4[2], p.v, p, bf16, 64) || !make_map(&m4[3], p.dout, p, bf16, fa::kRowsQ))
+      return FA_ERR_CUDA;
+    return cuda_rc(fa::launch_dq_tmem(p, bf16, m4, st));
+  }
   CUtensorMap maps[5];
   if (!make_map(&maps[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], p.k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], p.v, p, bf16, fa::kStepKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kRowsQ))
