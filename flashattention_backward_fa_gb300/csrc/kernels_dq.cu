@@ -57,9 +57,8 @@ struct DqCfg {
   static constexpr int bQReady = 1;                             // Q, dO copied into TMEM
   static constexpr int bFull = 2;                               // [kNS] K, V of a step landed
   static constexpr int bEmpty = bFull + kNS;                    // [kNS] stage released (after dQ)
-  static constexpr int bSFull = bEmpty + kNS;                   // [2]
-  static constexpr int bDPFull = bSFull + 2;                    // [2]
-  static constexpr int bSEmpty = bDPFull + 2;                   // [2] dQ MMAs done with the image
+  static constexpr int bSFull = bEmpty + kNS;                   // [2] S and dP of a step landed (two commits)
+  static constexpr int bSEmpty = bSFull + 2;                    // [2] dQ MMAs done with the image
   static constexpr int bDPEmpty = bSEmpty + 2;                  // [2] row math has read dP
   static constexpr int bPFull = bDPEmpty + 2;                   // [2] dS image written
   static constexpr int bAcc = bPFull + 2;
@@ -110,8 +109,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(bar(C::bEmpty + s), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(C::bSFull + x), 1);
-      mbar_init(bar(C::bDPFull + x), 1);
+      mbar_init(bar(C::bSFull + x), 2);
       mbar_init(bar(C::bSEmpty + x), 1);
       mbar_init(bar(C::bDPEmpty + x), 256);
       mbar_init(bar(C::bPFull + x), 256);
@@ -175,7 +173,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       constexpr uint32_t idS = make_idesc(128, kDqStepKV, kBf16, false, false);
       const uint32_t tA = isS ? tQ : tDO;
       const uint32_t tD = isS ? tS : tdP;
-      const int bF = isS ? C::bSFull : C::bDPFull, bE = isS ? C::bSEmpty : C::bDPEmpty;
+      const int bE = isS ? C::bSEmpty : C::bDPEmpty;
       const uint64_t b0 = make_sdesc(sb + C::oRing + (isS ? 0u : C::kKVTile), 16, 1024);
       bool ok = warp_wait<kIssuerPoll>(bar(C::bQReady), 0, abort_flag, p.status);
       for (int it = 0; ok && it < nsteps; ++it) {
@@ -191,7 +189,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int k = 0; k < D / 16; ++k)
           tc_mma_ts_w(tD + 64 * bb, tA + 8 * k, desc_add(bd, (k >> 2) * C::kKVPanel + (k & 3) * 32), idS,
                       k > 0 ? 1u : 0u);
-        tc_commit_w(bar(bF + bb));
+        tc_commit_w(bar(C::bSFull + bb));  // S and dP both arrive here
       }
       // Every MMA this warp issued is complete before the CTA frees TMEM and exits.
       const int dr = isS ? 0 : 2;
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     warp_arrive(bar(C::bQReady));
     // -L*log2(e) (-inf for a row with no allowed key) and -D of this row; the
     // negated forms are addends of one FMA / add.
-    const long long ws = u.ws + il;  // il < the padded row count always
+    const long long ws = u.ws + i;  // i < the padded row count always
     const float nL2 = p.ws_nL2[ws];
     const float nD = p.ws_nD[ws];
     const float slope_raw = kAlibi ? alibi_slope_raw(p, u) : 0.f;
@@ -289,16 +287,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(Nl - base, p.causal ? i + 1 - base : 32));
       uint32_t keep = 0xFFFFFFFFu;
       if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, Nl, i, base);
+      // this warpgroup's S and dP columns in one go (no wait between a TMEM load
+      // and its completion wait), then the dP buffer is released
       uint32_t sr2[2][16], dr2[2][16];
       __syncwarp();
       tmem_ld16(tSc, sr2[0]);
       tmem_ld16(tSc + 16, sr2[1]);
-      // all of this warpgroup's dP columns, then the dP buffer is released
-      if (!warp_wait<kRowMathPoll>(bar(C::bDPFull + bb), (it >> 1) & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       tmem_ld16(tdPc, dr2[0]);
       tmem_ld16(tdPc + 16, dr2[1]);
       tmem_ld_wait16x4(sr2[0], sr2[1], dr2[0], dr2[1]);
