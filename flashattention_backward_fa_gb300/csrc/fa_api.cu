@@ -265,7 +265,7 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
 constexpr bool kDkdvPairs = false;
 // Whether the deterministic dQ step uses the kernel with Q and dO resident in
 // TMEM (kernels_dq.cu) where it applies (16-bit, d in {64, 128}, no bias tensor).
-constexpr bool kDqTmem = true;
+constexpr bool kDqTmem = false;
 
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
