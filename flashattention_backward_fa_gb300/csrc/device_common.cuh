@@ -84,30 +84,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// The same two probes with acquire at cluster scope, for barriers that other
-// CTAs of the cluster arrive on (their earlier writes become visible here).
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Blocking waits let the hardware suspend the waiting warp (kPoll = false);
 // polling waits spin on test_wait (kPoll = true), which wakes sooner at the
 // cost of issue slots. Measured on the causal d=128 backward: polling in the
@@ -121,14 +97,10 @@ constexpr bool kConsumerPoll = false;
 
 // Returns false (after setting the timeout status bit and *abort) when the
 // wall-clock limit passes or another role of the CTA has already aborted.
-// kCluster: acquire at cluster scope (barriers with arrivals from other CTAs).
-template <bool kPoll = false, bool kCluster = false>
+template <bool kPoll = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status) {
-  auto probe = [&]() {
-    if constexpr (kCluster) return kPoll ? mbar_test_wait_cl(bar, parity) : mbar_try_wait_cl(bar, parity);
-    return kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
-  };
+  auto probe = [&]() { return kPoll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
@@ -148,10 +120,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // the wait together and converged (for the warp-wide issue forms below). Having
 // lane 0 wait alone while the other lanes park at a shuffle measured twice as
 // slow on the MMA-issuing warps.
-template <bool kPoll = false, bool kCluster = false>
+template <bool kPoll = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status) {
-  const bool ok = mbar_wait<kPoll, kCluster>(bar, parity, abort_flag, status);
+  const bool ok = mbar_wait<kPoll>(bar, parity, abort_flag, status);
   return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 
@@ -352,76 +324,6 @@ __device__ __forceinline__ void tc_commit_w(uint32_t bar) {
 }
 
 // ------------------------- CTA pairs (cta_group::2) -------------------------
-// Two CTAs of a cluster work as one pair: the leader (rank 0) issues MMAs with
-// M = 256 whose A operand is split by rows between the two CTAs (each supplies
-// its own 128 rows, from its shared memory or its TMEM, at the same address)
-// and whose B operand is split along N (each CTA holds N/2 columns at the same
-// address); D lands in each CTA's TMEM (its 128 rows, all N columns). TMEM is
-// allocated and freed by one warp of each CTA together; every tcgen05 op of a
-// pair kernel uses cta_group::2.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// One arrival worth `count` on an mbarrier of another CTA of the cluster
-// (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote_cnt(uint32_t cluster_addr, uint32_t count) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-// Every thread of both CTAs (release, then acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_mma_ss_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the barrier at this shared-memory offset in both CTAs of the
-// pair when every tcgen05 op this thread issued so far is done.
-__device__ __forceinline__ void tc_commit_pair_w(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-          bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-
 // Store 16 consecutive 32-bit columns of this thread's lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -661,6 +563,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // Philox-4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): per round two
 // 32x32->64 multiplies, the output permutation of that paper, and a Weyl key
 // schedule between rounds.
+// 32 x 32 -> 64-bit product as one instruction (low word, high word).
+__device__ __forceinline__ void mul_wide_u32(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b64 t;\n\tmul.wide.u32 t, %2, %3;\n\tmov.b64 {%0, %1}, t;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(a), "r"(b));
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
@@ -668,8 +577,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide_u32(0xD2511F53u, c.x, lo0, hi0);
+    mul_wide_u32(0xCD9E8D57u, c.z, lo1, hi1);
     c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
   }
   return c;
@@ -690,11 +600,13 @@ struct DropoutParams {
 // iff that half >= threshold.
 
 // The eight keep bits of one Philox output (bit 2w + h <-> half h of word w).
+// With T16 = T << 16: the high half of x is >= T iff x >= T16, and the low half
+// iff (x << 16) >= T16 (unsigned), so each decision is one compare.
 __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
-  return (uint32_t)((w.x & 0xFFFFu) >= T) | ((uint32_t)((w.x >> 16) >= T) << 1) |
-         ((uint32_t)((w.y & 0xFFFFu) >= T) << 2) | ((uint32_t)((w.y >> 16) >= T) << 3) |
-         ((uint32_t)((w.z & 0xFFFFu) >= T) << 4) | ((uint32_t)((w.z >> 16) >= T) << 5) |
-         ((uint32_t)((w.w & 0xFFFFu) >= T) << 6) | ((uint32_t)((w.w >> 16) >= T) << 7);
+  const uint32_t T16 = T << 16;
+  return (uint32_t)((w.x << 16) >= T16) | ((uint32_t)(w.x >= T16) << 1) | ((uint32_t)((w.y << 16) >= T16) << 2) |
+         ((uint32_t)(w.y >= T16) << 3) | ((uint32_t)((w.z << 16) >= T16) << 4) | ((uint32_t)(w.z >= T16) << 5) |
+         ((uint32_t)((w.w << 16) >= T16) << 6) | ((uint32_t)(w.w >= T16) << 7);
 }
 
 __device__ __forceinline__ uint4 philox_at(const DropoutParams& dp, uint64_t g) {
@@ -716,7 +628,7 @@ __device__ __forceinline__ bool dropout_keep(const DropoutParams& dp, uint32_t b
 // eight keys (one 8-lane group) for one query, so lane 8g + r evaluates the
 // queries i0 + 8t + r (t < 4) for its group and the eight lanes trade their
 // results through shuffles: 4 calls per lane instead of 32.
-static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
+static __device__ __forceinline__ uint32_t keep_bits_for_key(const DropoutParams dp, uint32_t bh, int N, int i0, int j) {
   const int lane = threadIdx.x & 31, r = lane & 7;
   const uint64_t n8 = (uint64_t)((N + 7) >> 3);
   const uint64_t row0 = (uint64_t)(bh + dp.bh_off) * (uint64_t)N;
@@ -725,12 +637,15 @@ static __device__ __noinline__ uint32_t keep_bits_for_key(const DropoutParams dp
   for (int t = 0; t < 4; ++t)
     mine |= keep_byte(philox_at(dp, (row0 + (uint64_t)(i0 + 8 * t + r)) * n8 + (uint64_t)(j >> 3)), dp.threshold)
             << (8 * t);
+  // From lane 8g + rs, this lane (8g + r) needs bit r of each byte t (the
+  // queries i0 + 8t + rs), placed at bit 8t + rs: one shift brings bit r of
+  // every byte to the byte's bit 0, one mask keeps those four, one shift
+  // moves them to bit rs.
   uint32_t bits = 0;
 #pragma unroll
   for (int rs = 0; rs < 8; ++rs) {
-    const uint32_t v = __shfl_sync(0xffffffffu, mine, (lane & ~7) + rs);  // queries i0 + 8t + rs
-#pragma unroll
-    for (int t = 0; t < 4; ++t) bits |= ((v >> (8 * t + r)) & 1u) << (8 * t + rs);
+    const uint32_t v = __shfl_sync(0xffffffffu, mine, (lane & ~7) + rs);
+    bits |= ((v >> r) & 0x01010101u) << rs;
   }
   return bits;
 }

@@ -13,16 +13,13 @@
 #include "fa_internal.h"
 
 namespace fa {
-cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st);
+cudaError_t launch_preprocess(const AttnParams& p, int dtype, const CUtensorMap* maps, cudaStream_t st);
 cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st);
 cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dq_f32(const AttnParams& p, cudaStream_t st);
-cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, bool pair, const CUtensorMap* maps,
+cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, const CUtensorMap* maps,
                                cudaStream_t st);
-bool dkdv_pair_supported(const AttnParams& p, bool atomic);
-bool dq_tmem_supported(const AttnParams& p);
-cudaError_t launch_dq_tmem(const AttnParams& p, bool bf16, const CUtensorMap* maps, cudaStream_t st);
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st);
 }  // namespace fa
@@ -128,17 +125,19 @@ bool valid_dq_mode(int deterministic) {
 bool needs_dq_accum(int dtype, int deterministic) { return dq_algo(dtype, deterministic) != DqAlgo::kRecompute; }
 
 struct WsLayout {
-  size_t off_L2, off_D, off_dq, off_flags, off_ticket, total;
+  size_t off_L2, off_D, off_ctr, off_dq, off_flags, off_ticket, total;
 };
 
-// [-L*log2e | -D | fp32 dQ accumulator (atomic, ordered) | chunk counters and
-// the unit ticket (ordered)], each part 256-byte aligned.
+// [-L*log2e | -D | the persistent kernels' unit counters | fp32 dQ accumulator
+// (atomic, ordered) | chunk counters and the unit ticket (ordered)], each part
+// 256-byte aligned.
 WsLayout ws_layout(int B, int H, int N, int d, int dtype, int deterministic) {
   const size_t rows = (size_t)B * H * pad_rows(N);
   WsLayout w;
   w.off_L2 = 0;
   w.off_D = round256(rows * 4);
-  w.off_dq = w.off_D + round256(rows * 4);
+  w.off_ctr = w.off_D + round256(rows * 4);
+  w.off_dq = w.off_ctr + 256;
   w.off_flags = w.off_dq + (needs_dq_accum(dtype, deterministic) ? round256(rows * (size_t)d * 4) : 0);
   const bool ordered = dq_algo(dtype, deterministic) == DqAlgo::kOrdered;
   w.off_ticket = w.off_flags + (ordered ? round256(rows / 32 * 4) : 0);
@@ -147,6 +146,17 @@ WsLayout ws_layout(int B, int H, int N, int d, int dtype, int deterministic) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor-map encoding (cuTensorMapEncodeTiled) is a driver call that needs a
+// current context on the calling thread. A thread whose CUDA calls so far bound
+// none (pointer queries, this library's cached lookups) would see it fail, so
+// every entry point makes the current device's primary context current first:
+// cudaSetDevice initialises that context and binds it to the thread.
+int bind_device_context() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
 
 // Every buffer a kernel touches must be memory of the current device (or
 // managed memory): a host or another device's pointer would make the kernels
@@ -260,23 +270,23 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Whether the key/value-major kernel runs as CTA pairs (cta_group::2) where
-// that form applies (d = 128, deterministic dQ, no bias tensor, fixed length).
-constexpr bool kDkdvPairs = false;
-// Whether the deterministic dQ step uses the kernel with Q and dO resident in
-// TMEM (kernels_dq.cu) where it applies (16-bit, d in {64, 128}, no bias tensor).
-constexpr bool kDqTmem = false;
-
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stage == FA_BWD_PREPROCESS) return cuda_rc(fa::launch_preprocess(p, dtype, st));
+  if (stage == FA_BWD_PREPROCESS) {
+    // 16-bit tensors with d in {64, 128}: O and dO stream through shared memory in 64-row TMA boxes
+    CUtensorMap maps[2];
+    if (dtype != FA_F32 && (p.d == 64 || p.d == 128) &&
+        (!make_map(&maps[0], p.o, p, dtype == FA_BF16, 64) || !make_map(&maps[1], p.dout, p, dtype == FA_BF16, 64)))
+      return FA_ERR_CUDA;
+    return cuda_rc(fa::launch_preprocess(p, dtype, maps, st));
+  }
   if (dtype == FA_F32)
     return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
   const bool bf16 = dtype == FA_BF16;
   const bool accum = dq_algo(dtype, deterministic) != DqAlgo::kRecompute;
   if (stage == FA_BWD_DKDV) {
-    CUtensorMap maps[8];
+    CUtensorMap maps[6];
     if (!make_map(&maps[0], p.q, p, bf16, fa::kStepQ) || !make_map(&maps[1], p.k, p, bf16, fa::kRowsKV) ||
         !make_map(&maps[2], p.v, p, bf16, fa::kRowsKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kStepQ))
       return FA_ERR_CUDA;
@@ -284,22 +294,9 @@ int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int dete
     if (!p.bias) maps[4] = maps[0];  // unused
     if (accum ? !make_dq_accum_map(&maps[5], p) : false) return FA_ERR_CUDA;
     if (!accum) maps[5] = maps[0];  // unused
-    // the CTA-pair form of the deterministic kernel also reads Q and dO in 32-row boxes
-    const bool pair = kDkdvPairs && fa::dkdv_pair_supported(p, accum);
-    if (pair ? (!make_map(&maps[6], p.q, p, bf16, 32) || !make_map(&maps[7], p.dout, p, bf16, 32)) : false)
-      return FA_ERR_CUDA;
-    if (!pair) maps[6] = maps[7] = maps[0];  // unused
-    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, pair, maps, st));
+    return cuda_rc(fa::launch_bwd_dkdv_tc(p, bf16, accum, maps, st));
   }
   if (accum) return cuda_rc(fa::launch_dq_convert(p, dtype, st));
-  if (kDqTmem && fa::dq_tmem_supported(p)) {
-    // Q and dO in TMEM (TS MMAs), 64-key steps
-    CUtensorMap m4[4];
-    if (!make_map(&m4[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&m4[1], p.k, p, bf16, 64) ||
-        !make_map(&m4[2], p.v, p, bf16, 64) || !make_map(&m4[3], p.dout, p, bf16, fa::kRowsQ))
-      return FA_ERR_CUDA;
-    return cuda_rc(fa::launch_dq_tmem(p, bf16, m4, st));
-  }
   CUtensorMap maps[5];
   if (!make_map(&maps[0], p.q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], p.k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], p.v, p, bf16, fa::kStepKV) || !make_map(&maps[3], p.dout, p, bf16, fa::kRowsQ))
@@ -459,6 +456,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
     return FA_ERR_WORKSPACE;
   if (check_ptrs && (rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, ex.alibi, ex.bias})))
     return rc;
+  if ((rc = bind_device_context())) return rc;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
   apply_extras(p, ex);
@@ -475,6 +473,7 @@ int bwd_stage_run(fa_bwd_stage_id stage, const void* q, const void* k, const voi
   p.ws_nL2 = reinterpret_cast<float*>(ws + w.off_L2);
   p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
   p.ws_dq = needs_dq_accum(dtype, deterministic) ? reinterpret_cast<float*>(ws + w.off_dq) : nullptr;
+  p.unit_ctr = reinterpret_cast<unsigned int*>(ws + w.off_ctr);
   if (dq_algo(dtype, deterministic) == DqAlgo::kOrdered) {
     p.dq_flags = reinterpret_cast<unsigned int*>(ws + w.off_flags);
     p.dq_ticket = reinterpret_cast<unsigned int*>(ws + w.off_ticket);
@@ -493,6 +492,7 @@ int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
   if ((rc = check_device_ptrs({q, k, v, o, lse, ex.alibi, ex.bias}))) return rc;
+  if ((rc = bind_device_context())) return rc;
   AttnParams p;
   fill_params(p, B, H, N, d, strides, scale, causal, window, dropout_p, seed, offset);
   apply_extras(p, ex);
@@ -642,7 +642,7 @@ namespace {
 
 struct VarlenWs {
   int seq_pad, acc_rows;
-  size_t off_L2, off_D, off_dq, off_flags, off_ticket, total;
+  size_t off_L2, off_D, off_ctr, off_dq, off_flags, off_ticket, total;
 };
 
 VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int deterministic) {
@@ -652,7 +652,8 @@ VarlenWs varlen_ws_layout(int nseq, int max_seqlen, int total, int H, int d, int
   const size_t vec = (size_t)H * nseq * w.seq_pad * 4;
   w.off_L2 = 0;
   w.off_D = round256(vec);
-  w.off_dq = w.off_D + round256(vec);
+  w.off_ctr = w.off_D + round256(vec);
+  w.off_dq = w.off_ctr + 256;
   const DqAlgo a = dq_algo(FA_BF16, deterministic);
   w.off_flags = w.off_dq + (a != DqAlgo::kRecompute ? round256((size_t)H * w.acc_rows * d * 4) : 0);
   w.off_ticket = w.off_flags + (a == DqAlgo::kOrdered ? round256(vec / 32) : 0);
@@ -707,6 +708,7 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGNMENT;
   if ((rc = check_device_ptrs({q, k, v, o, lse, cu_seqlens, alibi_slopes}))) return rc;
+  if ((rc = bind_device_context())) return rc;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -741,6 +743,7 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
     return FA_ERR_WORKSPACE;
   if ((rc = check_device_ptrs({q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, alibi_slopes}))) return rc;
+  if ((rc = bind_device_context())) return rc;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -756,6 +759,7 @@ int fa_varlen_bwd(const void* q, const void* k, const void* v, const void* o, co
   p.ws_nD = reinterpret_cast<float*>(ws + w.off_D);
   const DqAlgo algo = dq_algo(dtype, deterministic);
   p.ws_dq = algo == DqAlgo::kRecompute ? nullptr : reinterpret_cast<float*>(ws + w.off_dq);
+  p.unit_ctr = reinterpret_cast<unsigned int*>(ws + w.off_ctr);
   if (algo == DqAlgo::kOrdered) {
     p.dq_flags = reinterpret_cast<unsigned int*>(ws + w.off_flags);
     p.dq_ticket = reinterpret_cast<unsigned int*>(ws + w.off_ticket);

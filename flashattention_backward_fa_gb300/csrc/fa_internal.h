@@ -47,6 +47,11 @@ struct AttnParams {
   // zeroed by the preprocess.
   unsigned int* dq_flags;
   unsigned int* dq_ticket;
+  // Persistent backward kernels (null: units in a fixed stride over the grid):
+  // four counters in the workspace, zeroed by the preprocess: [0] the next unit
+  // ticket and [1] the CTAs done of the key/value-major kernel, [2], [3] the
+  // same for the query-major dQ kernel. The last CTA of a launch resets its pair.
+  unsigned int* unit_ctr;
   unsigned int* status;   // device status word (timeout bits)
   // Packed variable-length input (null cu_seqlens otherwise): the tensors are
   // [total, H, d] (B = 1, N = total), sequence s occupies packed rows

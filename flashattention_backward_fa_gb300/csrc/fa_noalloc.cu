@@ -5,11 +5,12 @@
 // allocations, runtimes that record work before any allocator exists, or
 // embedding environments that hand over only the tensors themselves. For them
 // this entry point takes the scratch it needs (the per-row D and L*log2(e)
-// vectors of the deterministic backward) from one fixed device array that is
+// vectors of the deterministic backward and four unit counters of its
+// persistent kernels) from one fixed device array that is
 // part of this library's module, so the call allocates nothing.
 //
 // Limits and sharing:
-//  * The array holds kNoAllocScratchBytes (8 MiB): B*H*roundup(N,128) must not
+//  * The array holds kNoAllocScratchBytes (8 MiB + 256 bytes): B*H*roundup(N,128) must not
 //    exceed 1,048,576 rows. Larger problems are rejected with FA_ERR_WORKSPACE
 //    before anything is launched; use fa_bwd with a workspace for them.
 //  * Every GPU that loads the library holds the array until the process exits.
@@ -31,7 +32,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 8u << 20;
+constexpr size_t kNoAllocScratchBytes = (8u << 20) + 256u;
 constexpr int kMaxDevicesNoAlloc = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

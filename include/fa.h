@@ -48,7 +48,7 @@
  *
  * Ownership and execution. The caller owns every buffer, and no call
  * allocates device memory. The library does hold a little module state per
- * device: the device status word (see fa_get_device_status), the fixed 8 MiB
+ * device: the device status word (see fa_get_device_status), the fixed 8 MiB (+256 B)
  * scratch array of fa_bwd_noalloc (shared by all of its calls, which keeps the
  * last call's contents; see its declaration), and, created on first use, one
  * side stream with two events for the deterministic fa_bwd and two copy
@@ -172,8 +172,9 @@ int fa_bwd_stage(fa_bwd_stage_id stage, const void* q, const void* k, const void
  * embedding that hands over only the tensors). The pages describe no such
  * entry point; it is this library's own. Arguments as fa_bwd, without the
  * deterministic flag (always FA_DQ_RECOMPUTE) and without a workspace: the
- * scratch (D and lse*log2(e) vectors) lives in one fixed 8 MiB device array
- * inside the library, so the call allocates nothing. Limit:
+ * scratch (D and lse*log2(e) vectors, four unit counters) lives in one fixed
+ * device array of 8 MiB + 256 bytes inside the library, so the call allocates
+ * nothing. Limit:
  * B*H*roundup(N,128) <= 1048576; larger problems return FA_ERR_WORKSPACE and
  * launch nothing. All calls on a device share the array (each call overwrites
  * what it reads, nothing needs clearing); calls that overlap on the GPU race,

@@ -49,9 +49,10 @@ def _rows(N):
 def test_workspace_size(lib, B, H, N, d):
     r = B * H * _rows(N)
     vec = (r * 4 + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, True) == 2 * vec
-    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, False) == 2 * vec + (r * d * 4 + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, N, d, F32, False) == 2 * vec  # fp32 never accumulates dQ atomically
+    ctr = 256  # the persistent kernels' unit counters
+    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, True) == 2 * vec + ctr
+    assert fa.fa_bwd_workspace_size(B, H, N, d, BF16, False) == 2 * vec + ctr + (r * d * 4 + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, N, d, F32, False) == 2 * vec + ctr  # fp32 never accumulates dQ atomically
     assert fa.fa_bwd_workspace_size(0, H, N, d, BF16, True) == 0
     assert fa.fa_bwd_workspace_size(B, H, N, 129, BF16, True) == 0
 
@@ -218,9 +219,10 @@ def test_varlen_workspace_size(lib):
     nseq, msl, total, H, d = 3, 300, 700, 4, 128
     vec = H * nseq * 384 * 4
     vec = (vec + 255) // 256 * 256
-    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, BF16, True) == 2 * vec
+    ctr = 256  # the persistent kernels' unit counters
+    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, BF16, True) == 2 * vec + ctr
     acc = H * (768 + 128) * d * 4
-    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, F16, False) == 2 * vec + acc
+    assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, F16, False) == 2 * vec + ctr + acc
     assert fa.fa_varlen_bwd_workspace_size(nseq, msl, total, H, d, F32, True) == 0
     assert fa.fa_varlen_bwd_workspace_size(0, msl, total, H, d, BF16, True) == 0
 

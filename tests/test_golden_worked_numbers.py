@@ -51,12 +51,14 @@ def test_printed_figures_follow_from_the_sizes():
 
 def test_library_keeps_linear_state(lib):
     """What the backward holds besides the inputs is O, L and the workspace; it
-    grows linearly in N and stays within 2% of the page's O + L + D."""
+    grows linearly in N (plus a constant block) and stays within 2% of the
+    page's O + L + D."""
     rows, _ = _fixture()
     d = 128
     for N, p_printed, saved_printed, ratio_printed in rows:
         ws = fa.fa_bwd_workspace_size(1, 1, N, d, fa.FA_BF16, True)
-        assert ws == 2 * 4 * ((N + 127) // 128 * 128)  # -L*log2(e) and -D, fp32, padded rows
+        # -L*log2(e) and -D, fp32, padded rows, plus a constant 256-byte block of unit counters
+        assert ws == 2 * 4 * ((N + 127) // 128 * 128) + 256
         ours = N * d * 2 + N * 4 + ws                    # O + L + workspace
         page = N * d * 2 + N * 4 * 2
         assert ours <= 1.02 * page

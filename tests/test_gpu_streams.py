@@ -84,3 +84,35 @@ def test_two_host_threads_two_streams_bit_identical():
     for res in out["b"]:
         for x, y in zip(r2, res):
             assert torch.equal(x, y)
+
+
+def test_calls_from_a_fresh_host_thread():
+    """A thread whose first CUDA work is a library call (no context bound to it
+    yet) gets the same forward and backward as the main thread: the entry points
+    bind the device's context before encoding their tensor maps."""
+    q, k, v, o, do, lse = _setup()
+    ref = _bwd((q, k, v, o, do, lse), torch.cuda.current_stream())[:3]
+    torch.cuda.synchronize()
+    out = {}
+
+    def worker():
+        try:
+            o2 = torch.empty_like(o)
+            lse2 = torch.empty_like(lse)
+            fa.fa_fwd(q, k, v, o2, lse2, causal=True)
+            dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+            ws = fa.alloc_workspace(q, True)
+            fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, causal=True, deterministic=True)
+            torch.cuda.synchronize()
+            out["r"] = (o2, lse2, dq, dk, dv)
+        except Exception as e:  # reported in the main thread
+            out["e"] = e
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "e" not in out, out.get("e")
+    o2, lse2, dq, dk, dv = out["r"]
+    assert torch.equal(o2, o) and torch.equal(lse2, lse)
+    for a, b in zip((dq, dk, dv), ref):
+        assert torch.equal(a, b)
