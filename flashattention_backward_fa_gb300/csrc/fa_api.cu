@@ -13,7 +13,7 @@
 #include "fa_internal.h"
 
 namespace fa {
-cudaError_t launch_preprocess(const AttnParams& p, int dtype, const CUtensorMap* maps, cudaStream_t st);
+cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st);
 cudaError_t launch_dq_convert(const AttnParams& p, int dtype, cudaStream_t st);
 cudaError_t launch_fwd_f32(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_bwd_dkdv_f32(const AttnParams& p, cudaStream_t st);
@@ -273,14 +273,7 @@ bool make_dq_accum_map(CUtensorMap* m, const AttnParams& p) {
 // Launches one backward stage for fully validated and filled parameters.
 int launch_stage(fa_bwd_stage_id stage, const AttnParams& p, int dtype, int deterministic, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (stage == FA_BWD_PREPROCESS) {
-    // 16-bit tensors with d in {64, 128}: O and dO stream through shared memory in 64-row TMA boxes
-    CUtensorMap maps[2];
-    if (dtype != FA_F32 && (p.d == 64 || p.d == 128) &&
-        (!make_map(&maps[0], p.o, p, dtype == FA_BF16, 64) || !make_map(&maps[1], p.dout, p, dtype == FA_BF16, 64)))
-      return FA_ERR_CUDA;
-    return cuda_rc(fa::launch_preprocess(p, dtype, maps, st));
-  }
+  if (stage == FA_BWD_PREPROCESS) return cuda_rc(fa::launch_preprocess(p, dtype, st));
   if (dtype == FA_F32)
     return cuda_rc(stage == FA_BWD_DKDV ? fa::launch_bwd_dkdv_f32(p, st) : fa::launch_bwd_dq_f32(p, st));
   const bool bf16 = dtype == FA_BF16;

@@ -106,12 +106,15 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __grid_constant__
   }
 }
 
-// Helpers of the 16-bit kernels with d in {64, 128}: a group of d/8 lanes owns
-// one row and each lane handles 8 elements (16 bytes), so a warp covers whole
-// 128-byte lines.
+// 16-bit tensors with d in {64, 128}: a group of d/8 lanes owns one row and
+// each lane reads 16 bytes of O and of dO, so a warp moves whole 128-byte lines.
+// Rows are enumerated in [B*H, n_pad] order (positions fastest), which keeps
+// the workspace vectors and L contiguous (measured faster than streaming the
+// [B, N, H, d] tensors front to back); every thread takes kVecRows rows and
+// issues all of their loads before reducing, to keep enough bytes in flight.
 constexpr int kVecRows = 4;
 
-// Rows of one (batch, head) per block of the dQ conversion: 8 warps x (32 / (d/8)) rows x kVecRows.
+// Rows of one (batch, head) per block: 8 warps x (32 / (d/8)) rows x kVecRows.
 template <int D>
 constexpr int vec_block_rows() { return 8 * (32 / (D / 8)) * kVecRows; }
 
@@ -135,169 +138,66 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b, float acc)
   return acc;
 }
 
-// Preprocess of 16-bit tensors with d in {64, 128}, staged through shared
-// memory by TMA. The work is cut into chunks of kPreRows consecutive positions
-// of one (batch, head) (or (sequence, head)); chunk c is unit c % units,
-// position block c / units, so the chunks in flight at any moment cover every
-// head of one contiguous range of positions (a [B, N, H, d] tensor is read
-// front to back, whole DRAM pages at a time). The grid is persistent, one
-// block per SM: one thread streams the O and dO tiles of the block's chunks
-// into a ring of kNS stages (192 KB in flight per SM), and sixteen warps reduce
-// each staged chunk in one pass, eight lanes a row (each lane d/8 elements of
-// O and of dO, three shuffles), then store -D and -L*log2e (and the zero fills
-// of the accumulating dQ modes).
-constexpr int kPreRows = 64;    // positions per chunk (one TMA box of rows)
-constexpr int kPreWarps = 16;   // reducing warps (8 lanes a row); one more warp issues the loads
-constexpr int kPreThreads = 32 * (kPreWarps + 1);
-static_assert(kPreWarps * 32 == 8 * kPreRows, "one reducing pass covers a chunk");
-
-template <int D>
-struct PreCfg {
-  static constexpr int kPanels = D / 64;
-  static constexpr uint32_t kPanel = kPreRows * 128;     // 64 rows x 64 elements, 128-byte swizzle
-  static constexpr uint32_t kTile = kPanels * kPanel;    // one tensor's chunk
-  static constexpr uint32_t kStage = 2 * kTile;          // O then dO
-  static constexpr int kNS = (int)((192u * 1024u) / kStage);
-  static constexpr uint32_t oBar = kNS * kStage;         // full[kNS], empty[kNS]
-  static constexpr uint32_t oAbort = oBar + 16u * kNS;
-  static constexpr uint32_t kSmem = oAbort + 16 + 1024;  // + slack for 1024-byte alignment
-  static_assert(kSmem <= 227u * 1024u, "shared memory budget exceeded");
-};
-
-// units: B*H (or nseq*H); nchunks = units * (padded rows per unit / kPreRows).
+// Grid: x = block of vec_block_rows<D>() positions, y = batch * head.
 template <typename T, int D>
-__global__ void __launch_bounds__(kPreThreads, 1)
-    preprocess_tma_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmO,
-                          const __grid_constant__ CUtensorMap tmDO, int units, long long nchunks) {
-  using C = PreCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const uint32_t sb = smem_u32(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::oAbort);
-  auto full = [&](int s) -> uint32_t { return sb + C::oBar + 8u * s; };
-  auto empty = [&](int s) -> uint32_t { return sb + C::oBar + 8u * (C::kNS + s); };
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kNS; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), kPreWarps);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-    if (blockIdx.x == 0) {
-      if (p.dq_ticket != nullptr) *p.dq_ticket = 0u;
-      if (p.unit_ctr != nullptr)
-        for (int x = 0; x < 4; ++x) p.unit_ctr[x] = 0u;
+__global__ void __launch_bounds__(256) preprocess_vec_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int G = D / 8;            // lanes per row
+  constexpr int kRowsPerWarp = 32 / G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ib = blockIdx.x * vec_block_rows<D>() + warp * (kRowsPerWarp * kVecRows) + lane / G;
+  const int e0 = (lane % G) * 8;
+  // y = batch * head, or sequence * head for packed variable-length input; rows
+  // below are local to it (n of them, padded to `pad` workspace rows).
+  int bh, row0 = 0, n = p.N, pad = p.n_pad;
+  long long ws0, lse0;
+  if (p.cu_seqlens == nullptr) {
+    bh = blockIdx.y;
+    ws0 = (long long)bh * p.n_pad;
+    lse0 = (long long)bh * p.N;
+  } else {
+    const int sq = blockIdx.y / p.H, h = blockIdx.y % p.H;
+    const int s0 = min(max(p.cu_seqlens[sq], 0), p.N), s1 = min(max(p.cu_seqlens[sq + 1], s0), p.N);
+    bh = h;  // B = 1
+    row0 = s0;
+    n = min(s1 - s0, p.max_seqlen);
+    pad = p.seq_pad;
+    ws0 = ((long long)h * p.nseq + sq) * p.seq_pad;
+    lse0 = (long long)h * p.N + s0;
+  }
+  const T* o = static_cast<const T*>(p.o) + (long long)(bh / p.H) * p.sb + (long long)(bh % p.H) * p.sh +
+               (long long)row0 * p.sn + e0;
+  const T* g = static_cast<const T*>(p.dout) + (o - static_cast<const T*>(p.o));
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    if (p.dq_ticket != nullptr) *p.dq_ticket = 0u;
+    if (p.unit_ctr != nullptr)
+      for (int x = 0; x < 4; ++x) p.unit_ctr[x] = 0u;
+  }
+  uint4 ov[kVecRows], gv[kVecRows];
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const int i = ib + r * kRowsPerWarp;
+    ov[r] = gv[r] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < n) {
+      ov[r] = __ldg(reinterpret_cast<const uint4*>(o + (long long)i * p.sn));
+      gv[r] = __ldg(reinterpret_cast<const uint4*>(g + (long long)i * p.sn));
     }
   }
-  __syncthreads();
-  // Chunk c: unit y (batch * head, or sequence * head for packed input) and
-  // its first position i0; rows are local to the unit, n of them, padded to
-  // `pad` workspace rows starting at ws0.
-  struct Chunk {
-    int y, i0, b, h, row0, n, pad;
-    long long ws0, lse0;
-  };
-  auto decode = [&](long long c) {
-    Chunk k;
-    k.y = (int)(c % units);
-    k.i0 = (int)(c / units) * kPreRows;
-    if (p.cu_seqlens == nullptr) {
-      k.b = k.y / p.H;
-      k.h = k.y % p.H;
-      k.row0 = 0;
-      k.n = p.N;
-      k.pad = p.n_pad;
-      k.ws0 = (long long)k.y * p.n_pad;
-      k.lse0 = (long long)k.y * p.N;
-    } else {
-      const int sq = k.y / p.H;
-      k.h = k.y % p.H;
-      k.b = 0;
-      const int s0 = min(max(p.cu_seqlens[sq], 0), p.N), s1 = min(max(p.cu_seqlens[sq + 1], s0), p.N);
-      k.row0 = s0;
-      k.n = min(s1 - s0, p.max_seqlen);
-      k.pad = p.seq_pad;
-      k.ws0 = ((long long)k.h * p.nseq + sq) * p.seq_pad;
-      k.lse0 = (long long)k.h * p.N + s0;
+#pragma unroll
+  for (int r = 0; r < kVecRows; ++r) {
+    const int i = ib + r * kRowsPerWarp;
+    const float acc = group_sum<D>(dot8<T>(ov[r], gv[r], 0.f));
+    if (i >= pad) continue;
+    if (e0 == 0) {
+      p.ws_nD[ws0 + i] = -acc;
+      p.ws_nL2[ws0 + i] = (i < n) ? neg_l2(p.lse[lse0 + i]) : __int_as_float(0xff800000);
+      // ordered dQ: the contribution counter of each 32-row chunk starts at 0
+      if (p.dq_flags != nullptr && (i & 31) == 0) p.dq_flags[(long long)blockIdx.y * (pad / 32) + i / 32] = 0u;
     }
-    return k;
-  };
-
-  if (warp == kPreWarps) {
-    // ------------------------------ TMA producer ------------------------------
-    if (lane == 0) {
-      prefetch_tmap(&tmO);
-      prefetch_tmap(&tmDO);
-      int t = 0, issued = 0;
-      for (long long c = blockIdx.x; c < nchunks; c += gridDim.x, ++t) {
-        const int s = t % C::kNS;
-        if (!mbar_wait(empty(s), ((t / C::kNS) & 1) ^ 1, abort_flag, p.status)) break;
-        const Chunk k = decode(c);
-        // Rows past the unit's end read zeros past the tensor, or the next
-        // sequence's rows of packed input (in bounds); the reducers ignore them.
-        mbar_arrive_expect_tx(full(s), C::kStage);
-        const uint32_t st = sb + s * C::kStage;
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_load_4d(st + pn * C::kPanel, &tmO, full(s), 64 * pn, k.row0 + k.i0, k.h, k.b);
-          tma_load_4d(st + C::kTile + pn * C::kPanel, &tmDO, full(s), 64 * pn, k.row0 + k.i0, k.h, k.b);
-        }
-        issued = t + 1;
-      }
-      if (*abort_flag) {
-        // Let every copy this thread started land before the block exits.
-        for (int x = max(0, issued - C::kNS); x < issued; ++x)
-          mbar_wait_drain(full(x % C::kNS), (x / C::kNS) & 1, p.status);
-      }
-    }
-  } else {
-    // ------------------------------- reducers --------------------------------
-    // Thread t of the reducers owns row t / 8 of a chunk and its 16-byte pieces
-    // kCPT * (t % 8) .. + kCPT - 1 (both in one 64-element panel). In a
-    // 128-byte-swizzled panel piece x of row r sits at slot (x % 8) ^ (r & 7).
-    constexpr int kCPT = D / 64;          // 16-byte pieces per lane and tensor
-    const int r = threadIdx.x >> 3;       // row within the chunk
-    const int part = threadIdx.x & 7;
-    const int x0 = kCPT * part;           // first piece
-    const uint32_t row_off = (uint32_t)(x0 / 8) * C::kPanel + (uint32_t)r * 128;
-    int t = 0;
-    for (long long c = blockIdx.x; c < nchunks; c += gridDim.x, ++t) {
-      const int s = t % C::kNS;
-      const Chunk k = decode(c);
-      const int i = k.i0 + r;  // < k.pad: chunks tile the padded rows exactly
-      // this row's L, loaded before the wait so that its latency overlaps it
-      const float lse_i = (part == 0 && i < k.n) ? p.lse[k.lse0 + i] : 0.f;
-      if (!warp_wait<kRowMathPoll>(full(s), (t / C::kNS) & 1, abort_flag, p.status)) break;
-      const uint32_t st = sb + s * C::kStage + row_off;
-      uint4 ov[kCPT], gv[kCPT];
-#pragma unroll
-      for (int x = 0; x < kCPT; ++x) {
-        const uint32_t at = st + ((uint32_t)(((x0 + x) % 8) ^ (r & 7)) << 4);
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(ov[x].x), "=r"(ov[x].y), "=r"(ov[x].z), "=r"(ov[x].w) : "r"(at));
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(gv[x].x), "=r"(gv[x].y), "=r"(gv[x].z), "=r"(gv[x].w) : "r"(at + C::kTile));
-      }
-      float acc = 0.f;
-#pragma unroll
-      for (int x = 0; x < kCPT; ++x) acc = dot8<T>(ov[x], gv[x], acc);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      if (part == 0) {
-        p.ws_nD[k.ws0 + i] = i < k.n ? -acc : -0.f;
-        p.ws_nL2[k.ws0 + i] = i < k.n ? neg_l2(lse_i) : __int_as_float(0xff800000);
-        // ordered dQ: the contribution counter of each 32-row chunk starts at 0
-        if (p.dq_flags != nullptr && (i & 31) == 0) p.dq_flags[(long long)k.y * (k.pad / 32) + i / 32] = 0u;
-      }
-      // accumulating dQ modes (packed input: the accumulator is zeroed separately)
-      if (p.ws_dq != nullptr && p.cu_seqlens == nullptr) {
-        float4* dq = reinterpret_cast<float4*>(p.ws_dq + (k.ws0 + i) * D + 8 * x0);
-#pragma unroll
-        for (int x = 0; x < 2 * kCPT; ++x) dq[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(s));
+    // (packed input: the dQ accumulator is zeroed separately)
+    if (p.ws_dq != nullptr && p.cu_seqlens == nullptr) {
+      float4* dq = reinterpret_cast<float4*>(p.ws_dq + (ws0 + i) * D + e0);
+      dq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -573,33 +473,22 @@ static inline unsigned grid_for_rows_strided(long long rows, int rows_per_block)
   return (unsigned)(g < (1ll << 20) ? (g > 0 ? g : 1) : (1ll << 20));
 }
 
-template <typename T, int D>
-static cudaError_t launch_preprocess_tma(const AttnParams& p, const CUtensorMap* maps, cudaStream_t st) {
-  using C = PreCfg<D>;
-  auto kern = preprocess_tma_kernel<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int prow = p.cu_seqlens ? p.seq_pad : p.n_pad;  // a multiple of kPadRows, hence of kPreRows
-  const int units = p.cu_seqlens ? p.nseq * p.H : p.B * p.H;
-  const long long nchunks = (long long)units * (prow / kPreRows);
-  const long long grid = nchunks < sms ? nchunks : sms;
-  kern<<<(unsigned)(grid > 0 ? grid : 1), kPreThreads, C::kSmem, st>>>(p, maps[0], maps[1], units, nchunks);
-  return cudaGetLastError();
-}
-
-// maps: O and dO with boxes of kPreRows rows (16-bit tensors with d in {64, 128}); unused otherwise.
-cudaError_t launch_preprocess(const AttnParams& p, int dtype, const CUtensorMap* maps, cudaStream_t st) {
-  if (dtype != 0 && (p.d == 64 || p.d == 128)) {
-    if (p.d == 128)
-      return dtype == 1 ? launch_preprocess_tma<__half, 128>(p, maps, st)
-                        : launch_preprocess_tma<__nv_bfloat16, 128>(p, maps, st);
-    return dtype == 1 ? launch_preprocess_tma<__half, 64>(p, maps, st)
-                      : launch_preprocess_tma<__nv_bfloat16, 64>(p, maps, st);
-  }
+cudaError_t launch_preprocess(const AttnParams& p, int dtype, cudaStream_t st) {
   const long long rows = (long long)p.B * p.n_pad * p.H;
+  // packed variable-length input: y = sequence * head, x over seq_pad rows
+  const int prow = p.cu_seqlens ? p.seq_pad : p.n_pad;
+  const int units = p.cu_seqlens ? p.nseq * p.H : p.B * p.H;
+  if (dtype != 0 && (p.d == 64 || p.d == 128) && units <= 65535) {
+    const dim3 g((unsigned)((prow + vec_block_rows<128>() - 1) / vec_block_rows<128>()), (unsigned)units);
+    const dim3 g64((unsigned)((prow + vec_block_rows<64>() - 1) / vec_block_rows<64>()), (unsigned)units);
+    if (p.d == 128)
+      dtype == 1 ? preprocess_vec_kernel<__half, 128><<<g, 256, 0, st>>>(p)
+                 : preprocess_vec_kernel<__nv_bfloat16, 128><<<g, 256, 0, st>>>(p);
+    else
+      dtype == 1 ? preprocess_vec_kernel<__half, 64><<<g64, 256, 0, st>>>(p)
+                 : preprocess_vec_kernel<__nv_bfloat16, 64><<<g64, 256, 0, st>>>(p);
+    return cudaGetLastError();
+  }
   const unsigned grid = grid_for_rows_strided(rows, 8);
   if (dtype == 0) preprocess_kernel<float><<<grid, 256, 0, st>>>(p);
   else if (dtype == 1) preprocess_kernel<__half><<<grid, 256, 0, st>>>(p);
