@@ -22,6 +22,8 @@ cudaError_t launch_bwd_dkdv_tc(const AttnParams& p, bool bf16, bool atomic, cons
                                cudaStream_t st);
 cudaError_t launch_qmajor_tc(const AttnParams& p, bool bf16, bool dq_mode, const CUtensorMap* maps,
                              cudaStream_t st);
+bool fwd_pingpong_supported(const AttnParams& p);
+cudaError_t launch_fwd_pingpong(const AttnParams& p, bool bf16, const CUtensorMap* maps, cudaStream_t st);
 }  // namespace fa
 
 namespace {
@@ -502,6 +504,8 @@ int fwd_run(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], v, p, bf16, fa::kStepKV))
     return FA_ERR_CUDA;
+  // the common case (no dropout, ALiBi, bias or window): two query tiles per CTA in ping-pong
+  if (fa::fwd_pingpong_supported(p)) return cuda_rc(fa::launch_fwd_pingpong(p, bf16, maps, st));
   maps[3] = maps[0];
   if (p.bias ? !make_bias_map(&maps[4], p, bf16, true) : false) return FA_ERR_CUDA;
   if (!p.bias) maps[4] = maps[0];  // unused
@@ -713,6 +717,7 @@ int fa_varlen_fwd(const void* q, const void* k, const void* v, void* o, float* l
   if (!make_map(&maps[0], q, p, bf16, fa::kRowsQ) || !make_map(&maps[1], k, p, bf16, fa::kStepKV) ||
       !make_map(&maps[2], v, p, bf16, fa::kStepKV))
     return FA_ERR_CUDA;
+  if (fa::fwd_pingpong_supported(p)) return cuda_rc(fa::launch_fwd_pingpong(p, bf16, maps, static_cast<cudaStream_t>(stream)));
   maps[3] = maps[0];
   maps[4] = maps[0];  // no attention bias on packed input
   return cuda_rc(fa::launch_qmajor_tc(p, bf16, false, maps, static_cast<cudaStream_t>(stream)));
