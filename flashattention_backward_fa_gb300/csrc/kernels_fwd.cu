@@ -29,16 +29,17 @@
 // more than 2^8 (so probabilities relative to a stale reference stay below 2^8);
 // then the row of O is rescaled in TMEM after that tile's previous O MMA.
 //
-// Warp roles (640 threads): warp 0 issues TMA loads (Q_A, Q_B once; K and V
-// per key block into rings), warp 1 owns TMEM and issues every MMA, warps 2-3
-// only take part in setup; warps 4-11 are tile A's softmax warps (4-7 the first
-// 64 keys of each block, 8-11 the last 64), warps 12-19 tile B's. This path serves 16-bit inputs with d in {64, 128}, fixed-length or
+// Warp roles (576 threads): warp 0 issues TMA loads (Q_A, Q_B once; K and V
+// per key block into rings), warp 1 owns TMEM and issues every MMA; warps 2-9
+// are tile A's softmax warps (2-5 the first 64 keys of each block, 6-9 the last
+// 64), warps 10-17 tile B's. A warp reaches the TMEM lanes of its quarter
+// (warp % 4), so the two warps of a row share a scheduler. This path serves 16-bit inputs with d in {64, 128}, fixed-length or
 // packed sequences, without dropout, ALiBi, an attention bias or a window.
 #include "fa_internal.h"
 
 namespace fa {
 
-constexpr int kFwdThreads = 640;
+constexpr int kFwdThreads = 576;
 constexpr int kFwdRows = 256;  // queries per CTA (two 128-row tiles)
 // The reference maximum of a row moves only when a block's maximum exceeds it
 // by more than this (log2 units), bounding relative probabilities by 2^8.
@@ -270,10 +271,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_commit_w(bar(C::bDrain));
     if (lane == 0) mbar_wait_drain(bar(C::bDrain), 0, p.status);
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------ softmax warps ------------------------------
-    const int x = (warp - 4) >> 3;         // tile
-    const int half = ((warp - 4) >> 2) & 1;  // keys [64 half, 64 half + 64) of a block
+    // warps 2-17; a warp reaches TMEM lanes 32 (warp % 4) .. + 31
+    const int x = (warp - 2) >> 3;         // tile
+    const int half = ((warp - 2) >> 2) & 1;  // keys [64 half, 64 half + 64) of a block
     const int wq = warp & 3;
     const int il = wq * 32 + lane;  // row in the tile, TMEM lane
     const int i = q0 + 128 * x + il;
@@ -369,15 +371,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // final row sum, so the bound holds for the final P); zeros otherwise.
       const uint64_t cc2 = f2_pack(c2, c2), nm2 = f2_pack(-mref, -mref);
       bool split = false;
-      uint32_t r[2][32];  // chunk q in r[q]; chunk 1 loads while chunk 0 is computed
-      __syncwarp();
-      tmem_ld32(tS, r[0]);
-      tmem_ld32(tS + 32, r[1]);
-      tmem_ld_wait(r[0]);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        uint32_t (&cur)[32] = r[q];
-        if (q == 1) tmem_ld_wait(r[1]);
+        uint32_t cur[32];
+        __syncwarp();
+        tmem_ld32(tS + 32 * q, cur);
+        tmem_ld_wait(cur);
         uint64_t sum2 = f2_pack(0.f, 0.f);
         float cm0 = 0.f, cm1 = 0.f;
         if (hi >= 64) {
