@@ -410,16 +410,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         lsum += s0 + s1;
         const bool sp = __any_sync(0xffffffffu, fmaxf(cm0, cm1) > kSplitThreshold * lsum);
         split |= sp;
+        // (sp is warp-uniform: a real branch, the residuals are computed only when needed)
+        if (sp) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          uint32_t w[16];
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[16];
 #pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float a = __uint_as_float(cur[16 * k + 2 * t]), c = __uint_as_float(cur[16 * k + 2 * t + 1]);
-            w[t] = pack2<kBf16>(a, c);
-            w[8 + t] = sp ? pack2_residual<kBf16>(a, c, w[t]) : 0u;
+            for (int t = 0; t < 8; ++t) {
+              const float a = __uint_as_float(cur[16 * k + 2 * t]), c = __uint_as_float(cur[16 * k + 2 * t + 1]);
+              w[t] = pack2<kBf16>(a, c);
+              w[8 + t] = pack2_residual<kBf16>(a, c, w[t]);
+            }
+            tmem_st16(tS + 32 * q + 16 * k, w);
           }
-          tmem_st16(tS + 32 * q + 16 * k, w);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t w[16];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              w[t] = pack2<kBf16>(__uint_as_float(cur[16 * k + 2 * t]), __uint_as_float(cur[16 * k + 2 * t + 1]));
+              w[8 + t] = 0u;
+            }
+            tmem_st16(tS + 32 * q + 16 * k, w);
+          }
         }
       }
       tmem_st_wait();
