@@ -366,10 +366,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // Pass 2, 32 keys at a time: P = exp2(S * scale * log2e - mref) (0 where
       // masked), this half's running sum, and the 16-bit image of the two MMA K
-      // steps over the same columns. A chunk writes residual columns where a
-      // probability may exceed 1/64 of this half's sum so far (a part of the
-      // final row sum, so the bound holds for the final P); zeros otherwise.
+      // steps over the same columns. A chunk writes residual columns where the
+      // block's largest probability may exceed 1/64 of this half's sum so far (a
+      // part of the final row sum, so the bound holds for the final P); zeros
+      // otherwise.
       const uint64_t cc2 = f2_pack(c2, c2), nm2 = f2_pack(-mref, -mref);
+      // the largest P of this block for this row (its block maximum against the reference)
+      const float pmax = ex2_approx(bmax - mref);
       bool split = false;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -378,7 +381,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld32(tS + 32 * q, cur);
         tmem_ld_wait(cur);
         uint64_t sum2 = f2_pack(0.f, 0.f);
-        float cm0 = 0.f, cm1 = 0.f;
         if (hi >= 64) {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -386,7 +388,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])), cc2, nm2), p0, p1);
             p0 = ex2_approx(p0);
             p1 = ex2_approx(p1);
-            if (e & 2) cm1 = fmax3(cm1, p0, p1); else cm0 = fmax3(cm0, p0, p1);
             sum2 = f2_add(sum2, f2_pack(p0, p1));
             cur[e] = __float_as_uint(p0);
             cur[e + 1] = __float_as_uint(p1);
@@ -398,7 +399,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])), cc2, nm2), p0, p1);
             p0 = (32 * q + e < hi) ? ex2_approx(p0) : 0.f;
             p1 = (32 * q + e + 1 < hi) ? ex2_approx(p1) : 0.f;
-            if (e & 2) cm1 = fmax3(cm1, p0, p1); else cm0 = fmax3(cm0, p0, p1);
             sum2 = f2_add(sum2, f2_pack(p0, p1));
             cur[e] = __float_as_uint(p0);
             cur[e + 1] = __float_as_uint(p1);
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float s0, s1;
         f2_unpack(sum2, s0, s1);
         lsum += s0 + s1;
-        const bool sp = __any_sync(0xffffffffu, fmaxf(cm0, cm1) > kSplitThreshold * lsum);
+        const bool sp = __any_sync(0xffffffffu, pmax > kSplitThreshold * lsum);
         split |= sp;
         // (sp is warp-uniform: a real branch, the residuals are computed only when needed)
         if (sp) {
