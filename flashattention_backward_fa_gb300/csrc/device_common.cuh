@@ -633,7 +633,7 @@ static __device__ __forceinline__ uint32_t keep_bits_for_key(const DropoutParams
   const uint64_t n8 = (uint64_t)((N + 7) >> 3);
   const uint64_t row0 = (uint64_t)(bh + dp.bh_off) * (uint64_t)N;
   uint32_t mine = 0;  // byte t: keep bits of the group's eight keys for query i0 + 8t + r
-#pragma unroll 1
+#pragma unroll
   for (int t = 0; t < 4; ++t)
     mine |= keep_byte(philox_at(dp, (row0 + (uint64_t)(i0 + 8 * t + r)) * n8 + (uint64_t)(j >> 3)), dp.threshold)
             << (8 * t);
@@ -656,7 +656,7 @@ static __device__ __noinline__ uint32_t keep_bits_for_query(const DropoutParams 
   const uint64_t n8 = (uint64_t)((N + 7) >> 3);
   const uint64_t g0 = ((uint64_t)(bh + dp.bh_off) * (uint64_t)N + (uint64_t)i) * n8 + (uint64_t)(j0 >> 3);
   uint32_t bits = 0;
-#pragma unroll 1
+#pragma unroll
   for (int x = 0; x < 4; ++x) bits |= keep_byte(philox_at(dp, g0 + (uint64_t)x), dp.threshold) << (8 * x);
   return bits;
 }

@@ -614,16 +614,10 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           const int gs = G + it;
           const int s = gs % C::kNS;
           const int i0 = step_i0(it);
-          if (!warp_wait<kRowMathPoll>(bar(C::bQFull + s), (gs / C::kNS) & 1, abort_flag, p.status) ||
-              !warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (gs >> 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * kStepQ * 4 + 128 * c);
-        const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + s * kStepQ * 4 + 128 * c);
         const int base = i0 + 32 * c;
-        // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep bits
+        // allowed pairs of this chunk (bit x <-> query base + x) and dropout keep
+        // bits: both depend on positions only, so they are formed before the waits
+        // and the Philox calls overlap the loads and MMAs of this step.
         uint32_t allow = 0u;
         if (j < Nl) {
           const int lo = p.causal ? j - base : 0;
@@ -636,6 +630,14 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
           __syncwarp();  // warp-collective (shuffles)
           keep = keep_bits_for_key(p.drop, bh, Nl, base, j);
         }
+          if (!warp_wait<kRowMathPoll>(bar(C::bQFull + s), (gs / C::kNS) & 1, abort_flag, p.status) ||
+              !warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (gs >> 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        const float4* L4 = reinterpret_cast<const float4*>(smem + C::oL + s * kStepQ * 4 + 128 * c);
+        const float4* D4 = reinterpret_cast<const float4*>(smem + C::oD + s * kStepQ * 4 + 128 * c);
         float P[32];          // P (before dropout) of this thread's 32 pairs, for the dS phase
         bool split_h[2];
         // ---- phase 1: P~T image over the S^T columns ----

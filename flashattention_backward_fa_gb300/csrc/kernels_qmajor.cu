@@ -556,16 +556,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
                            bw[4 * t + 2], bw[4 * t + 3]);
             warp_arrive(bar(C::bBEmpty));
           }
+          // allowed keys of this warpgroup's 32 columns (bit x <-> key base + x) and
+          // their dropout keep bits: both depend on positions only, so the Philox
+          // calls run while the S MMAs of this step are still in flight.
+          const uint32_t allow =
+              bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(Nl - base, p.causal ? i + 1 - base : 32));
+          uint32_t keep = 0xFFFFFFFFu;
+          if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, Nl, i, base);
           if (!warp_wait<kRowMathPoll>(bar(C::bSFull + bb), (gs / C::kSBuf) & 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // allowed keys of this warpgroup's 32 columns (bit x <-> key base + x)
-          const uint32_t allow =
-              bit_range(p.window > 0 ? i - p.window + 1 - base : 0, min(Nl - base, p.causal ? i + 1 - base : 32));
-          uint32_t keep = 0xFFFFFFFFu;
-          if constexpr (kDrop) keep = keep_bits_for_query(p.drop, bh, Nl, i, base);
           // dQ: both halves of this warpgroup's dP columns come in with S, so the dP
           // buffer is released (and the next dP MMAs may run) before any arithmetic.
           // Forward: all of S comes in, for the row maximum.
