@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
     for (int x = 0; x < 3; ++x) mbar_init(bar(C::bDrain + x), 1);
     mbar_init(bar(C::bAcc), 1);
     mbar_init(bar(C::bKVFree), kAtomic ? 3 : 2);               // S^T, dP^T (and dQ^T) issuers
-    mbar_init(bar(C::bAccFree), 16 * 32);                      // every row-math warp
+    mbar_init(bar(C::bAccFree), 8 * 32);                       // the epilogue pair's row-math warps
     for (int x = 0; x < kUnitSlots; ++x) {
       mbar_init(bar(C::bUnit + x), 1);
       mbar_init(bar(C::bUnitFree + x), kUnitReaders * 32);
@@ -815,50 +815,64 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
         }
         }
         if (!ok) break;
-        // Epilogue: warpgroups 0, 1 write dV and 2, 3 write scale * dK, each half
-        // of the columns. The accumulators are loaded and released (AccFree) before
-        // the stores, so the next unit's first dV / dK MMAs can start meanwhile.
-        const bool isK = rg >= 2;
-        constexpr int kChunks = D / 64;  // 32-column TMEM loads per thread
-        uint32_t r[kChunks][32];
-        if (nsteps > 0) {
-          if (!warp_wait<kRowMathPoll>(bar(C::bAcc), kl & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t col0 = (isK ? tdK : tdV) + lane_off + c * (D / 2);
-          tmem_ld32(col0, r[0]);
-          if constexpr (kChunks == 2) {
-            tmem_ld32(col0 + 32, r[1]);
-            tmem_ld_wait2(r[0], r[1]);
-          } else {
-            tmem_ld_wait(r[0]);
-          }
-          tc_fence_before();
-          warp_arrive(bar(C::bAccFree));
-          ++kl;
-        } else {
-#pragma unroll
-          for (int cc = 0; cc < kChunks; ++cc)
-#pragma unroll
-            for (int x = 0; x < 32; ++x) r[cc][x] = 0u;
-        }
-        if (j < Nl) {
+        // Epilogue, by the warpgroup pair that ran the unit's last query step (the
+        // other pair goes on to the next unit's first step meanwhile): dV, then
+        // scale * dK, each warpgroup half of the columns. dK is read out after dV's
+        // stores are issued; both accumulators are then released (AccFree) before
+        // dK's stores, so the next unit's first dV / dK MMAs can start meanwhile.
+        const bool epi = nsteps > 0 ? bb == ((G + nsteps - 1) & 1) : bb == 0;
+        if (epi) {
+          constexpr int kChunks = D / 64;  // 32-column TMEM loads per thread and accumulator
           const long long off = (long long)b * p.sb + (long long)(u.row0 + j) * p.sn + (long long)h * p.sh;
-          uint16_t* dst = static_cast<uint16_t*>(isK ? p.dk : p.dv) + off + c * (D / 2);
-          const float mul = isK ? p.scale : 1.f;
+#pragma unroll 1
+          for (int which = 0; which < 2; ++which) {
+            const bool isK = which == 1;
+            uint32_t r[kChunks][32];
+            if (nsteps > 0) {
+              if (!isK) {
+                if (!warp_wait<kRowMathPoll>(bar(C::bAcc), kl & 1, abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
+              __syncwarp();  // the stores above are per-lane: converge for the TMEM loads
+              const uint32_t col0 = (isK ? tdK : tdV) + lane_off + c * (D / 2);
+              tmem_ld32(col0, r[0]);
+              if constexpr (kChunks == 2) {
+                tmem_ld32(col0 + 32, r[1]);
+                tmem_ld_wait2(r[0], r[1]);
+              } else {
+                tmem_ld_wait(r[0]);
+              }
+              if (isK) {
+                tc_fence_before();
+                warp_arrive(bar(C::bAccFree));
+              }
+            } else {
 #pragma unroll
-          for (int cc = 0; cc < kChunks; ++cc) {
-            uint32_t w[16];
+              for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
-            for (int x = 0; x < 16; ++x)
-              w[x] = pack2<kBf16>(__uint_as_float(r[cc][2 * x]) * mul, __uint_as_float(r[cc][2 * x + 1]) * mul);
-            uint4* gp = reinterpret_cast<uint4*>(dst + 32 * cc);
+                for (int x = 0; x < 32; ++x) r[cc][x] = 0u;
+            }
+            if (j < Nl) {
+              uint16_t* dst = static_cast<uint16_t*>(isK ? p.dk : p.dv) + off + c * (D / 2);
+              const float mul = isK ? p.scale : 1.f;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) gp[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+              for (int cc = 0; cc < kChunks; ++cc) {
+                uint32_t w[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                  w[x] = pack2<kBf16>(__uint_as_float(r[cc][2 * x]) * mul, __uint_as_float(r[cc][2 * x + 1]) * mul);
+                uint4* gp = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) gp[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+              }
+            }
           }
+          if (!ok) break;
         }
+        if (nsteps > 0) ++kl;
         (void)bh;
         G += nsteps;
       }
