@@ -30,7 +30,7 @@
 // the three MMA streams are issued in parallel (one thread issues at most about
 // one MMA per 50 cycles); four row-math warpgroups (warps 4-19) take alternate
 // query steps (warpgroups 0, 1 the even ones, in TMEM buffer 0; 2, 3 the odd
-// ones) and write the dV (warpgroups 0, 1) / dK (2, 3) epilogue.
+// ones); the pair that ran a unit's last step writes its dV and dK epilogue.
 //
 // Persistent grid (deterministic kernel): one CTA per SM runs unit after unit,
 // taking the next unit from a counter in the workspace (the first one is its
@@ -41,7 +41,7 @@
 // epilogue finish. Two hand-offs separate consecutive units: the next unit's
 // K and V overwrite this unit's once its last S^T / dP^T (and dQ^T) MMAs have
 // completed (KVFree), and its first dV / dK MMAs overwrite the accumulators once
-// every row-math warp has loaded them (AccFree). The producer publishes each
+// the epilogue pair has loaded them (AccFree). The producer publishes each
 // next unit in a small ring in shared memory, read by every other role. The
 // ordered dQ mode takes its one unit from the ticket counter in launch order,
 // which its deadlock argument needs.
@@ -589,8 +589,8 @@ __global__ void __launch_bounds__(KVCfg<D, kAtomic, kBias>::kThreads, 1)
     // warpgroup rg & 1 takes query columns [32 (rg & 1), 32 (rg & 1) + 32) of
     // the step, in halves of 16 columns (one MMA K step). Each step runs in two
     // phases: P~T from S^T (released to the dV MMA at once), then dS^T from
-    // dP^T and the kept fp32 P. After a unit's steps every warp writes its part
-    // of the dV / dK epilogue.
+    // dP^T and the kept fp32 P. After a unit's steps the pair that ran its last
+    // step writes the dV / dK epilogue; the other pair goes on to the next unit.
     const int rg = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int c = rg & 1;
